@@ -1,0 +1,390 @@
+"""Pins for the fp64 oracle: it is checked against things other than itself.
+
+Each ``pin_*`` function takes an oracle module and raises AssertionError when the
+module disagrees with a closed form, an invariant, a brute-force evaluation or a
+library routine. ``test_pins_hold`` runs every pin on the real oracle;
+``test_planted_mistakes_are_caught`` plants plausible mistakes in copies of the
+oracle's source and checks that some pin fails for each one.
+"""
+import json
+import math
+import os
+import types
+
+import numpy as np
+import pytest
+
+from oracle import attention as oracle_attention
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+GOLDEN = json.load(open(os.path.join(HERE, "golden", "worked_examples.json")))
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def _visible_count(N, causal):
+    return np.arange(1, N + 1) if causal else np.full(N, N)
+
+
+# ----------------------------------------------------------------------------- pins
+def pin_probability_rows(m):
+    """Rows of P sum to one; P is in (0, 1] on visible keys and 0 on hidden ones
+    ('flash-attention-backpropagation', 显存困境 and 数值稳定)."""
+    for causal in (False, True):
+        q, k = _rand((9, 5), 1), _rand((9, 5), 2)
+        P, mx, l = m.softmax_rows(m.scores(q, k, 0.4, causal, np.arange(9)))
+        assert np.allclose(P.sum(1), 1.0, rtol=0, atol=1e-14)
+        vis = np.tril(np.ones((9, 9), bool)) if causal else np.ones((9, 9), bool)
+        assert (P[vis] > 0).all() and (P[vis] <= 1).all()
+        assert (P[~vis] == 0).all()
+
+
+def pin_zero_query_uniform(m):
+    """Q = 0 makes every visible score 0: P is uniform, O_i is the mean of the
+    visible V rows (the prefix mean when causal) and LSE_i = ln(#visible)."""
+    N, d = 11, 6
+    v = _rand((N, d), 3)
+    k = _rand((N, d), 4)
+    for causal in (False, True):
+        O, LSE = m.head_forward(np.zeros((N, d)), k, v, 0.7, causal)
+        cnt = _visible_count(N, causal)
+        mean = np.cumsum(v, 0) / cnt[:, None] if causal else np.broadcast_to(v.mean(0), v.shape)
+        assert np.allclose(O, mean, rtol=0, atol=1e-13)
+        assert np.allclose(LSE, np.log(cnt), rtol=0, atol=1e-13)
+
+
+def pin_single_key(m):
+    """N = 1: O = V_0, LSE = scale q.k, dQ = dK = 0, dV = dO."""
+    q, k, v, do = (_rand((1, 7), s) for s in (5, 6, 7, 8))
+    for causal in (False, True):
+        r = m.head_backward(q, k, v, do, 0.3, causal)
+        assert np.allclose(r["o"], v, atol=1e-15)
+        assert np.allclose(r["lse"], 0.3 * (q @ k.T).ravel(), atol=1e-14)
+        assert np.abs(r["dq"]).max() < 1e-15 and np.abs(r["dk"]).max() < 1e-15
+        assert np.allclose(r["dv"], do, atol=1e-15)
+
+
+def pin_constant_values(m):
+    """Identical V rows: O equals that row whatever P is, so dQ = dK = 0."""
+    N, d = 8, 5
+    q, k, do = _rand((N, d), 9), _rand((N, d), 10), _rand((N, d), 11)
+    v = np.tile(_rand((1, d), 12), (N, 1))
+    for causal in (False, True):
+        r = m.head_backward(q, k, v, do, 0.5, causal)
+        assert np.allclose(r["o"], v, atol=1e-14)
+        assert np.abs(r["dq"]).max() < 1e-13 and np.abs(r["dk"]).max() < 1e-13
+
+
+def pin_key_shift(m):
+    """Adding c to every K row adds scale q_i.c to row i's scores: O is unchanged and
+    LSE_i moves by exactly scale q_i.c."""
+    N, d = 10, 4
+    q, k, v = _rand((N, d), 13), _rand((N, d), 14), _rand((N, d), 15)
+    c = _rand((d,), 16)
+    for causal in (False, True):
+        O0, L0 = m.head_forward(q, k, v, 0.6, causal)
+        O1, L1 = m.head_forward(q, k + c, v, 0.6, causal)
+        assert np.allclose(O0, O1, atol=1e-13)
+        assert np.allclose(L1 - L0, 0.6 * q @ c, atol=1e-13)
+
+
+def pin_gradient_sums(m):
+    """sum_j dS_ij = 0 for every row (the D term removes the softmax's common-mode
+    gradient, 'flash-attention-backpropagation' Softmax梯度); hence sum_j dK_j = 0."""
+    N, d = 12, 6
+    q, k, v, do = (_rand((N, d), s) for s in (17, 18, 19, 20))
+    for causal in (False, True):
+        r = m.head_backward(q, k, v, do, 0.45, causal, return_ds=True)
+        assert np.abs(r["ds"].sum(1)).max() < 1e-13
+        assert np.abs(r["dk"].sum(0)).max() < 1e-13
+
+
+def pin_dv_brute_force(m):
+    """dV_j = sum_i P_ij dO_i, with P built by pure-Python loops from the definition."""
+    N, d, scale = 5, 3, 0.8
+    q, k, v, do = (_rand((N, d), s) for s in (21, 22, 23, 24))
+    for causal in (False, True):
+        P = [[0.0] * N for _ in range(N)]
+        for i in range(N):
+            vis = [j for j in range(N) if not (causal and j > i)]
+            s = {j: scale * sum(q[i][c] * k[j][c] for c in range(d)) for j in vis}
+            mx = max(s.values())
+            z = sum(math.exp(s[j] - mx) for j in vis)
+            for j in vis:
+                P[i][j] = math.exp(s[j] - mx) / z
+        dv = [[sum(P[i][j] * do[i][c] for i in range(N)) for c in range(d)] for j in range(N)]
+        o = [[sum(P[i][j] * v[j][c] for j in range(N)) for c in range(d)] for i in range(N)]
+        r = m.head_backward(q, k, v, do, scale, causal)
+        assert np.allclose(r["dv"], dv, atol=1e-14)
+        assert np.allclose(r["o"], o, atol=1e-14)
+
+
+def _loss(m, q, k, v, do, scale, causal):
+    O, _ = m.head_forward(q, k, v, scale, causal)
+    return float((O * do).sum())
+
+
+def pin_finite_differences(m):
+    """Central differences of L = <O, dO> with respect to every element of Q, K and V
+    match dQ, dK and dV (brute force, N <= 16)."""
+    h = 1e-5
+    for N, d, causal, seed in ((1, 3, False, 0), (5, 4, False, 1), (7, 4, True, 2), (16, 4, True, 3),
+                               (16, 3, False, 4)):
+        q, k, v, do = (_rand((N, d), 100 * seed + s) for s in range(4))
+        scale = 1.0 / math.sqrt(d)
+        r = m.head_backward(q, k, v, do, scale, causal)
+        for name, x in (("dq", q), ("dk", k), ("dv", v)):
+            g = np.empty_like(x)
+            for idx in np.ndindex(*x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args = {"dq": (0,), "dk": (1,), "dv": (2,)}[name][0]
+                ap = [q, k, v]
+                am = [q, k, v]
+                ap[args], am[args] = xp, xm
+                g[idx] = (_loss(m, *ap, do, scale, causal) - _loss(m, *am, do, scale, causal)) / (2 * h)
+            err = np.abs(g - r[name]).max() / max(1e-300, np.abs(g).max())
+            assert err < 1e-7, (name, N, causal, err)
+
+
+def pin_mpmath_gradients(m):
+    """A 40-digit mpmath evaluation of the forward definition, differentiated by central
+    differences with step 1e-15, agrees with the oracle's O, LSE and gradients."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 40
+    N, d, scale = 4, 3, 0.55
+    q, k, v, do = (_rand((N, d), 40 + s) for s in range(4))
+
+    def fwd(Q, K, V, causal):
+        O, L = [], []
+        for i in range(N):
+            vis = [j for j in range(N) if not (causal and j > i)]
+            s = [scale * mp.fsum(Q[i][c] * K[j][c] for c in range(d)) for j in vis]
+            z = mp.fsum(mp.exp(x) for x in s)
+            O.append([mp.fsum(mp.exp(s[a]) / z * V[j][c] for a, j in enumerate(vis)) for c in range(d)])
+            L.append(mp.log(z))
+        return O, L
+
+    def loss(Q, K, V, causal):
+        O, _ = fwd(Q, K, V, causal)
+        return mp.fsum(O[i][c] * mp.mpf(do[i][c]) for i in range(N) for c in range(d))
+
+    h = mp.mpf("1e-15")
+    for causal in (False, True):
+        X = [[[mp.mpf(float(a[i][c])) for c in range(d)] for i in range(N)] for a in (q, k, v)]
+        r = m.head_backward(q, k, v, do, scale, causal)
+        O, L = fwd(*X, causal)
+        assert np.allclose(r["o"], np.array(O, dtype=float), rtol=0, atol=1e-14)
+        assert np.allclose(r["lse"], np.array(L, dtype=float), rtol=0, atol=1e-14)
+        for which, name in enumerate(("dq", "dk", "dv")):
+            g = np.empty((N, d))
+            for i in range(N):
+                for c in range(d):
+                    Xp = [[row[:] for row in M] for M in X]
+                    Xm = [[row[:] for row in M] for M in X]
+                    Xp[which][i][c] += h
+                    Xm[which][i][c] -= h
+                    g[i, c] = float((loss(*Xp, causal) - loss(*Xm, causal)) / (2 * h))
+            assert np.allclose(r[name], g, rtol=0, atol=1e-12), (name, causal)
+
+
+def pin_torch_sdpa(m):
+    """PyTorch's CPU float64 scaled_dot_product_attention and autograd agree."""
+    torch = pytest.importorskip("torch")
+    B, H, N, d = 2, 3, 37, 8
+    arrs = [_rand((B, H, N, d), 60 + s) for s in range(4)]
+    for causal in (False, True):
+        t = [torch.tensor(a, dtype=torch.float64, requires_grad=(i < 3)) for i, a in enumerate(arrs)]
+        o = torch.nn.functional.scaled_dot_product_attention(t[0], t[1], t[2], is_causal=causal, scale=0.3)
+        (o * t[3]).sum().backward()
+        r = m.backward(*arrs, 0.3, causal)
+        assert np.allclose(r["o"], o.detach().numpy(), rtol=0, atol=1e-12)
+        for name, ten in zip(("dq", "dk", "dv"), t[:3]):
+            assert np.allclose(r[name], ten.grad.numpy(), rtol=0, atol=1e-12), name
+        s = 0.3 * torch.matmul(t[0], t[1].transpose(-1, -2)).detach()
+        if causal:
+            s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+        assert np.allclose(r["lse"], torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+
+
+# -- the pages' block-wise recurrences, restated independently -----------------------
+def _blockwise_forward(q, k, v, scale, causal, block):
+    """Tiled forward with the online softmax: per block, the local max and local exp-sum
+    are merged into the running (m, l) as l_new = l e^{m - m_new} + l_loc e^{m_loc - m_new}
+    ('知识点13', section 4), and the un-normalised output is rescaled by e^{m - m_new}
+    and divided by l at the end ('flash-attention-backpropagation', Python 演示)."""
+    N, d = q.shape
+    O = np.zeros((N, v.shape[1]))
+    mrun = np.full(N, -np.inf)
+    lrun = np.zeros(N)
+    for j0 in range(0, N, block):
+        kb, vb = k[j0:j0 + block], v[j0:j0 + block]
+        for i0 in range(0, N, block):
+            if causal and j0 > i0 + block - 1:
+                continue
+            s = scale * q[i0:i0 + block] @ kb.T
+            if causal:
+                ii = np.arange(i0, min(N, i0 + block))[:, None]
+                jj = np.arange(j0, min(N, j0 + block))[None, :]
+                s = np.where(jj > ii, -np.inf, s)
+            mloc = s.max(1)
+            e = np.exp(s - mloc[:, None])
+            e[~np.isfinite(s)] = 0.0
+            lloc = e.sum(1)
+            mo = mrun[i0:i0 + block]
+            mn = np.maximum(mo, mloc)
+            a = np.where(np.isfinite(mo), np.exp(mo - mn), 0.0)
+            b = np.where(np.isfinite(mloc), np.exp(mloc - mn), 0.0)
+            lrun[i0:i0 + block] = lrun[i0:i0 + block] * a + lloc * b
+            O[i0:i0 + block] = O[i0:i0 + block] * a[:, None] + (e * b[:, None]) @ vb
+            mrun[i0:i0 + block] = mn
+    return O / lrun[:, None], mrun + np.log(lrun)
+
+
+def _blockwise_backward(q, k, v, do, scale, causal, block):
+    """Outer loop over key/value blocks, inner loop over query blocks; P is rebuilt from
+    the forward's statistics and dV, dQ, dK are accumulated block by block
+    ('flash-attention-backpropagation', QKV梯度)."""
+    N = q.shape[0]
+    O, lse = _blockwise_forward(q, k, v, scale, causal, block)
+    D = (do * O).sum(1)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for j0 in range(0, N, block):
+        for i0 in range(0, N, block):
+            s = scale * q[i0:i0 + block] @ k[j0:j0 + block].T
+            p = np.exp(s - lse[i0:i0 + block, None])
+            if causal:
+                ii = np.arange(i0, min(N, i0 + block))[:, None]
+                jj = np.arange(j0, min(N, j0 + block))[None, :]
+                p = np.where(jj > ii, 0.0, p)
+            dv[j0:j0 + block] += p.T @ do[i0:i0 + block]
+            dp = do[i0:i0 + block] @ v[j0:j0 + block].T
+            ds = p * (dp - D[i0:i0 + block, None])
+            dq[i0:i0 + block] += scale * ds @ k[j0:j0 + block]
+            dk[j0:j0 + block] += scale * ds.T @ q[i0:i0 + block]
+    return O, lse, dq, dk, dv
+
+
+def pin_worked_examples(m):
+    """The pages' worked examples: block-wise equals dense within the page's own bar."""
+    ex = GOLDEN["fa2_pure_python_demo"]
+    q, k, v = (np.array(ex[n], dtype=np.float64) for n in ("Q", "K", "V"))
+    scale = 1 / math.sqrt(ex["d"])
+    O, L = m.head_forward(q, k, v, scale, ex["causal"])
+    Ob, Lb = _blockwise_forward(q, k, v, scale, ex["causal"], ex["block"])
+    assert np.abs(O - Ob).max() < ex["max_abs_diff"]
+    assert np.abs(L - Lb).max() < ex["max_abs_diff"]
+
+    ex = GOLDEN["bwd_numpy_demo"]
+    rng = np.random.default_rng(0)
+    q, k, v, do = (rng.normal(size=(ex["N"], ex["d"])) for _ in range(4))
+    scale = 1 / math.sqrt(ex["d"])
+    r = m.head_backward(q, k, v, do, scale, ex["causal"])
+    _, _, dq, dk, dv = _blockwise_backward(q, k, v, do, scale, ex["causal"], ex["block"])
+    for a, b in ((r["dq"], dq), (r["dk"], dk), (r["dv"], dv)):
+        assert np.abs(a - b).max() < ex["atol"]
+
+    ex = GOLDEN["kp13_causal_equivalence"]
+    rng = np.random.default_rng(0)
+    shp = (ex["B"], ex["H"], ex["N"], ex["d"])
+    q, k, v = (rng.standard_normal(shp, dtype=np.float32).astype(np.float64) for _ in range(3))
+    do = rng.standard_normal(shp, dtype=np.float32).astype(np.float64)
+    scale = 1 / math.sqrt(ex["d"])
+    r = m.backward(q, k, v, do, scale, True)
+    for b in range(ex["B"]):
+        for h in range(ex["H"]):
+            Ob, Lb, dq, dk, dv = _blockwise_backward(q[b, h], k[b, h], v[b, h], do[b, h], scale, True, ex["block"])
+            assert np.abs(r["o"][b, h] - Ob).max() < ex["max_abs_diff"]
+            # the same recurrences in float64 agree far below the page's float32 bar
+            for a, bb in ((r["lse"][b, h], Lb), (r["dq"][b, h], dq), (r["dk"][b, h], dk), (r["dv"][b, h], dv)):
+                assert np.abs(a - bb).max() < 1e-11
+
+
+def pin_blockwise_random(m):
+    """Block-wise recurrences equal the dense oracle to 1e-12 on ragged random cases."""
+    for N, d, block, causal, seed in ((13, 5, 4, False, 0), (13, 5, 4, True, 1), (33, 8, 8, True, 2)):
+        q, k, v, do = (_rand((N, d), 200 + 10 * seed + s) for s in range(4))
+        scale = 0.9 / math.sqrt(d)
+        r = m.head_backward(q, k, v, do, scale, causal)
+        O, L, dq, dk, dv = _blockwise_backward(q, k, v, do, scale, causal, block)
+        for a, b in ((r["o"], O), (r["lse"], L), (r["dq"], dq), (r["dk"], dk), (r["dv"], dv)):
+            assert np.abs(a - b).max() < 1e-12
+
+
+def pin_row_sampling(m):
+    """Row subsets and row grouping give the same numbers as the whole head."""
+    N, d = 40, 4
+    q, k, v = (_rand((N, d), 300 + s) for s in range(3))
+    for causal in (False, True):
+        O, L = m.head_forward(q, k, v, 0.5, causal)
+        rows = np.array([0, 7, 39, 20])
+        Os, Ls = m.head_forward(q, k, v, 0.5, causal, rows=rows)
+        assert np.array_equal(Os, O[rows]) or np.allclose(Os, O[rows], atol=1e-15)
+        assert np.allclose(Ls, L[rows], atol=1e-15)
+
+
+PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
+def test_pins_hold(pin):
+    pin(oracle_attention)
+
+
+def test_row_grouping_matches_single_group(monkeypatch):
+    """The memory-bounding row groups change nothing beyond rounding."""
+    N, d = 50, 4
+    q, k, v, do = (_rand((N, d), 400 + s) for s in range(4))
+    ref = oracle_attention.head_backward(q, k, v, do, 0.5, True)
+    monkeypatch.setattr(oracle_attention, "_GROUP_ELEMS", 7 * N)
+    got = oracle_attention.head_backward(q, k, v, do, 0.5, True)
+    for n in ref:
+        assert np.allclose(ref[n], got[n], rtol=0, atol=1e-13), n
+
+
+# ----------------------------------------------------------- planted mistakes
+MUTATIONS = [
+    ("dropped D term in dS", "dS = P * (dP - D[r, None])", "dS = P * dP"),
+    ("wrong sign in dS", "dS = P * (dP - D[r, None])", "dS = P * (D[r, None] - dP)"),
+    ("scale missing on dK", "dK += scale * (dS.T @ q[r])", "dK += dS.T @ q[r]"),
+    ("scale missing on dQ", "dQ[r] = scale * (dS @ k)", "dQ[r] = dS @ k"),
+    ("dV uses V instead of dO", "dV += P.T @ do[r]", "dV += P.T @ v[r]"),
+    ("dV without the transpose", "dV += P.T @ do[r]", "dV += P @ do[r]"),
+    ("dQ uses Q instead of K", "dQ[r] = scale * (dS @ k)", "dQ[r] = scale * (dS @ q)"),
+    ("dP uses K instead of V", "dP = do[r] @ v.T", "dP = do[r] @ k.T"),
+    ("mask hides diagonal", "j[None, :] > rows[:, None]", "j[None, :] >= rows[:, None]"),
+    ("mask keeps the future", "j[None, :] > rows[:, None]", "j[None, :] < rows[:, None]"),
+    ("max not subtracted from LSE", "LSE[a:a + g] = m + np.log(l)", "LSE[a:a + g] = np.log(l)"),
+    ("log2 in LSE", "LSE[a:a + g] = m + np.log(l)", "LSE[a:a + g] = m + np.log2(l)"),
+    ("D from dO.dO", 'np.einsum("ic,ic->i", np.asarray(do, np.float64), np.asarray(o, np.float64))',
+     'np.einsum("ic,ic->i", np.asarray(do, np.float64), np.asarray(do, np.float64))'),
+    ("scale missing on scores", "s = scale * (q[rows] @ k.T)", "s = q[rows] @ k.T"),
+    ("no normalisation", "return e / l[:, None], m, l", "return e, m, l"),
+]
+
+
+def _mutant(old, new):
+    src = open(oracle_attention.__file__).read()
+    assert old in src, old
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(src.replace(old, new), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("mut", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistakes_are_caught(mut):
+    _, old, new = mut
+    mod = _mutant(old, new)
+    failed = []
+    for pin in PINS:
+        if pin is pin_mpmath_gradients:
+            continue  # slow; the other pins already cover every mutation
+        try:
+            with np.errstate(all="ignore"):
+                pin(mod)
+        except (AssertionError, FloatingPointError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught: {mut[0]}"
