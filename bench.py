@@ -1,0 +1,368 @@
+#!/usr/bin/env python
+"""Benchmark: exact attention forward + backward on GB300, one JSON line on rank 0.
+
+A step is one pass of the whole path on one batch: fa_fwd (O, LSE), fa_bwd_preprocess
+(D = rowsum(dO*O)) and fa_bwd (dQ, dK, dV), on the headline workload B=2, H=16,
+N=8192, d=128, bf16, causal, unless --workload names another. FLOPs follow the
+convention 4*B*H*N^2*d for the forward (halved when causal) and 2.5x that for the
+backward. The inputs and outputs (8 tensors of 67 MB) exceed the 129 MB L2, so no
+flush runs between steps.
+
+--impl reference times the fp64 CPU oracle instead (a deliberately slow baseline),
+one head of the workload per step, on the host cores.
+
+Multi-GPU (torchrun): each rank runs its own copy of the workload (attention heads are
+independent; no collective on the data path); value = all ranks' FLOPs / max time.
+"""
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16, N=8192 d=128 causal), % of dense tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            cmd = ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, c in zip(names, r[5:9]):
+                if c.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def oracle_head_step(w, x, b, h):
+    from oracle import attention as ora
+    import numpy as np
+    args = [x[n][b, h].astype(np.float64) for n in ("q", "k", "v", "do")]
+    ora.head_backward(*args, w.scale, w.causal)
+
+
+def cpu_baseline(w, x, budget_s=12.0, max_heads=8):
+    """The oracle, as it stands, on whole heads of the workload until ~budget_s."""
+    flop_head = (w.fwd_flop() + w.bwd_flop()) / (w.B * w.H)
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_heads and (time.perf_counter() - t0) < budget_s:
+        oracle_head_step(w, x, n // w.H % w.B, n % w.H)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": flop_head * n / dt / 1e12, "unit": "TFLOP/s",
+            "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1)), "kind": "oracle",
+            "sample": f"{n} whole head(s) of the workload (fwd+bwd, fp64 numpy), {dt:.1f} s; "
+                      f"FLOPs counted by the same convention as the GPU line"}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from exact_attention_02_gb300.workloads import make_inputs
+    x = make_inputs(w)
+    flop_head = (w.fwd_flop() + w.bwd_flop()) / (w.B * w.H)
+    for i in range(args.warmup):
+        oracle_head_step(w, x, 0, i % w.H)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_head_step(w, x, (i // w.H) % w.B, i % w.H)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = flop_head / dt / 1e12
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "step": "one whole head (fwd+bwd) of the workload per step, fp64 numpy oracle on the host"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "one head of the workload per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def count_launches(step):
+    """Kernels one step launches, counted with the CUDA activity profiler."""
+    import torch
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            step()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if str(getattr(e, "device_type", "")).endswith("CUDA")]
+        ours = [n for n in names if "fa::" in n or n.startswith("_ZN2fa")]
+        return len(ours), sorted(set(ours))
+    except Exception as e:  # profiler unavailable: report nothing rather than guess
+        return None, [f"profiler unavailable: {e}"]
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_02_gb300 as fa
+    from exact_attention_02_gb300.build import build
+    from exact_attention_02_gb300.workloads import make_inputs
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        dist.barrier()
+    fa.lib()
+    dev = torch.device("cuda", local)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    x = make_inputs(w)
+    host = {n: torch.from_numpy(x[n]).to(tdt).pin_memory() for n in ("q", "k", "v", "do")}
+    q, k, v, do = (host[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    D = torch.empty_like(lse)
+    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d, tdt)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        fa.fa_fwd(q, k, v, w.causal, w.scale, o=o, lse=lse)
+
+    def pre():
+        fa.fa_bwd_preprocess(o, do, D=D)
+
+    def bwd():
+        fa.fa_bwd(q, k, v, o, do, lse, w.causal, w.scale, D=D, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    def step():
+        fwd()
+        pre()
+        bwd()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    launches, kernel_names = count_launches(step)
+
+    peaks, peak_src = load_peaks()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for i in range(args.steps):
+        e = ev[i]
+        e[0].record(stream)
+        fwd()
+        e[1].record(stream)
+        pre()
+        e[2].record(stream)
+        bwd()
+        e[3].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    if world > 1:
+        t = torch.tensor([ms, fwd_ms, pre_ms, bwd_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, fwd_ms, pre_ms, bwd_ms = t.tolist()
+    status = fa.fa_get_last_device_status()
+    if status != fa.FA_OK:
+        raise RuntimeError(f"device status {fa.error_string(status)}")
+
+    flop = w.fwd_flop() + w.bwd_flop()
+    value = world * flop / (ms * 1e-3) / 1e12
+
+    # end to end: pinned host inputs in, results (O, LSE, dQ, dK, dV) back to pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    for n, t in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items()}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+
+        def e2e_step():
+            for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
+                dst.copy_(host[n], non_blocking=True)
+            step()
+            for n, src in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items():
+                out_host[n].copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, args.steps // 2)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = t.item()
+        e2e = {"value": world * flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    esz = 2 if w.dtype == "bf16" else 4
+    rows = w.B * w.H * w.N
+    pre_bytes = 2 * rows * w.d * esz + rows * 4
+    kern = {"fa_fwd": fwd_ms, "fa_bwd": bwd_ms, "fa_bwd_preprocess": pre_ms}
+    dominant = max(kern, key=kern.get)
+    tensor_path = w.dtype == "bf16" and fa.TENSOR_CORE_PATH
+    if tensor_path:
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        peak_desc = f"bf16 dense, sustained ({peak_src})"
+        bound, unit = "tensor", "TFLOP/s"
+    else:
+        # FFMA path: 152 SMs x 128 FMA/clk x 2 FLOP x max SM clock
+        peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        peak_desc = "fp32 FFMA: 152 SMs x 128 FMA/clk x 2 x max SM clock (derived)"
+        bound, unit = "alu", "TFLOP/s"
+    dom_flop = {"fa_fwd": w.fwd_flop(), "fa_bwd": w.bwd_flop()}.get(dominant)
+    if dom_flop is None:
+        achieved = pre_bytes / (pre_ms * 1e-3) / 1e9
+        peak, bound, unit, peak_desc = peaks["hbm_gbs"], "hbm", "GB/s", f"HBM copy ({peak_src})"
+    else:
+        achieved = dom_flop / (kern[dominant] * 1e-3) / 1e12
+    roofline = {"kernel": dominant, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "peak_source": peak_desc, "traffic": None}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "scale": w.scale, "parallelism": f"replicas x{world} (heads independent, no collective)",
+                   "l2": "no flush: the 8 [B,H,N,d] tensors (537 MB) exceed the 129 MB L2"},
+        "fwd": {"ms": fwd_ms, "tflops": w.fwd_flop() / (fwd_ms * 1e-3) / 1e12},
+        "bwd": {"ms": pre_ms + bwd_ms, "tflops": w.bwd_flop() / ((pre_ms + bwd_ms) * 1e-3) / 1e12,
+                "note": "preprocess + fa_bwd"},
+        "preprocess": {"ms": pre_ms, "gbs": pre_bytes / (pre_ms * 1e-3) / 1e9,
+                       "frac_hbm": pre_bytes / (pre_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "roofline": roofline,
+        "gpu_launches": None if launches is None else launches * args.steps,
+        "kernels_per_step": kernel_names,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    line["fwd"]["frac_peak"] = line["fwd"]["tflops"] / peak if bound == "tensor" else None
+    line["bwd"]["frac_peak"] = line["bwd"]["tflops"] / peak if bound == "tensor" else None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, x)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    from exact_attention_02_gb300.workloads import HEADLINE, WORKLOADS
+    w = WORKLOADS[args.workload or HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

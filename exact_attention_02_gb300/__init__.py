@@ -1,0 +1,160 @@
+"""Exact tiled attention (forward + backward) for GB300 — thin Python binding.
+
+Every function here marshals torch tensors into the C ABI of ``libfa_gb300.so``
+(declared in ``include/fa.h``) and calls it on the current CUDA stream. All arithmetic
+runs in the library's CUDA kernels; PyTorch only provides device memory and streams.
+The library must be built (``exact_attention_02_gb300.build.build()``); if it is
+missing, every call raises instead of computing anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from .workloads import HEADLINE, WORKLOADS, Workload, make_inputs  # noqa: F401
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT, FA_ERR_WORKSPACE = range(6)
+FA_DTYPE_BF16, FA_DTYPE_FP32 = 0, 1
+
+# True once bf16 calls run on the tcgen05 tensor-core kernels (the fp32 path is FFMA).
+TENSOR_CORE_PATH = False
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {error_string(status)}")
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"the CUDA library {LIB_PATH} is not built; run exact_attention_02_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    L.fa_fwd.restype = i
+    L.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+    L.fa_bwd_preprocess.restype = i
+    L.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
+    L.fa_bwd_workspace_size.restype = sz
+    L.fa_bwd.argtypes = [vp] * 11 + [sz, i, i, i, i, f, i, i, vp]
+    L.fa_bwd.restype = i
+    L.fa_get_error_string.argtypes = [i]
+    L.fa_get_error_string.restype = ctypes.c_char_p
+    L.fa_get_last_device_status.argtypes = []
+    L.fa_get_last_device_status.restype = i
+    _lib = L
+    return L
+
+
+def lib():
+    """The loaded ctypes library (raises if it is not built)."""
+    return _load()
+
+
+def error_string(status: int) -> str:
+    return _load().fa_get_error_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return FA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return FA_DTYPE_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    return tuple(int(x) for x in q.shape)
+
+
+def _same(ref, *ts):
+    for t in ts:
+        if t is None:
+            continue
+        if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device:
+            raise ValueError("Q/K/V/O/dO/dQ/dK/dV must share shape, dtype and device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def fa_fwd(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None, stream=None):
+    """O, LSE = attention forward of [B, H, N, d] CUDA tensors (see ``fa_fwd`` in fa.h)."""
+    import torch
+    B, H, N, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _same(q, k, v, o)
+    _check(_load().fa_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d, scale, int(bool(causal)),
+                          _dtype_code(q), _stream_ptr(stream)), "fa_fwd")
+    return o, lse
+
+
+def fa_bwd_preprocess(o, do, D=None, stream=None):
+    """D = rowsum(dO * O) as float32 [B, H, N] (see ``fa_bwd_preprocess`` in fa.h)."""
+    import torch
+    B, H, N, d = _shape(o)
+    _same(o, do)
+    D = torch.empty((B, H, N), dtype=torch.float32, device=o.device) if D is None else D
+    _check(_load().fa_bwd_preprocess(_p(o), _p(do), _p(D), B, H, N, d, _dtype_code(o),
+                                     _stream_ptr(stream)), "fa_bwd_preprocess")
+    return D
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int, d: int, dtype) -> int:
+    import torch
+    code = dtype if isinstance(dtype, int) else (FA_DTYPE_BF16 if dtype == torch.bfloat16 else FA_DTYPE_FP32)
+    return int(_load().fa_bwd_workspace_size(B, H, N, d, code))
+
+
+def fa_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None, D=None,
+           dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of attention from the forward's O and LSE (see ``fa_bwd`` in fa.h)."""
+    import torch
+    B, H, N, d = _shape(q)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _same(q, k, v, o, do, dq, dk, dv)
+    need = fa_bwd_workspace_size(B, H, N, d, q.dtype) + (0 if D is not None else 4 * B * H * N)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_load().fa_bwd(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(D), _p(dq), _p(dk), _p(dv),
+                          _p(workspace), wbytes, B, H, N, d, scale, int(bool(causal)), _dtype_code(q),
+                          _stream_ptr(stream)), "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_get_last_device_status() -> int:
+    return int(_load().fa_get_last_device_status())

@@ -1,0 +1,134 @@
+// C ABI entry points: argument checks, dispatch to the kernels, status reporting.
+#include <math.h>
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+__device__ int g_device_status;  // 0 or FA_ERR_DEVICE_TIMEOUT, per device
+
+int* device_status_ptr() {
+  static std::mutex mu;
+  static int* cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status_t check_shape(const Shape& s, int dtype, float* scale) {
+  if (s.B < 1 || s.H < 1 || s.N < 1 || s.d < 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
+  // B*H*N*d must be representable; keep B*H below 2^31 and the element count < 2^60.
+  const int64_t bh = (int64_t)s.B * s.H;
+  if (bh >= (int64_t(1) << 31)) return FA_ERR_INVALID_ARG;
+  if (bh * s.N > (int64_t(1) << 50) || s.elems() > (int64_t(1) << 60)) return FA_ERR_INVALID_ARG;
+  if (scale && !(isfinite(*scale) && *scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (s.d != 64 && s.d != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_BF16 && s.N % 128 != 0) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_FP32 && s.N > 4096) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status_t check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+fa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace fa
+
+using fa::Shape;
+
+extern "C" fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                              int B, int H, int N, int d, float scale, int causal, int dtype,
+                              void* stream) {
+  const Shape s{B, H, N, d};
+  fa_status_t r = fa::check_shape(s, dtype, &scale);
+  if (r != FA_OK) return r;
+  if ((r = fa::check_ptrs({Q, K, V, O, LSE})) != FA_OK) return r;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return fa::from_cuda(
+      fa::simt_fwd(Q, K, V, O, LSE, s, scale, causal == 1, dtype == FA_DTYPE_BF16, st));
+}
+
+extern "C" fa_status_t fa_bwd_preprocess(const void* O, const void* dO, float* D, int B, int H,
+                                         int N, int d, int dtype, void* stream) {
+  const Shape s{B, H, N, d};
+  fa_status_t r = fa::check_shape(s, dtype, nullptr);
+  if (r != FA_OK) return r;
+  if ((r = fa::check_ptrs({O, dO, D})) != FA_OK) return r;
+  return fa::from_cuda(
+      fa::preprocess_d(O, dO, D, s, dtype == FA_DTYPE_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d, int dtype) {
+  const Shape s{B, H, N, d};
+  if (fa::check_shape(s, dtype, nullptr) != FA_OK) return 0;
+  return dtype == FA_DTYPE_BF16 ? (size_t)s.elems() * sizeof(float) : 0;
+}
+
+extern "C" fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O,
+                              const void* dO, const float* LSE, const float* D, void* dQ,
+                              void* dK, void* dV, void* workspace, size_t workspace_bytes, int B,
+                              int H, int N, int d, float scale, int causal, int dtype,
+                              void* stream) {
+  const Shape s{B, H, N, d};
+  fa_status_t r = fa::check_shape(s, dtype, &scale);
+  if (r != FA_OK) return r;
+  if ((r = fa::check_ptrs({Q, K, V, O, dO, LSE, dQ, dK, dV})) != FA_OK) return r;
+  if (D && !fa::aligned16(D)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  const size_t need = fa_bwd_workspace_size(B, H, N, d, dtype);
+  const size_t need_d = D ? 0 : (size_t)s.rows() * sizeof(float);
+  if (need + need_d > 0) {
+    if (!workspace || workspace_bytes < need + need_d) return FA_ERR_WORKSPACE;
+    if (!fa::aligned16(workspace)) return FA_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  if (!D) {
+    float* Dw = reinterpret_cast<float*>(static_cast<char*>(workspace) + need);
+    if ((r = fa::from_cuda(fa::preprocess_d(O, dO, Dw, s, bf16, st))) != FA_OK) return r;
+    D = Dw;
+  }
+  return fa::from_cuda(fa::simt_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal == 1, bf16, st));
+}
+
+extern "C" const char* fa_get_error_string(fa_status_t status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null/misaligned pointer or bad size, scale or flag";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: valid arguments outside what is implemented (d, N, dtype)";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call or kernel launch failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a bounded device-side wait gave up";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or smaller than fa_bwd_workspace_size()";
+  }
+  return "unknown fa_status_t";
+}
+
+extern "C" fa_status_t fa_get_last_device_status(void) {
+  int* p = fa::device_status_ptr();
+  if (!p) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return v == 0 ? FA_OK : static_cast<fa_status_t>(v);
+}

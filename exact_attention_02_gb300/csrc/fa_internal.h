@@ -1,0 +1,35 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Sizes of one call, validated on the host.
+struct Shape {
+  int B, H, N, d;
+  int64_t heads() const { return (int64_t)B * H; }
+  int64_t rows() const { return heads() * N; }
+  int64_t elems() const { return rows() * d; }
+};
+
+// Device status word: bounded waits that give up write FA_ERR_DEVICE_TIMEOUT here.
+// Defined in fa_api.cu; kernels in other units reach it through this pointer, which
+// fa_api.cu resolves once per device.
+int* device_status_ptr();
+
+// ---- exact FFMA path (fa_simt.cu): fp32 and bf16 element types ----
+cudaError_t simt_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                     const Shape& s, float scale, bool causal, bool bf16, cudaStream_t st);
+cudaError_t simt_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                     const float* LSE, const float* D, void* dQ, void* dK, void* dV,
+                     const Shape& s, float scale, bool causal, bool bf16, cudaStream_t st);
+
+// ---- memory-bound helpers (fa_simt.cu) ----
+cudaError_t preprocess_d(const void* O, const void* dO, float* D, const Shape& s, bool bf16,
+                         cudaStream_t st);
+
+}  // namespace fa

@@ -1,0 +1,351 @@
+// Exact attention on the FFMA pipes: the float32 path, and the row-dot D pass.
+//
+// One warp owns one query row (forward, dQ) or one key row (dK/dV); each step stages
+// 32 keys (or queries) in shared memory, one per lane, so a warp forms 32 scores in
+// parallel and merges them into its running statistics with one max and one sum
+// reduction. This is the online softmax of "flash-attention-v2-sram-tiling" §5 with
+// the un-normalised accumulator of "flash-attention-backpropagation" (Python 演示):
+// O is rescaled by exp(m_old - m_new) whenever the row max grows and divided by l
+// once at the end. Scores are kept in log2 units (the scale is folded into q, §7).
+// The backward rebuilds P = exp(s - LSE) and follows Softmax梯度 / QKV梯度 of
+// "flash-attention-backpropagation": dK/dV in one kernel over key rows, dQ in a
+// second kernel over query rows, so no accumulator is shared between warps.
+#include <cuda_bf16.h>
+
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kWarps = 8;   // rows per CTA, one warp each
+constexpr int kChunk = 32;  // keys (or queries) staged per step, one per lane
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void stf(float* p, float v) { *p = v; }
+__device__ __forceinline__ void stf(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Forward: grid = tiles * heads (flattened), block = kWarps warps, warp w -> query row.
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarps * 32)
+simt_fwd_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
+                T* __restrict__ O, float* __restrict__ LSE, int N, int tiles, float scale,
+                int causal) {
+  __shared__ float ks[kChunk][D + 1];
+  __shared__ float vs[kChunk][D];
+  __shared__ float qs[kWarps][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t head = blockIdx.x / tiles;
+  const int row0 = (blockIdx.x % tiles) * kWarps;
+  const int row = row0 + warp;
+  const bool active = row < N;
+  const size_t base = (size_t)head * N * D;
+  const float sl2 = scale * kLog2e;
+  for (int c = lane; c < D; c += 32)
+    qs[warp][c] = active ? ldf(Q + base + (size_t)row * D + c) * sl2 : 0.f;
+
+  float m = -INFINITY, l = 0.f, acc[D / 32];
+#pragma unroll
+  for (int t = 0; t < D / 32; ++t) acc[t] = 0.f;
+
+  const int kv_end = causal ? min(N, row0 + kWarps) : N;
+  for (int j0 = 0; j0 < kv_end; j0 += kChunk) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < kChunk * D; e += blockDim.x) {
+      const int r = e / D, c = e % D, j = j0 + r;
+      float kv = 0.f, vv = 0.f;
+      if (j < N) {
+        kv = ldf(K + base + (size_t)j * D + c);
+        vv = ldf(V + base + (size_t)j * D + c);
+      }
+      ks[r][c] = kv;
+      vs[r][c] = vv;
+    }
+    __syncthreads();
+    const int j = j0 + lane;
+    float s = 0.f;
+#pragma unroll 16
+    for (int c = 0; c < D; ++c) s = fmaf(qs[warp][c], ks[lane][c], s);
+    const bool vis = active && j < N && (!causal || j <= row);
+    s = vis ? s : -INFINITY;
+    const float mnew = fmaxf(m, warp_max(s));
+    if (mnew == -INFINITY) continue;  // nothing visible yet in this row (warp-uniform)
+    const float p = vis ? exp2f(s - mnew) : 0.f;
+    const float corr = exp2f(m - mnew);
+    l = l * corr + warp_sum(p);
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) acc[t] *= corr;
+#pragma unroll 8
+    for (int jj = 0; jj < kChunk; ++jj) {
+      const float pj = __shfl_sync(0xffffffffu, p, jj);
+#pragma unroll
+      for (int t = 0; t < D / 32; ++t) acc[t] = fmaf(pj, vs[jj][lane + 32 * t], acc[t]);
+    }
+    m = mnew;
+  }
+  if (active) {
+    const float inv = 1.f / l;
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) stf(O + base + (size_t)row * D + lane + 32 * t, acc[t] * inv);
+    if (lane == 0) LSE[head * N + row] = (m + log2f(l)) * kLn2;
+  }
+}
+
+// dK, dV: warp w -> key row j; steps over query rows i >= (first key of the CTA) when causal.
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarps * 32)
+simt_bwd_dkdv_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
+                     const T* __restrict__ dO, const float* __restrict__ LSE,
+                     const float* __restrict__ Dr, T* __restrict__ dK, T* __restrict__ dV, int N,
+                     int tiles, float scale, int causal) {
+  __shared__ float qs[kChunk][D + 1];
+  __shared__ float dos[kChunk][D + 1];
+  __shared__ float kr[kWarps][D];
+  __shared__ float vr[kWarps][D];
+  __shared__ float lse2[kChunk], dd[kChunk];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t head = blockIdx.x / tiles;
+  const int key0 = (blockIdx.x % tiles) * kWarps;
+  const int key = key0 + warp;
+  const bool active = key < N;
+  const size_t base = (size_t)head * N * D;
+  const float sl2 = scale * kLog2e;
+  for (int c = lane; c < D; c += 32) {
+    kr[warp][c] = active ? ldf(K + base + (size_t)key * D + c) * sl2 : 0.f;
+    vr[warp][c] = active ? ldf(V + base + (size_t)key * D + c) : 0.f;
+  }
+  float dk[D / 32], dv[D / 32];
+#pragma unroll
+  for (int t = 0; t < D / 32; ++t) dk[t] = dv[t] = 0.f;
+
+  const int i_start = causal ? (key0 / kChunk) * kChunk : 0;
+  for (int i0 = i_start; i0 < N; i0 += kChunk) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < kChunk * D; e += blockDim.x) {
+      const int r = e / D, c = e % D, i = i0 + r;
+      float qv = 0.f, dov = 0.f;
+      if (i < N) {
+        qv = ldf(Q + base + (size_t)i * D + c);
+        dov = ldf(dO + base + (size_t)i * D + c);
+      }
+      qs[r][c] = qv;
+      dos[r][c] = dov;
+    }
+    if (threadIdx.x < kChunk) {
+      const int i = i0 + threadIdx.x;
+      lse2[threadIdx.x] = i < N ? LSE[head * N + i] * kLog2e : 0.f;
+      dd[threadIdx.x] = i < N ? Dr[head * N + i] : 0.f;
+    }
+    __syncthreads();
+    const int i = i0 + lane;
+    float s = 0.f, dp = 0.f;
+#pragma unroll 16
+    for (int c = 0; c < D; ++c) {
+      s = fmaf(qs[lane][c], kr[warp][c], s);
+      dp = fmaf(dos[lane][c], vr[warp][c], dp);
+    }
+    const bool vis = active && i < N && (!causal || key <= i);
+    const float p = vis ? exp2f(s - lse2[lane]) : 0.f;
+    const float ds = p * (dp - dd[lane]);
+#pragma unroll 8
+    for (int ii = 0; ii < kChunk; ++ii) {
+      const float pi = __shfl_sync(0xffffffffu, p, ii);
+      const float dsi = __shfl_sync(0xffffffffu, ds, ii);
+#pragma unroll
+      for (int t = 0; t < D / 32; ++t) {
+        dv[t] = fmaf(pi, dos[ii][lane + 32 * t], dv[t]);
+        dk[t] = fmaf(dsi, qs[ii][lane + 32 * t], dk[t]);
+      }
+    }
+  }
+  if (active) {
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) {
+      stf(dV + base + (size_t)key * D + lane + 32 * t, dv[t]);
+      stf(dK + base + (size_t)key * D + lane + 32 * t, dk[t] * scale);
+    }
+  }
+}
+
+// dQ: warp w -> query row i; steps over keys j <= (last row of the CTA) when causal.
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarps * 32)
+simt_bwd_dq_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
+                   const T* __restrict__ dO, const float* __restrict__ LSE,
+                   const float* __restrict__ Dr, T* __restrict__ dQ, int N, int tiles, float scale,
+                   int causal) {
+  __shared__ float ks[kChunk][D + 1];
+  __shared__ float vs[kChunk][D + 1];
+  __shared__ float qr[kWarps][D];
+  __shared__ float dor[kWarps][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t head = blockIdx.x / tiles;
+  const int row0 = (blockIdx.x % tiles) * kWarps;
+  const int row = row0 + warp;
+  const bool active = row < N;
+  const size_t base = (size_t)head * N * D;
+  const float sl2 = scale * kLog2e;
+  for (int c = lane; c < D; c += 32) {
+    qr[warp][c] = active ? ldf(Q + base + (size_t)row * D + c) * sl2 : 0.f;
+    dor[warp][c] = active ? ldf(dO + base + (size_t)row * D + c) : 0.f;
+  }
+  const float lse2 = active ? LSE[head * N + row] * kLog2e : 0.f;
+  const float drow = active ? Dr[head * N + row] : 0.f;
+  float dq[D / 32];
+#pragma unroll
+  for (int t = 0; t < D / 32; ++t) dq[t] = 0.f;
+
+  const int kv_end = causal ? min(N, row0 + kWarps) : N;
+  for (int j0 = 0; j0 < kv_end; j0 += kChunk) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < kChunk * D; e += blockDim.x) {
+      const int r = e / D, c = e % D, j = j0 + r;
+      float kv = 0.f, vv = 0.f;
+      if (j < N) {
+        kv = ldf(K + base + (size_t)j * D + c);
+        vv = ldf(V + base + (size_t)j * D + c);
+      }
+      ks[r][c] = kv;
+      vs[r][c] = vv;
+    }
+    __syncthreads();
+    const int j = j0 + lane;
+    float s = 0.f, dp = 0.f;
+#pragma unroll 16
+    for (int c = 0; c < D; ++c) {
+      s = fmaf(qr[warp][c], ks[lane][c], s);
+      dp = fmaf(dor[warp][c], vs[lane][c], dp);
+    }
+    const bool vis = active && j < N && (!causal || j <= row);
+    const float p = vis ? exp2f(s - lse2) : 0.f;
+    const float ds = p * (dp - drow);
+#pragma unroll 8
+    for (int jj = 0; jj < kChunk; ++jj) {
+      const float dsj = __shfl_sync(0xffffffffu, ds, jj);
+#pragma unroll
+      for (int t = 0; t < D / 32; ++t) dq[t] = fmaf(dsj, ks[jj][lane + 32 * t], dq[t]);
+    }
+  }
+  if (active) {
+#pragma unroll
+    for (int t = 0; t < D / 32; ++t) stf(dQ + base + (size_t)row * D + lane + 32 * t, dq[t] * scale);
+  }
+}
+
+// D_i = sum_c dO_ic O_ic. Each thread reads 16 bytes of O and of dO; the G threads
+// that cover one row (G = row bytes / 16, a power of two <= 32) reduce by shuffles.
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+preprocess_kernel(const T* __restrict__ O, const T* __restrict__ dO, float* __restrict__ Dr,
+                  int64_t rows) {
+  constexpr int kVec = 16 / sizeof(T);
+  constexpr int G = D / kVec;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = tid / G;
+  const int part = (int)(tid % G);
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(O + row * D + part * kVec);
+    const uint4 b = *reinterpret_cast<const uint4*>(dO + row * D + part * kVec);
+    if constexpr (sizeof(T) == 2) {
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 fa = __bfloat1622float2(pa[u]);
+        const float2 fb = __bfloat1622float2(pb[u]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
+    } else {
+      const float* pa = reinterpret_cast<const float*>(&a);
+      const float* pb = reinterpret_cast<const float*>(&b);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc = fmaf(pa[u], pb[u], acc);
+    }
+  }
+#pragma unroll
+  for (int o = G / 2; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (row < rows && part == 0) Dr[row] = acc;
+}
+
+template <typename T, int D>
+cudaError_t launch_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                       const Shape& s, float scale, bool causal, cudaStream_t st) {
+  const int tiles = (s.N + kWarps - 1) / kWarps;
+  const int64_t grid = (int64_t)tiles * s.heads();
+  simt_fwd_kernel<T, D><<<(unsigned)grid, kWarps * 32, 0, st>>>(
+      (const T*)Q, (const T*)K, (const T*)V, (T*)O, LSE, s.N, tiles, scale, causal ? 1 : 0);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                       const float* LSE, const float* Dr, void* dQ, void* dK, void* dV,
+                       const Shape& s, float scale, bool causal, cudaStream_t st) {
+  const int tiles = (s.N + kWarps - 1) / kWarps;
+  const int64_t grid = (int64_t)tiles * s.heads();
+  simt_bwd_dkdv_kernel<T, D><<<(unsigned)grid, kWarps * 32, 0, st>>>(
+      (const T*)Q, (const T*)K, (const T*)V, (const T*)dO, LSE, Dr, (T*)dK, (T*)dV, s.N, tiles,
+      scale, causal ? 1 : 0);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  simt_bwd_dq_kernel<T, D><<<(unsigned)grid, kWarps * 32, 0, st>>>(
+      (const T*)Q, (const T*)K, (const T*)V, (const T*)dO, LSE, Dr, (T*)dQ, s.N, tiles, scale,
+      causal ? 1 : 0);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_pre(const void* O, const void* dO, float* Dr, const Shape& s, cudaStream_t st) {
+  constexpr int G = D / (16 / sizeof(T));
+  const int64_t threads = s.rows() * G;
+  const int64_t grid = (threads + 255) / 256;
+  preprocess_kernel<T, D><<<(unsigned)grid, 256, 0, st>>>((const T*)O, (const T*)dO, Dr, s.rows());
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t simt_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                     const Shape& s, float scale, bool causal, bool bf16, cudaStream_t st) {
+  if (bf16)
+    return s.d == 64 ? launch_fwd<__nv_bfloat16, 64>(Q, K, V, O, LSE, s, scale, causal, st)
+                     : launch_fwd<__nv_bfloat16, 128>(Q, K, V, O, LSE, s, scale, causal, st);
+  return s.d == 64 ? launch_fwd<float, 64>(Q, K, V, O, LSE, s, scale, causal, st)
+                   : launch_fwd<float, 128>(Q, K, V, O, LSE, s, scale, causal, st);
+}
+
+cudaError_t simt_bwd(const void* Q, const void* K, const void* V, const void* dO,
+                     const float* LSE, const float* D, void* dQ, void* dK, void* dV,
+                     const Shape& s, float scale, bool causal, bool bf16, cudaStream_t st) {
+  if (bf16)
+    return s.d == 64
+               ? launch_bwd<__nv_bfloat16, 64>(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal, st)
+               : launch_bwd<__nv_bfloat16, 128>(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal, st);
+  return s.d == 64 ? launch_bwd<float, 64>(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal, st)
+                   : launch_bwd<float, 128>(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal, st);
+}
+
+cudaError_t preprocess_d(const void* O, const void* dO, float* D, const Shape& s, bool bf16,
+                         cudaStream_t st) {
+  if (bf16)
+    return s.d == 64 ? launch_pre<__nv_bfloat16, 64>(O, dO, D, s, st)
+                     : launch_pre<__nv_bfloat16, 128>(O, dO, D, s, st);
+  return s.d == 64 ? launch_pre<float, 64>(O, dO, D, s, st) : launch_pre<float, 128>(O, dO, D, s, st);
+}
+
+}  // namespace fa

@@ -1,0 +1,119 @@
+/*
+ * fa.h — C ABI of the exact-attention library (GB300, sm_103a).
+ *
+ * Exact scaled-dot-product attention over contiguous [B, H, N, d] tensors, with no
+ * N x N matrix in device memory: the forward pass keeps O and one float per query
+ * row (LSE); the backward pass rebuilds the attention weights from LSE.
+ *
+ * Sources (web pages, by title and section):
+ *   "flash-attention-backpropagation" (aiqz.cc): 前向台账 (row max m, row sum l),
+ *       反向总览 (P rebuilt from the forward's statistics), Softmax梯度 (D, dP, dS),
+ *       QKV梯度 (dV, dQ, dK accumulated block by block).
+ *   "flash-attention-v2-sram-tiling" (aiqz.cc): §1 (Attention = softmax(QK^T/sqrt d)V),
+ *       §4 (tiling), §5 (online softmax), §6 (recompute and fusion), §7 (scale folding,
+ *       row-parallel work split).
+ *   "知识点13 FlashAttention深度攻略" (blog.xiaohack.org): 代码手撕 (causal mask j > i).
+ *
+ * Conventions shared by every entry point
+ *   Layout   Q, K, V, O, dO, dQ, dK, dV: contiguous row-major [B, H, N, d]; all share
+ *            one element type (dtype). LSE and D: contiguous float32 [B, H, N].
+ *   dtype    FA_DTYPE_BF16 (tensor-core path) or FA_DTYPE_FP32 (exact FFMA path).
+ *   Shapes   B, H, N >= 1; d in {64, 128}. bf16: N a multiple of 128.
+ *            fp32: N <= 4096. B*H*N*d must fit in a signed 64-bit count and B*H < 2^31.
+ *   scale    finite and > 0; scores are s_ij = scale * q_i . k_j (1/sqrt(d) on the pages).
+ *   causal   0: every key is visible. 1: key j is hidden from query i when j > i.
+ *   Pointers device pointers (cudaMalloc or torch), 16-byte aligned, non-overlapping
+ *            between inputs and outputs. The caller owns every buffer and the stream.
+ *   stream   a cudaStream_t passed as void* (NULL = legacy default stream). Every call
+ *            only enqueues work on it and returns; nothing synchronises.
+ *   Errors   Arguments are checked on the host before anything is launched: a bad
+ *            argument returns FA_ERR_INVALID_ARG or FA_ERR_UNSUPPORTED and touches no
+ *            buffer. A failed launch returns FA_ERR_CUDA. A device-side wait that runs
+ *            out of time records FA_ERR_DEVICE_TIMEOUT in a device status word, which
+ *            fa_get_last_device_status() reads after the caller synchronises.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,    /* null pointer, bad size/scale/alignment */
+  FA_ERR_UNSUPPORTED = 2,    /* valid but not implemented (d, N, dtype combination) */
+  FA_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
+  FA_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait gave up */
+  FA_ERR_WORKSPACE = 5       /* workspace missing or too small */
+} fa_status_t;
+
+typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP32 = 1 } fa_dtype_t;
+
+/*
+ * fa_fwd — attention forward.
+ *   O_i   = sum_j P_ij V_j,  P_ij = exp(s_ij - m_i) / l_i over the visible keys j,
+ *   LSE_i = m_i + ln(l_i),   m_i = max_j s_ij,  l_i = sum_j exp(s_ij - m_i).
+ * ("flash-attention-v2-sram-tiling" §1, §4, §5; "flash-attention-backpropagation" 前向台账.)
+ * In:  Q, K, V [B,H,N,d] dtype.   Out: O [B,H,N,d] dtype, LSE [B,H,N] float32.
+ * LSE is natural-log, in units of the scaled scores; it replaces the pages' (m, l) pair.
+ */
+FA_API fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                   int B, int H, int N, int d, float scale, int causal, int dtype,
+                   void* stream);
+
+/*
+ * fa_bwd_preprocess — D_i = sum_c dO_ic * O_ic ("flash-attention-backpropagation",
+ * Softmax梯度). In: O, dO [B,H,N,d] dtype. Out: D [B,H,N] float32.
+ */
+FA_API fa_status_t fa_bwd_preprocess(const void* O, const void* dO, float* D,
+                              int B, int H, int N, int d, int dtype, void* stream);
+
+/*
+ * fa_bwd_workspace_size — bytes of device workspace fa_bwd needs for these sizes
+ * (the float32 dQ accumulator of the bf16 path; 0 for fp32). Returns 0 for
+ * arguments fa_bwd would reject.
+ */
+FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d, int dtype);
+
+/*
+ * fa_bwd — attention backward from the forward's O and LSE.
+ *   P_ij  = exp(s_ij - LSE_i)          (P rebuilt, 反向总览 / 数值稳定)
+ *   dV_j  = sum_i P_ij dO_i            (QKV梯度)
+ *   dP_ij = dO_i . V_j,  dS_ij = P_ij (dP_ij - D_i)     (Softmax梯度)
+ *   dQ_i  = scale sum_j dS_ij K_j,  dK_j = scale sum_i dS_ij Q_i   (QKV梯度)
+ * In:  Q, K, V, O, dO [B,H,N,d] dtype; LSE [B,H,N] float32 from fa_fwd; D [B,H,N]
+ *      float32 from fa_bwd_preprocess, or NULL, in which case fa_bwd computes it
+ *      first into the workspace (the size query then includes room for it).
+ * Out: dQ, dK, dV [B,H,N,d] dtype (overwritten).
+ * workspace: device buffer of at least fa_bwd_workspace_size(...) bytes (plus
+ *      4*B*H*N bytes when D is NULL); its contents on entry do not matter.
+ */
+FA_API fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O,
+                   const void* dO, const float* LSE, const float* D,
+                   void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                   int B, int H, int N, int d, float scale, int causal, int dtype,
+                   void* stream);
+
+/* Text for a status code (static storage; never NULL). */
+FA_API const char* fa_get_error_string(fa_status_t status);
+
+/*
+ * fa_get_last_device_status — reads and clears the device status word of the
+ * current device. Call it after synchronising the streams the library ran on.
+ * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, or FA_ERR_CUDA if the read itself failed.
+ */
+FA_API fa_status_t fa_get_last_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_GB300_H */

@@ -1,0 +1,112 @@
+"""Host-side checks of the C ABI: the library builds, loads without a GPU, exports every
+function include/fa.h declares, and rejects bad arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_02_gb300.build import build
+    path = build()
+    import exact_attention_02_gb300 as fa
+    assert os.path.samefile(path, fa.LIB_PATH)
+    return fa.lib()
+
+
+def _declared():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"^FA_API\s+[\w\s\*]+?\b(\w+)\s*\(", src, flags=re.M)
+    return names
+
+
+def test_header_declares_the_boundary():
+    assert set(_declared()) >= {"fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_bwd_workspace_size",
+                                "fa_get_error_string", "fa_get_last_device_status"}
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_error_strings(lib):
+    import exact_attention_02_gb300 as fa
+    for code in range(6):
+        assert fa.error_string(code).startswith("FA_")
+    assert "unknown" in fa.error_string(99)
+
+
+def test_workspace_size(lib):
+    import exact_attention_02_gb300 as fa
+    assert fa.fa_bwd_workspace_size(2, 16, 8192, 128, fa.FA_DTYPE_BF16) == 2 * 16 * 8192 * 128 * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 128, 64, fa.FA_DTYPE_FP32) == 0
+    assert fa.fa_bwd_workspace_size(1, 1, 100, 64, fa.FA_DTYPE_BF16) == 0  # rejected shape
+    assert fa.fa_bwd_workspace_size(0, 1, 128, 64, fa.FA_DTYPE_BF16) == 0
+
+
+P = 0x10000  # a 16-byte-aligned dummy address: never dereferenced, calls fail validation first
+GOOD = dict(B=1, H=1, N=128, d=64, scale=0.125, causal=0, dtype=0)
+
+
+def _fwd(lib, ptrs=(P, P, P, P, P), **kw):
+    a = dict(GOOD, **kw)
+    return lib.fa_fwd(*[ctypes.c_void_p(p) for p in ptrs], a["B"], a["H"], a["N"], a["d"],
+                      ctypes.c_float(a["scale"]), a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), 1), (dict(H=-1), 1), (dict(N=0), 1), (dict(d=0), 1),
+    (dict(d=96), 2), (dict(d=256), 2), (dict(N=100), 2), (dict(N=8192 + 64), 2),
+    (dict(dtype=1, N=8192), 2), (dict(dtype=7), 1),
+    (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=float("nan")), 1),
+    (dict(scale=float("inf")), 1), (dict(causal=2), 1),
+    (dict(B=1 << 16, H=1 << 15), 1),
+])
+def test_fwd_rejects(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+@pytest.mark.parametrize("ptrs", [(0, P, P, P, P), (P, P, P, P, 0), (P + 2, P, P, P, P),
+                                  (P, P, P + 8, P, P)])
+def test_fwd_rejects_pointers(lib, ptrs):
+    assert _fwd(lib, ptrs=ptrs) == 1
+
+
+def test_preprocess_rejects(lib):
+    vp = ctypes.c_void_p
+    assert lib.fa_bwd_preprocess(vp(0), vp(P), vp(P), 1, 1, 128, 64, 0, None) == 1
+    assert lib.fa_bwd_preprocess(vp(P), vp(P), vp(P), 1, 1, 128, 80, 0, None) == 2
+
+
+def _bwd(lib, D=P, ws=P, wsb=1 << 30, **kw):
+    a = dict(GOOD, **kw)
+    vp = ctypes.c_void_p
+    return lib.fa_bwd(vp(P), vp(P), vp(P), vp(P), vp(P), vp(P), vp(D), vp(P), vp(P), vp(P), vp(ws),
+                      ctypes.c_size_t(wsb), a["B"], a["H"], a["N"], a["d"], ctypes.c_float(a["scale"]),
+                      a["causal"], a["dtype"], None)
+
+
+def test_bwd_rejects(lib):
+    assert _bwd(lib, N=130) == 2
+    assert _bwd(lib, scale=0.0) == 1
+    assert _bwd(lib, D=P + 4) == 1
+    assert _bwd(lib, ws=0) == 5                          # bf16 needs the dQ accumulator
+    assert _bwd(lib, wsb=128 * 64 * 4 - 16) == 5         # one row short
+    assert _bwd(lib, D=0, wsb=128 * 64 * 4) == 5         # no room for D
+    assert _bwd(lib, ws=P + 8) == 1
+
+
+def test_binding_refuses_to_run_without_library(monkeypatch):
+    import exact_attention_02_gb300 as fa
+    monkeypatch.setattr(fa, "_lib", None)
+    monkeypatch.setattr(fa, "LIB_PATH", os.path.join(ROOT, "does_not_exist.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        fa.lib()
