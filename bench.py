@@ -153,16 +153,20 @@ def run_reference(args, w):
 
 
 def count_launches(step):
-    """Kernels one step launches, counted with the CUDA activity profiler."""
+    """Kernels one step launches, counted with the CUDA activity profiler (CUPTI)."""
     import torch
     try:
         from torch.profiler import ProfilerActivity, profile
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
             step()
             torch.cuda.synchronize()
-        names = [e.name for e in prof.events() if str(getattr(e, "device_type", "")).endswith("CUDA")]
-        ours = [n for n in names if "fa::" in n or n.startswith("_ZN2fa")]
-        return len(ours), sorted(set(ours))
+        evs = list(prof.events())
+        kern = [e.name for e in evs if "CUDA" in str(getattr(e, "device_type", "")).upper()]
+        ours = [n for n in kern if "fa::" in n or "_ZN2fa" in n or "fa_" in n]
+        if not ours:
+            seen = sorted({f"{getattr(e, 'device_type', '?')}:{e.name[:60]}" for e in evs})[:12]
+            return None, ["no library kernels seen by the profiler"] + seen
+        return len(ours), sorted(set(n.split("(")[0][:120] for n in ours))
     except Exception as e:  # profiler unavailable: report nothing rather than guess
         return None, [f"profiler unavailable: {e}"]
 
@@ -299,22 +303,22 @@ def run_ours(args, w):
     pre_bytes = 2 * rows * w.d * esz + rows * 4
     kern = {"fa_fwd": fwd_ms, "fa_bwd": bwd_ms, "fa_bwd_preprocess": pre_ms}
     dominant = max(kern, key=kern.get)
-    tensor_path = w.dtype == "bf16" and fa.TENSOR_CORE_PATH
-    if tensor_path:
+    bound = fa.BF16_KERNEL_BOUND[dominant] if w.dtype == "bf16" else ("hbm" if dominant == "fa_bwd_preprocess" else "alu")
+    dom_flop = {"fa_fwd": w.fwd_flop(), "fa_bwd": w.bwd_flop()}.get(dominant)
+    if bound == "tensor":
         peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
         peak_desc = f"bf16 dense, sustained ({peak_src})"
-        bound, unit = "tensor", "TFLOP/s"
-    else:
+        unit = "TFLOP/s"
+        achieved = dom_flop / (kern[dominant] * 1e-3) / 1e12
+    elif bound == "alu":
         # FFMA path: 152 SMs x 128 FMA/clk x 2 FLOP x max SM clock
         peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         peak_desc = "fp32 FFMA: 152 SMs x 128 FMA/clk x 2 x max SM clock (derived)"
-        bound, unit = "alu", "TFLOP/s"
-    dom_flop = {"fa_fwd": w.fwd_flop(), "fa_bwd": w.bwd_flop()}.get(dominant)
-    if dom_flop is None:
-        achieved = pre_bytes / (pre_ms * 1e-3) / 1e9
-        peak, bound, unit, peak_desc = peaks["hbm_gbs"], "hbm", "GB/s", f"HBM copy ({peak_src})"
-    else:
+        unit = "TFLOP/s"
         achieved = dom_flop / (kern[dominant] * 1e-3) / 1e12
+    else:
+        achieved = pre_bytes / (pre_ms * 1e-3) / 1e9
+        peak, unit, peak_desc = peaks["hbm_gbs"], "GB/s", f"HBM copy ({peak_src})"
     roofline = {"kernel": dominant, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "peak_source": peak_desc, "traffic": None}
 
@@ -336,8 +340,10 @@ def run_ours(args, w):
         "clocks": clk,
         "e2e": e2e,
     }
-    line["fwd"]["frac_peak"] = line["fwd"]["tflops"] / peak if bound == "tensor" else None
-    line["bwd"]["frac_peak"] = line["bwd"]["tflops"] / peak if bound == "tensor" else None
+    tpeak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    line["fwd"]["frac_tensor_peak"] = line["fwd"]["tflops"] / tpeak if w.dtype == "bf16" else None
+    line["bwd"]["frac_tensor_peak"] = line["bwd"]["tflops"] / tpeak if w.dtype == "bf16" else None
+    line["frac_tensor_peak"] = value / world / tpeak if w.dtype == "bf16" else None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x)
     if rank == 0:

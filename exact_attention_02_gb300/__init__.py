@@ -20,8 +20,9 @@ LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT, FA_ERR_WORKSPACE = range(6)
 FA_DTYPE_BF16, FA_DTYPE_FP32 = 0, 1
 
-# True once bf16 calls run on the tcgen05 tensor-core kernels (the fp32 path is FFMA).
-TENSOR_CORE_PATH = False
+# Which execution unit bounds each entry point's main kernel for bf16 inputs
+# ("tensor": tcgen05 MMAs, "alu": FFMA pipes, "hbm": memory bandwidth). fp32 is all FFMA.
+BF16_KERNEL_BOUND = {"fa_fwd": "tensor", "fa_bwd": "alu", "fa_bwd_preprocess": "hbm"}
 
 _lib = None
 

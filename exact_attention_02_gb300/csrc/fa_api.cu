@@ -36,6 +36,8 @@ fa_status_t check_shape(const Shape& s, int dtype, float* scale) {
   if (scale && !(isfinite(*scale) && *scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (s.d != 64 && s.d != 128) return FA_ERR_UNSUPPORTED;
   if (dtype == FA_DTYPE_BF16 && s.N % 128 != 0) return FA_ERR_UNSUPPORTED;
+  // TMA coordinates are 32-bit row indices into the [B*H*N, d] view.
+  if (dtype == FA_DTYPE_BF16 && bh * s.N > INT32_MAX) return FA_ERR_UNSUPPORTED;
   if (dtype == FA_DTYPE_FP32 && s.N > 4096) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -62,8 +64,12 @@ extern "C" fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void*
   if ((r = fa::check_ptrs({Q, K, V, O, LSE})) != FA_OK) return r;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return fa::from_cuda(
-      fa::simt_fwd(Q, K, V, O, LSE, s, scale, causal == 1, dtype == FA_DTYPE_BF16, st));
+  if (dtype == FA_DTYPE_BF16) {
+    int* status = fa::device_status_ptr();
+    if (!status) return FA_ERR_CUDA;
+    return fa::from_cuda(fa::tc_fwd(Q, K, V, O, LSE, s, scale, causal == 1, status, st));
+  }
+  return fa::from_cuda(fa::simt_fwd(Q, K, V, O, LSE, s, scale, causal == 1, false, st));
 }
 
 extern "C" fa_status_t fa_bwd_preprocess(const void* O, const void* dO, float* D, int B, int H,

@@ -1,0 +1,362 @@
+// Attention forward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), bf16 in,
+// fp32 accumulate; what it computes is fa_fwd in include/fa.h.
+//
+// Method ("flash-attention-v2-sram-tiling" §4-§7): Q is cut into 128-row tiles, K/V
+// stream past in 128-row tiles, and each query row keeps a running max m and sum l
+// (the online softmax of §5, merged as in "知识点13" section 4). S and P never leave
+// the chip: S = Q K^T lands in TMEM, the softmax warps turn it into P (bf16) in place,
+// and O += P V accumulates in TMEM. The 1/sqrt(d) scale and log2(e) are folded into a
+// single multiplier so every exponential is one FFMA + one ex2 (§7, scale folding).
+//
+// CTA = two 128-row Q tiles of one head (rows 256*pair .. +255), 10 warps:
+//   warps 0-3  softmax for Q tile 0 (one thread per row = one TMEM lane)
+//   warps 4-7  softmax for Q tile 1
+//   warp 8     TMA producer: Q once, then K_j / V_j into a ring of shared-memory stages
+//   warp 9     MMA issuer (one thread): S_t = Q_t K_j^T, O_t += P_t V_j
+// The two tiles ping-pong: while one warpgroup exponentiates S_0, the tensor core works
+// on tile 1, and the other way round.
+//
+// TMEM (512 columns x 128 lanes): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
+// O_1 [256+d, 256+2d). P_t (bf16 pairs) overwrites the first 64 columns of S_t.
+//
+// Lazy rescale: O and l are rescaled only when the row max grows by more than 8 (log2
+// units); otherwise P uses the stale max (values <= 2^8). The result is exact because
+// O and l always share the same reference max, and O / l cancels it.
+//
+// Causal: tile t sees K tiles 0..qtile_t; the diagonal tile masks key > query.
+#include <cuda_bf16.h>
+
+#include "fa_internal.h"
+#include "sm100_ptx.cuh"
+#include "tma_host.h"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;  // query rows per Q tile
+constexpr int BN = 128;  // keys per K/V tile
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kBoxBytes = BM * 128;  // one [128 rows x 64 bf16] swizzled box
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTileBytes = BM * D * 2;
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kVOff + kStages * kTileBytes + 1024;
+  __device__ static constexpr uint32_t colS(int t) { return t ? 128u : 0u; }
+  __device__ static constexpr uint32_t colO(int t) { return t ? 256u + D : 256u; }
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+struct FwdParams {
+  __nv_bfloat16* O;
+  float* LSE;
+  int* status;
+  int N;
+  int heads;
+  int qtiles;
+  int pairs;
+  int causal;
+  float sl2;  // scale * log2(e)
+};
+
+struct FwdCtl {
+  uint64_t q_full;
+  uint64_t k_full[4], v_full[4], kv_empty[4];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ FwdCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  int pair, head;
+  if (p.causal) {  // heaviest pairs first
+    pair = p.pairs - 1 - (int)(blockIdx.x / p.heads);
+    head = (int)(blockIdx.x % p.heads);
+  } else {
+    pair = (int)(blockIdx.x % p.pairs);
+    head = (int)(blockIdx.x / p.pairs);
+  }
+  const int qt0 = 2 * pair;
+  const bool act1 = qt0 + 1 < p.qtiles;
+  const int nkv0 = p.causal ? qt0 + 1 : p.qtiles;
+  const int nkv1 = act1 ? (p.causal ? qt0 + 2 : p.qtiles) : 0;
+  const int nkv = max(nkv0, nkv1);
+  const int row_base = head * p.N;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl.q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&ctl.k_full[s], 1);
+      mbar_init(&ctl.v_full[s], 1);
+      mbar_init(&ctl.kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&ctl.s_full[t], 1);
+      mbar_init(&ctl.p_full[t], 128);
+      mbar_init(&ctl.o_full[t], 1);
+    }
+    mbar_init(&ctl.drain, 1);
+    ctl.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&ctl.tmem_base, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int* abort = &ctl.abort;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_expect_tx(&ctl.q_full, (act1 ? 2 : 1) * C::kTileBytes);
+      for (int t = 0; t < (act1 ? 2 : 1); ++t)
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_2d(smem + C::kQOff + (t * C::kBoxes + b) * kBoxBytes, &tmQ, &ctl.q_full, b * 64,
+                      row_base + (qt0 + t) * BM);
+      int last[4] = {-1, -1, -1, -1};
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % C::kStages;
+        if (j >= C::kStages && !mbar_wait(&ctl.kv_empty[s], ((j / C::kStages) - 1) & 1, p.status, abort))
+          break;
+        mbar_expect_tx(&ctl.k_full[s], C::kTileBytes);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_2d(smem + C::kKOff + (s * C::kBoxes + b) * kBoxBytes, &tmK, &ctl.k_full[s], b * 64,
+                      row_base + j * BN);
+        mbar_expect_tx(&ctl.v_full[s], C::kTileBytes);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_2d(smem + C::kVOff + (s * C::kBoxes + b) * kBoxBytes, &tmV, &ctl.v_full[s], b * 64,
+                      row_base + j * BN);
+        last[s] = j;
+      }
+      // Every issued copy must land before the CTA may exit.
+      mbar_wait(&ctl.q_full, 0, p.status, nullptr);
+      for (int s = 0; s < C::kStages; ++s)
+        if (last[s] >= 0) {
+          mbar_wait(&ctl.k_full[s], (last[s] / C::kStages) & 1, p.status, nullptr);
+          mbar_wait(&ctl.v_full[s], (last[s] / C::kStages) & 1, p.status, nullptr);
+        }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(BM, BN, false, false);
+      constexpr uint32_t idO = idesc_bf16(BM, D, false, true);
+      const uint32_t sQ = smem_u32(smem + C::kQOff);
+      const uint32_t sK = smem_u32(smem + C::kKOff);
+      const uint32_t sV = smem_u32(smem + C::kVOff);
+      auto issue_S = [&](int t, int s) {
+        const uint32_t qa = sQ + t * C::kBoxes * kBoxBytes, ka = sK + s * C::kBoxes * kBoxBytes;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32;
+          mma_ss(tmem + C::colS(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS,
+                 k > 0);
+        }
+      };
+      auto issue_PV = [&](int t, int s, bool acc) {
+        const uint32_t va = sV + s * C::kBoxes * kBoxBytes;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ts(tmem + C::colO(t), tmem + C::colS(t) + k * 8, sdesc_sw128(va + k * 2048, kBoxBytes, 1024), idO,
+                 (acc || k > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(&ctl.q_full, 0, p.status, abort) && mbar_wait(&ctl.k_full[0], 0, p.status, abort);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0, 0);
+        mma_commit(&ctl.s_full[0]);
+        if (nkv1 > 0) {
+          issue_S(1, 0);
+          mma_commit(&ctl.s_full[1]);
+        }
+      }
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int s = j % C::kStages;
+        ok = mbar_wait(&ctl.v_full[s], (j / C::kStages) & 1, p.status, abort);
+        bool k_next = false;
+        for (int t = 0; ok && t < 2; ++t) {
+          const int nk = t ? nkv1 : nkv0;
+          if (j >= nk) continue;
+          if (!(ok = mbar_wait(&ctl.p_full[t], j & 1, p.status, abort))) break;
+          tc_fence_after();
+          issue_PV(t, s, j > 0);
+          if (j + 1 < nk) {
+            if (!k_next) {
+              const int s2 = (j + 1) % C::kStages;
+              if (!(ok = mbar_wait(&ctl.k_full[s2], ((j + 1) / C::kStages) & 1, p.status, abort))) break;
+              tc_fence_after();
+              k_next = true;
+            }
+            issue_S(t, (j + 1) % C::kStages);
+            mma_commit(&ctl.s_full[t]);
+          } else {
+            mma_commit(&ctl.o_full[t]);
+          }
+        }
+        mma_commit(&ctl.kv_empty[s]);
+      }
+      // All MMAs must retire before TMEM is released.
+      mma_commit(&ctl.drain);
+      mbar_wait(&ctl.drain, 0, p.status, nullptr);
+    }
+  } else {
+    // ---------------- softmax warpgroups ----------------
+    const int t = warp >> 2;
+    const int nk = t ? nkv1 : nkv0;
+    const int r = (warp & 3) * 32 + lane;       // row in the tile = TMEM lane
+    const int qrow = (qt0 + t) * BM + r;        // query position in the head
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::colS(t);
+    const uint32_t tO = tmem + lane_off + C::colO(t);
+    const float sl2 = p.sl2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = nk > 0;
+    // tcgen05.ld/st are warp-collective (.sync.aligned): every branch that guards one
+    // is made uniform across the warp, including the outcome of each bounded wait.
+    for (int j = 0; ok && j < nk; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full[t], j & 1, p.status, abort));
+      if (!ok) break;
+      tc_fence_after();
+      float sv[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<float(*)[32]>(&sv[32 * c]));
+      if (p.causal && j == qt0 + t) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c > r) sv[c] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, sv[c]);
+      const float m_new = fmaxf(m, mx * sl2);
+      const bool grow = m_new > m + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, grow)) {
+        const float corr = grow ? ex2(m - m_new) : 1.f;
+        l *= corr;
+        if (j > 0) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float ov[32];
+            tmem_ld32(tO + c0, ov);
+            uint32_t w0[16], w1[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              w0[u] = __float_as_uint(ov[u] * corr);
+              w1[u] = __float_as_uint(ov[16 + u] * corr);
+            }
+            tmem_st16(tO + c0, w0);
+            tmem_st16(tO + c0 + 16, w1);
+          }
+        }
+        if (grow) m = m_new;
+      }
+      const float neg_m = -m;
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const float p0 = ex2(fmaf(sv[32 * q + 2 * u], sl2, neg_m));
+          const float p1 = ex2(fmaf(sv[32 * q + 2 * u + 1], sl2, neg_m));
+          rs0 += p0;
+          rs1 += p1;
+          pk[u] = pack_bf16(p0, p1);
+        }
+        tmem_st16(tS + 16 * q, pk);
+      }
+      l += rs0 + rs1;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&ctl.p_full[t]);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.o_full[t], 0, p.status, abort));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = p.O + (size_t)(row_base + qrow) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float ov[32];
+        tmem_ld32(tO + c0, ov);
+        uint4 w[4];
+        uint32_t* wu = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(ov[2 * u] * inv_l, ov[2 * u + 1] * inv_l);
+        uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = w[u];
+      }
+      p.LSE[row_base + qrow] = (m + log2f(l)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                   float scale, bool causal, int* status, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  CUtensorMap mq, mk, mv;
+  const int64_t rows = s.rows();
+  if (!make_map_bf16_2d(&mq, Q, rows, D, BM) || !make_map_bf16_2d(&mk, K, rows, D, BN) ||
+      !make_map_bf16_2d(&mv, V, rows, D, BN))
+    return cudaErrorInvalidValue;
+  static bool attr = [] {
+    return cudaFuncSetAttribute(fa_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmemBytes) == cudaSuccess;
+  }();
+  if (!attr) return cudaErrorInvalidConfiguration;
+  FwdParams p;
+  p.O = static_cast<__nv_bfloat16*>(O);
+  p.LSE = LSE;
+  p.status = status;
+  p.N = s.N;
+  p.heads = (int)s.heads();
+  p.qtiles = s.N / BM;
+  p.pairs = (p.qtiles + 1) / 2;
+  p.causal = causal ? 1 : 0;
+  p.sl2 = scale * 1.4426950408889634f;
+  const int64_t grid = (int64_t)p.pairs * p.heads;
+  fa_fwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                   float scale, bool causal, int* status, cudaStream_t st) {
+  return s.d == 64 ? launch<64>(Q, K, V, O, LSE, s, scale, causal, status, st)
+                   : launch<128>(Q, K, V, O, LSE, s, scale, causal, status, st);
+}
+
+}  // namespace fa

@@ -28,6 +28,10 @@ cudaError_t simt_bwd(const void* Q, const void* K, const void* V, const void* dO
                      const float* LSE, const float* D, void* dQ, void* dK, void* dV,
                      const Shape& s, float scale, bool causal, bool bf16, cudaStream_t st);
 
+// ---- tcgen05 tensor-core path (bf16, d in {64, 128}, N % 128 == 0) ----
+cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                   float scale, bool causal, int* status, cudaStream_t st);
+
 // ---- memory-bound helpers (fa_simt.cu) ----
 cudaError_t preprocess_d(const void* O, const void* dO, float* D, const Shape& s, bool bf16,
                          cudaStream_t st);

@@ -69,17 +69,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits until the phase with parity `parity` of `bar` has completed. Gives up after
 // kWaitLimitNs, or at once when *abort is set by another role of the CTA; on giving up
-// it records FA_ERR_DEVICE_TIMEOUT in *status, sets *abort and returns false.
+// it records FA_ERR_DEVICE_TIMEOUT in *status, sets *abort and returns false. A null
+// `abort` means: ignore other roles and wait (still bounded), as the drain paths need.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
+    if (abort && *abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       if (status) atomicExch(status, kErrTimeout);
-      *abort = 1;
+      if (abort) *abort = 1;
       return false;
     }
   }
