@@ -22,7 +22,7 @@ FA_DTYPE_BF16, FA_DTYPE_FP32 = 0, 1
 
 # Which execution unit bounds each entry point's main kernel for bf16 inputs
 # ("tensor": tcgen05 MMAs, "alu": FFMA pipes, "hbm": memory bandwidth). fp32 is all FFMA.
-BF16_KERNEL_BOUND = {"fa_fwd": "tensor", "fa_bwd": "alu", "fa_bwd_preprocess": "hbm"}
+BF16_KERNEL_BOUND = {"fa_fwd": "tensor", "fa_bwd": "tensor", "fa_bwd_preprocess": "hbm"}
 
 _lib = None
 

@@ -112,7 +112,13 @@ extern "C" fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const
     if ((r = fa::from_cuda(fa::preprocess_d(O, dO, Dw, s, bf16, st))) != FA_OK) return r;
     D = Dw;
   }
-  return fa::from_cuda(fa::simt_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal == 1, bf16, st));
+  if (bf16) {
+    int* status = fa::device_status_ptr();
+    if (!status) return FA_ERR_CUDA;
+    return fa::from_cuda(fa::tc_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, static_cast<float*>(workspace), s,
+                                    scale, causal == 1, status, st));
+  }
+  return fa::from_cuda(fa::simt_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal == 1, false, st));
 }
 
 extern "C" const char* fa_get_error_string(fa_status_t status) {

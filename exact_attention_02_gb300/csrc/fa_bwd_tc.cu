@@ -1,0 +1,449 @@
+// Attention backward on the tcgen05 tensor cores (bf16 in, fp32 accumulate); what it
+// computes is fa_bwd in include/fa.h.
+//
+// Method ("flash-attention-backpropagation", 反向总览 / Softmax梯度 / QKV梯度): the
+// outer loop runs over key/value tiles (one 128-key tile per CTA), the inner loop over
+// query tiles; P is rebuilt from the forward's LSE, and one recompute of each (i, j)
+// tile yields dV, dK and dQ together (the single-recompute loop the Ascend page
+// "FlashAttention 反向传播" recommends over one pass per gradient). All accumulators
+// are fp32 and are rounded to bf16 once, on write-back.
+//
+// Working in the transposed frame puts the 128 keys of the CTA on the 128 TMEM lanes:
+//   S^T  = K_j Q_i^T          [keys x queries]   tcgen05, A,B = smem (K-major)
+//   dP^T = V_j dO_i^T         [keys x queries]   tcgen05
+//   P^T  = exp2(S^T * scale*log2e - LSE_i*log2e), masked (causal: key > query)
+//   dS^T = P^T * (dP^T - D_i)                     softmax warps, one thread per key
+//   dV_j += P^T dO_i          TMEM accumulator    A = P^T from TMEM
+//   dK_j += dS^T Q_i          TMEM accumulator    A = dS^T from smem (K-major)
+//   d = 128: dQ_i^T = K_j^T dS^T   (lanes = head dim)   A = K_j (MN-major), B = dS^T (MN-major)
+//   d =  64: dQ_i   = dS K_j       (lanes = queries)    A = dS^T (MN-major), B = K_j (MN-major)
+// and dQ partials are added into an fp32 accumulator in global memory (one red.add per
+// element); a last pass scales it by `scale` and rounds to bf16.
+//
+// CTA = 14 warps: 0-7 softmax (two warpgroups split the query columns), 8-11 dQ
+// reduction + dK/dV epilogue, 12 TMA producer, 13 MMA issuer. Query tiles are BQ = 64
+// rows for d = 128 and 128 rows for d = 64, so TMEM holds dV, dK, S^T, dP^T, dQ and P^T
+// at once (448 / 512 columns).
+// Pipelining: S/dP of tile i+1 are issued right after dV(i) and before dK(i)/dQ(i), so
+// the softmax warps work on tile i+1 while the tensor core finishes tile i.
+#include <cuda_bf16.h>
+
+#include "fa_internal.h"
+#include "sm100_ptx.cuh"
+#include "tma_host.h"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+constexpr int BN = 128;  // keys per CTA
+constexpr int kThreads = 448;
+constexpr int kDqWarp0 = 8;
+constexpr int kLoadWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BQ = D == 128 ? 64 : 128;     // queries per tile
+  static constexpr bool kDqT = D == 128;             // dQ^T (lanes = head dim) or dQ (lanes = queries)
+  static constexpr int kBoxes = D / 64;              // 64-column boxes per row
+  static constexpr int kKVBytes = BN * D * 2;        // K_j or V_j
+  static constexpr int kQBox = BQ * 128;             // one [BQ x 64] box of Q_i / dO_i
+  static constexpr int kQBytes = BQ * D * 2;
+  static constexpr int kStages = 3;
+  static constexpr int kDsBytes = BN * BQ * 2;       // dS^T [keys x queries] bf16
+  // shared-memory layout
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kKVBytes;
+  static constexpr int kStageOff = kVOff + kKVBytes;
+  static constexpr int kStageBytes = 2 * kQBytes;    // Q_i then dO_i
+  static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
+  static constexpr int kVecOff = kDsOff + 2 * kDsBytes;        // LSE_i, D_i per stage
+  static constexpr int kVecBytes = 2 * BQ * 4;
+  static constexpr int kSmemBytes = kVecOff + kStages * kVecBytes + 1024;
+  // TMEM columns
+  static constexpr uint32_t kColDV = 0;
+  static constexpr uint32_t kColDK = D;
+  static constexpr uint32_t kColS = 2 * D;
+  static constexpr uint32_t kColDP = 2 * D + BQ;
+  static constexpr uint32_t kColDQ = 2 * D + 2 * BQ;
+  static constexpr uint32_t kColP = kColDQ + (kDqT ? BQ : D);
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColP + BQ / 2 <= 512, "TMEM budget");
+  static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
+};
+
+struct BwdParams {
+  const float* LSE;
+  const float* Dvec;
+  float* dQacc;
+  __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+  int* status;
+  int N;
+  int heads;
+  int kvtiles;
+  int qtiles;
+  int causal;
+  float scale;
+  float sl2;  // scale * log2(e)
+};
+
+struct BwdCtl {
+  uint64_t kv_full, stage_full[3], stage_empty[3];
+  uint64_t s_full, sm_done, dq_full, dq_empty, kv_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                 const BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int BQ = C::BQ;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ BwdCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  int kt, head;
+  if (p.causal) {  // key tiles near the start see the most queries: launch them first
+    kt = (int)(blockIdx.x / p.heads);
+    head = (int)(blockIdx.x % p.heads);
+  } else {
+    kt = (int)(blockIdx.x % p.kvtiles);
+    head = (int)(blockIdx.x / p.kvtiles);
+  }
+  const int row_base = head * p.N;
+  const int q_first = p.causal ? (kt * BN) / BQ : 0;
+  const int nq = p.qtiles - q_first;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl.kv_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&ctl.stage_full[s], 1);
+      mbar_init(&ctl.stage_empty[s], 1);
+    }
+    mbar_init(&ctl.s_full, 1);
+    mbar_init(&ctl.sm_done, 256);
+    mbar_init(&ctl.dq_full, 1);
+    mbar_init(&ctl.dq_empty, 128);
+    mbar_init(&ctl.kv_done, 1);
+    mbar_init(&ctl.drain, 1);
+    ctl.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&ctl.tmem_base, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int* abort = &ctl.abort;
+  uint8_t* sK = smem + C::kKOff;
+  uint8_t* sV = smem + C::kVOff;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmdO);
+      mbar_expect_tx(&ctl.kv_full, 2 * C::kKVBytes);
+      for (int b = 0; b < C::kBoxes; ++b) {
+        tma_load_2d(sK + b * (BN * 128), &tmK, &ctl.kv_full, b * 64, row_base + kt * BN);
+        tma_load_2d(sV + b * (BN * 128), &tmV, &ctl.kv_full, b * 64, row_base + kt * BN);
+      }
+      int last[3] = {-1, -1, -1};
+      for (int it = 0; it < nq; ++it) {
+        const int s = it % C::kStages;
+        if (it >= C::kStages && !mbar_wait(&ctl.stage_empty[s], ((it / C::kStages) - 1) & 1, p.status, abort))
+          break;
+        const int qrow = row_base + (q_first + it) * BQ;
+        uint8_t* st = smem + C::kStageOff + s * C::kStageBytes;
+        float* vec = reinterpret_cast<float*>(smem + C::kVecOff + s * C::kVecBytes);
+        mbar_expect_tx(&ctl.stage_full[s], C::kStageBytes + C::kVecBytes);
+        for (int b = 0; b < C::kBoxes; ++b) {
+          tma_load_2d(st + b * C::kQBox, &tmQ, &ctl.stage_full[s], b * 64, qrow);
+          tma_load_2d(st + C::kQBytes + b * C::kQBox, &tmdO, &ctl.stage_full[s], b * 64, qrow);
+        }
+        bulk_load(vec, p.LSE + qrow, BQ * 4, &ctl.stage_full[s]);
+        bulk_load(vec + BQ, p.Dvec + qrow, BQ * 4, &ctl.stage_full[s]);
+        last[s] = it;
+      }
+      mbar_wait(&ctl.kv_full, 0, p.status, nullptr);
+      for (int s = 0; s < C::kStages; ++s)
+        if (last[s] >= 0) mbar_wait(&ctl.stage_full[s], (last[s] / C::kStages) & 1, p.status, nullptr);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idSP = idesc_bf16(BN, BQ, false, false);   // S^T, dP^T
+      constexpr uint32_t idKV = idesc_bf16(BN, D, false, true);     // dV, dK
+      constexpr uint32_t idQ = C::kDqT ? idesc_bf16(D, BQ, true, true) : idesc_bf16(BQ, D, true, true);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+      const uint32_t aStage = smem_u32(smem + C::kStageOff);
+      const uint32_t aDs = smem_u32(smem + C::kDsOff);
+      auto issue_S_dP = [&](int s) {
+        const uint32_t q = aStage + s * C::kStageBytes, o = q + C::kQBytes;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t offKV = (k / 4) * (BN * 128) + (k % 4) * 32;
+          const uint32_t offQ = (k / 4) * C::kQBox + (k % 4) * 32;
+          mma_ss(tmem + C::kColS, sdesc_sw128(aK + offKV, 16, 1024), sdesc_sw128(q + offQ, 16, 1024), idSP, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t offKV = (k / 4) * (BN * 128) + (k % 4) * 32;
+          const uint32_t offQ = (k / 4) * C::kQBox + (k % 4) * 32;
+          mma_ss(tmem + C::kColDP, sdesc_sw128(aV + offKV, 16, 1024), sdesc_sw128(o + offQ, 16, 1024), idSP, k > 0);
+        }
+      };
+      bool ok = mbar_wait(&ctl.kv_full, 0, p.status, abort);
+      if (ok && nq > 0) {
+        ok = mbar_wait(&ctl.stage_full[0], 0, p.status, abort);
+        if (ok) {
+          tc_fence_after();
+          issue_S_dP(0);
+          mma_commit(&ctl.s_full);
+        }
+      }
+      for (int it = 0; ok && it < nq; ++it) {
+        const int s = it % C::kStages;
+        const int b = it & 1;  // dS^T buffer
+        const uint32_t q = aStage + s * C::kStageBytes, o = q + C::kQBytes;
+        if (!(ok = mbar_wait(&ctl.sm_done, it & 1, p.status, abort))) break;
+        tc_fence_after();
+        // dV += P^T dO_i  (K = queries)
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k)
+          mma_ts(tmem + C::kColDV, tmem + C::kColP + k * 8, sdesc_sw128(o + k * 2048, C::kQBox, 1024), idKV,
+                 (it > 0 || k > 0) ? 1u : 0u);
+        if (it + 1 < nq) {
+          const int s2 = (it + 1) % C::kStages;
+          if (!(ok = mbar_wait(&ctl.stage_full[s2], ((it + 1) / C::kStages) & 1, p.status, abort))) break;
+          tc_fence_after();
+          issue_S_dP(s2);
+          mma_commit(&ctl.s_full);
+        }
+        // dK += dS^T Q_i  (A = dS^T, K-major over queries)
+        const uint32_t ds = aDs + b * C::kDsBytes;
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k)
+          mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (k / 4) * (BN * 128) + (k % 4) * 32, 16, 1024),
+                 sdesc_sw128(q + k * 2048, C::kQBox, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        // dQ partial for this query tile (K = keys)
+        if (it > 0 && !(ok = mbar_wait(&ctl.dq_empty, (it - 1) & 1, p.status, abort))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          if constexpr (C::kDqT)
+            mma_ss(tmem + C::kColDQ, sdesc_sw128(aK + k * 2048, BN * 128, 1024),
+                   sdesc_sw128(ds + k * 2048, BN * 128, 1024), idQ, k > 0);
+          else
+            mma_ss(tmem + C::kColDQ, sdesc_sw128(ds + k * 2048, BN * 128, 1024),
+                   sdesc_sw128(aK + k * 2048, BN * 128, 1024), idQ, k > 0);
+        }
+        mma_commit(&ctl.dq_full);
+        mma_commit(&ctl.stage_empty[s]);
+      }
+      mma_commit(&ctl.kv_done);
+      mma_commit(&ctl.drain);
+      mbar_wait(&ctl.drain, 0, p.status, nullptr);
+    }
+  } else if (warp < kDqWarp0) {
+    // ---------------- softmax-backward warpgroups ----------------
+    constexpr int kCols = BQ / 2;  // query columns per warpgroup
+    const int wg = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;         // key row in the tile = TMEM lane
+    const int key = kt * BN + r;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const float sl2 = p.sl2;
+    bool ok = true;
+    for (int it = 0; ok && it < nq; ++it) {
+      const int s = it % C::kStages;
+      const int b = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full, it & 1, p.status, abort));
+      if (!ok) break;
+      tc_fence_after();
+      const float* vec = reinterpret_cast<const float*>(smem + C::kVecOff + s * C::kVecBytes);
+      const int q0 = (q_first + it) * BQ;
+      uint8_t* dsrow = smem + C::kDsOff + b * C::kDsBytes + r * 128;
+#pragma unroll
+      for (int ch = 0; ch < kCols / 32; ++ch) {
+        const int c0 = wg * kCols + ch * 32;  // first query column of this chunk
+        float sv[32], dp[32];
+        tmem_ld32(tmem + lane_off + C::kColS + c0, sv);
+        tmem_ld32(tmem + lane_off + C::kColDP + c0, dp);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = c0 + 2 * u + e;
+            float pr = ex2(fmaf(sv[2 * u + e], sl2, -vec[c] * kLog2e));
+            if (p.causal && key > q0 + c) pr = 0.f;
+            pv[e] = pr;
+            dsv[e] = pr * (dp[2 * u + e] - vec[BQ + c]);
+          }
+          pk[u] = pack_bf16(pv[0], pv[1]);
+          dk[u] = pack_bf16(dsv[0], dsv[1]);
+        }
+        tmem_st16(tmem + lane_off + C::kColP + c0 / 2, pk);
+        // dS^T row r, columns c0..c0+31: four 16-byte chunks of a 128-byte swizzled row
+        // (atom column c0 / 64, chunk (c0 % 64) / 8 + u, XOR (r % 8)).
+        uint8_t* atom = dsrow + (c0 / 64) * (BN * 128);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = ((c0 % 64) / 8 + u) ^ (r & 7);
+          *reinterpret_cast<uint4*>(atom + chunk * 16) =
+              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&ctl.sm_done);
+    }
+  } else if (warp < kLoadWarp) {
+    // ---------------- dQ reduction, then the dK/dV epilogue ----------------
+    const int r = (warp & 3) * 32 + lane;  // TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int it = 0; ok && it < nq; ++it) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dq_full, it & 1, p.status, abort));
+      if (!ok) break;
+      tc_fence_after();
+      const int q0 = row_base + (q_first + it) * BQ;
+      if constexpr (C::kDqT) {
+        // lane = head-dim index r; columns = the BQ queries of the tile
+        float v[BQ];
+#pragma unroll
+        for (int c = 0; c < BQ; c += 32) tmem_ld32(tmem + lane_off + C::kColDQ + c, *reinterpret_cast<float(*)[32]>(&v[c]));
+        tc_fence_before();
+        mbar_arrive(&ctl.dq_empty);
+        float* dst = p.dQacc + (size_t)q0 * D + r;
+#pragma unroll 8
+        for (int c = 0; c < BQ; ++c) atomicAdd(dst + (size_t)c * D, v[c]);
+      } else {
+        // lane = query row r of the tile; columns = head dim
+        float v[D];
+#pragma unroll
+        for (int c = 0; c < D; c += 32) tmem_ld32(tmem + lane_off + C::kColDQ + c, *reinterpret_cast<float(*)[32]>(&v[c]));
+        tc_fence_before();
+        mbar_arrive(&ctl.dq_empty);
+        float4* dst = reinterpret_cast<float4*>(p.dQacc + (size_t)(q0 + r) * D);
+#pragma unroll
+        for (int c = 0; c < D / 4; ++c) atomicAdd(dst + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+      }
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.kv_done, 0, p.status, abort));
+    if (ok) {
+      tc_fence_after();
+      const size_t row = (size_t)row_base + kt * BN + r;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float v[32];
+        uint4 w[4];
+        uint32_t* wu = reinterpret_cast<uint32_t*>(w);
+        tmem_ld32(tmem + lane_off + C::kColDV + c0, v);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
+        uint4* dv = reinterpret_cast<uint4*>(p.dV + row * D + c0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dv[u] = w[u];
+        tmem_ld32(tmem + lane_off + C::kColDK + c0, v);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u] * p.scale, v[2 * u + 1] * p.scale);
+        uint4* dk = reinterpret_cast<uint4*>(p.dK + row * D + c0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dk[u] = w[u];
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// dQ = bf16(scale * dQacc), 8 elements per thread.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
+                                                        __nv_bfloat16* __restrict__ dq, int64_t n8,
+                                                        float scale) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+  const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+  uint4 w;
+  w.x = pack_bf16(a.x * scale, a.y * scale);
+  w.y = pack_bf16(a.z * scale, a.w * scale);
+  w.z = pack_bf16(b.x * scale, b.y * scale);
+  w.w = pack_bf16(b.z * scale, b.w * scale);
+  reinterpret_cast<uint4*>(dq)[i] = w;
+}
+
+template <int D>
+cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                   const float* Dv, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
+                   float scale, bool causal, int* status, cudaStream_t st) {
+  using C = BwdCfg<D>;
+  CUtensorMap mq, mk, mv, mdo;
+  const int64_t rows = s.rows();
+  if (!make_map_bf16_2d(&mq, Q, rows, D, C::BQ) || !make_map_bf16_2d(&mk, K, rows, D, BN) ||
+      !make_map_bf16_2d(&mv, V, rows, D, BN) || !make_map_bf16_2d(&mdo, dO, rows, D, C::BQ))
+    return cudaErrorInvalidValue;
+  static bool attr = [] {
+    return cudaFuncSetAttribute(fa_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmemBytes) == cudaSuccess;
+  }();
+  if (!attr) return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaMemsetAsync(dQacc, 0, (size_t)s.elems() * sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  BwdParams p;
+  p.LSE = LSE;
+  p.Dvec = Dv;
+  p.dQacc = dQacc;
+  p.dK = static_cast<__nv_bfloat16*>(dK);
+  p.dV = static_cast<__nv_bfloat16*>(dV);
+  p.status = status;
+  p.N = s.N;
+  p.heads = (int)s.heads();
+  p.kvtiles = s.N / BN;
+  p.qtiles = s.N / C::BQ;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.sl2 = scale * kLog2e;
+  const int64_t grid = (int64_t)p.kvtiles * p.heads;
+  fa_bwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t n8 = s.elems() / 8;
+  dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(dQacc, static_cast<__nv_bfloat16*>(dQ),
+                                                                  n8, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                   const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
+                   float scale, bool causal, int* status, cudaStream_t st) {
+  return s.d == 64 ? launch<64>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, status, st)
+                   : launch<128>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, status, st);
+}
+
+}  // namespace fa

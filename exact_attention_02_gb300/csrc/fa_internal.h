@@ -31,6 +31,10 @@ cudaError_t simt_bwd(const void* Q, const void* K, const void* V, const void* dO
 // ---- tcgen05 tensor-core path (bf16, d in {64, 128}, N % 128 == 0) ----
 cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st);
+// dQacc: fp32 [B*H*N, d] workspace; zeroed, accumulated and converted inside the call.
+cudaError_t tc_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                   const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
+                   float scale, bool causal, int* status, cudaStream_t st);
 
 // ---- memory-bound helpers (fa_simt.cu) ----
 cudaError_t preprocess_d(const void* O, const void* dO, float* D, const Shape& s, bool bf16,
