@@ -103,6 +103,31 @@ FA_API fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const voi
                    int B, int H, int N, int d, float scale, int causal, int dtype,
                    void* stream);
 
+/*
+ * fa_bwd_noalloc — fa_bwd for callers that must not allocate device memory.
+ * The pages have no counterpart: this is a packaging of fa_bwd, not a step of the method.
+ * Some callers cannot call cudaMalloc: code hosted by a framework that owns all device
+ * memory through a fixed, pre-planned pool (serving engines, plugin hosts) may not
+ * allocate outside it, and latency-critical paths cannot take the implicit device
+ * synchronisation cudaMalloc/cudaFree may bring. This entry point takes no workspace: its
+ * scratch (the fp32 dQ accumulator, and D when D is NULL) is a static device array inside
+ * the library, FA_NOALLOC_MAX_ELEMS floats plus FA_NOALLOC_MAX_ELEMS/64 floats (32.5 MiB),
+ * held by every GPU that loads the library until the process exits. It allocates nothing.
+ * Arguments and results are those of fa_bwd (without workspace / workspace_bytes).
+ * Limits: B*H*N*d <= FA_NOALLOC_MAX_ELEMS, else FA_ERR_WORKSPACE and nothing runs.
+ * First call on a device: looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current and caches it; make that first call before any stream capture.
+ * Sharing: all calls use the same array. Each call clears the accumulator before use, so
+ * leftovers of earlier calls do not leak into results, but calls that overlap on the GPU
+ * (concurrent streams or threads) race on the array and must be serialised by the caller.
+ */
+#define FA_NOALLOC_MAX_ELEMS (8u * 1024u * 1024u)
+FA_API fa_status_t fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                           const void* dO, const float* LSE, const float* D,
+                           void* dQ, void* dK, void* dV,
+                           int B, int H, int N, int d, float scale, int causal, int dtype,
+                           void* stream);
+
 /* Text for a status code (static storage; never NULL). */
 FA_API const char* fa_get_error_string(fa_status_t status);
 
