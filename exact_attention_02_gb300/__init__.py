@@ -23,6 +23,12 @@ FA_DTYPE_BF16, FA_DTYPE_FP32 = 0, 1
 # Which execution unit bounds each entry point's main kernel for bf16 inputs
 # ("tensor": tcgen05 MMAs, "alu": FFMA pipes, "hbm": memory bandwidth). fp32 is all FFMA.
 BF16_KERNEL_BOUND = {"fa_fwd": "tensor", "fa_bwd": "tensor", "fa_bwd_preprocess": "hbm"}
+# Kernels each entry point launches, in order (the dQ accumulator clear in fa_bwd is a
+# cudaMemsetAsync, not a library kernel).
+BF16_KERNELS = {"fa_fwd": ["fa_fwd_tc_kernel"], "fa_bwd_preprocess": ["preprocess_kernel"],
+                "fa_bwd": ["fa_bwd_tc_kernel", "dq_convert_kernel"]}
+FP32_KERNELS = {"fa_fwd": ["simt_fwd_kernel"], "fa_bwd_preprocess": ["preprocess_kernel"],
+                "fa_bwd": ["simt_bwd_dkdv_kernel", "simt_bwd_dq_kernel"]}
 
 _lib = None
 
