@@ -3,10 +3,10 @@
 //
 // Method ("flash-attention-backpropagation", 反向总览 / Softmax梯度 / QKV梯度): the
 // outer loop runs over key/value tiles (one 128-key tile per CTA), the inner loop over
-// query tiles; P is rebuilt from the forward's LSE, and one recompute of each (i, j)
-// tile yields dV, dK and dQ together (the single-recompute loop the Ascend page
-// "FlashAttention 反向传播" recommends over one pass per gradient). All accumulators
-// are fp32 and are rounded to bf16 once, on write-back.
+// 128-row query tiles; P is rebuilt from the forward's LSE, and one recompute of each
+// (i, j) tile yields dV, dK and dQ together (the single-recompute loop the Ascend page
+// "FlashAttention 反向传播" recommends over one pass per gradient). All accumulators are
+// fp32 and are rounded to bf16 once, on write-back.
 //
 // Working in the transposed frame puts the 128 keys of the CTA on the 128 TMEM lanes:
 //   S^T  = K_j Q_i^T          [keys x queries]   tcgen05, A,B = smem (K-major)
@@ -14,18 +14,23 @@
 //   P^T  = exp2(S^T * scale*log2e - LSE_i*log2e), masked (causal: key > query)
 //   dS^T = P^T * (dP^T - D_i)                     softmax warps, one thread per key
 //   dV_j += P^T dO_i          TMEM accumulator    A = P^T from TMEM
-//   dK_j += dS^T Q_i          TMEM accumulator    A = dS^T from smem (K-major)
-//   d = 128: dQ_i^T = K_j^T dS^T   (lanes = head dim)   A = K_j (MN-major), B = dS^T (MN-major)
-//   d =  64: dQ_i   = dS K_j       (lanes = queries)    A = dS^T (MN-major), B = K_j (MN-major)
-// and dQ partials are added into an fp32 accumulator in global memory (one red.add per
-// element); a last pass scales it by `scale` and rounds to bf16.
+//   dK_j += dS^T Q_i          TMEM accumulator    A = dS^T from TMEM
+//   d = 128: dQ_i^T = K_j^T dS^T   (lanes = head dim)   A = K_j (MN-major), B = dS^T (smem, MN-major)
+//   d =  64: dQ_i   = dS K_j       (lanes = queries)    A = dS^T (smem, MN-major), B = K_j (MN-major)
+// and the dQ partials are added into an fp32 accumulator in global memory (red.add); a
+// last pass scales it by `scale` and rounds to bf16.
 //
-// CTA = 14 warps: 0-7 softmax (two warpgroups split the query columns), 8-11 dQ
-// reduction + dK/dV epilogue, 12 TMA producer, 13 MMA issuer. Query tiles are BQ = 64
-// rows for d = 128 and 128 rows for d = 64, so TMEM holds dV, dK, S^T, dP^T, dQ and P^T
-// at once (448 / 512 columns).
-// Pipelining: S/dP of tile i+1 are issued right after dV(i) and before dK(i)/dQ(i), so
-// the softmax warps work on tile i+1 while the tensor core finishes tile i.
+// TMEM (512 columns): dV | dK | NB buffers of (S^T | dP^T). Each softmax warpgroup
+// writes its bf16 P^T over the S^T columns it has just read and its bf16 dS^T over the
+// dP^T columns it has just read; the dQ partial of a tile then reuses its S^T columns
+// once dV has consumed P^T. Query tiles are BQ = 64 rows for d = 128, which leaves room
+// for NB = 2 buffers, so the softmax of tile i+1 overlaps the MMAs of tile i; for d = 64
+// they are BQ = 128 rows with one buffer (wider MMAs, fewer operand bytes per FLOP).
+// Per tile the tensor core runs dV, dK, dQ of tile i, then dP of tile i+NB while the dQ
+// warpgroup drains the partial, then S of tile i+NB.
+//
+// CTA = 14 warps: 0-7 softmax (two warpgroups splitting the query columns), 8-11 dQ
+// reduction + dK/dV epilogue, 12 TMA producer, 13 MMA issuer.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -44,34 +49,43 @@ constexpr int kLoadWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr float kLog2e = 1.4426950408889634f;
 
+struct BwdCtl {
+  uint64_t kv_full, stage_full[3], stage_empty[3];
+  uint64_t s_full[2], sm_done[2], dq_full, dq_empty, kv_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
 template <int D>
 struct BwdCfg {
   static constexpr int BQ = D == 128 ? 64 : 128;     // queries per tile
+  static constexpr int NB = D == 128 ? 2 : 1;        // S^T/dP^T buffers in TMEM
+  static constexpr int kCols = BQ / 2;               // query columns per softmax warpgroup
   static constexpr bool kDqT = D == 128;             // dQ^T (lanes = head dim) or dQ (lanes = queries)
   static constexpr int kBoxes = D / 64;              // 64-column boxes per row
   static constexpr int kKVBytes = BN * D * 2;        // K_j or V_j
   static constexpr int kQBox = BQ * 128;             // one [BQ x 64] box of Q_i / dO_i
   static constexpr int kQBytes = BQ * D * 2;
   static constexpr int kStages = 3;
-  static constexpr int kDsBytes = BN * BQ * 2;       // dS^T [keys x queries] bf16
-  // shared-memory layout
+  static constexpr int kDsBytes = BN * BQ * 2;       // dS^T [keys x queries] bf16, two buffers
+  // shared-memory layout (1024-byte aligned base; control block last)
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kKVBytes;
   static constexpr int kStageOff = kVOff + kKVBytes;
   static constexpr int kStageBytes = 2 * kQBytes;    // Q_i then dO_i
   static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kVecOff = kDsOff + 2 * kDsBytes;        // LSE_i, D_i per stage
+  static constexpr int kVecOff = kDsOff + 2 * kDsBytes;  // LSE_i, D_i per stage
   static constexpr int kVecBytes = 2 * BQ * 4;
-  static constexpr int kSmemBytes = kVecOff + kStages * kVecBytes + 1024;
+  static constexpr int kCtlOff = kVecOff + kStages * kVecBytes;
+  static constexpr int kSmemBytes = kCtlOff + (int)sizeof(BwdCtl);
   // TMEM columns
   static constexpr uint32_t kColDV = 0;
   static constexpr uint32_t kColDK = D;
-  static constexpr uint32_t kColS = 2 * D;
-  static constexpr uint32_t kColDP = 2 * D + BQ;
-  static constexpr uint32_t kColDQ = 2 * D + 2 * BQ;
-  static constexpr uint32_t kColP = kColDQ + (kDqT ? BQ : D);
+  __device__ static constexpr uint32_t colS(int b) { return 2 * D + b * 2 * BQ; }
+  __device__ static constexpr uint32_t colDP(int b) { return 2 * D + b * 2 * BQ + BQ; }
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kColP + BQ / 2 <= 512, "TMEM budget");
+  static_assert(2 * D + NB * 2 * BQ <= 512, "TMEM budget");
+  static_assert((kDqT ? BQ : D) <= BQ, "dQ partial must fit in the S^T columns");
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
 };
 
@@ -91,19 +105,20 @@ struct BwdParams {
   float sl2;  // scale * log2(e)
 };
 
-struct BwdCtl {
-  uint64_t kv_full, stage_full[3], stage_empty[3];
-  uint64_t s_full, sm_done, dq_full, dq_empty, kv_done, drain;
-  uint32_t tmem_base;
-  int abort;
-};
-
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// TMEM column of the packed bf16 operand for query block k (16 queries) when each of the
+// two softmax warpgroups packs its kCols queries into the first kCols/2 columns of its
+// half of the buffer.
+template <int kCols>
+__device__ __forceinline__ uint32_t packed_col(uint32_t base, int k) {
+  return base + (k / (kCols / 16)) * kCols + (k % (kCols / 16)) * 8;
 }
 
 template <int D>
@@ -113,10 +128,15 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                  const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ BwdCtl ctl;
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The swizzled operand layout needs a 1024-byte aligned base; the runtime provides it
+  // for this declaration, and the kernel refuses to run (status word) if it did not.
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0 && p.status) atomicExch(p.status, 3 /* FA_ERR_CUDA */);
+    return;
+  }
+  BwdCtl& ctl = *reinterpret_cast<BwdCtl*>(smem + C::kCtlOff);
 
   int kt, head;
   if (p.causal) {  // key tiles near the start see the most queries: launch them first
@@ -136,8 +156,10 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_init(&ctl.stage_full[s], 1);
       mbar_init(&ctl.stage_empty[s], 1);
     }
-    mbar_init(&ctl.s_full, 1);
-    mbar_init(&ctl.sm_done, 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl.s_full[b], 1);
+      mbar_init(&ctl.sm_done[b], 256);
+    }
     mbar_init(&ctl.dq_full, 1);
     mbar_init(&ctl.dq_empty, 128);
     mbar_init(&ctl.kv_done, 1);
@@ -194,68 +216,76 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
       const uint32_t aStage = smem_u32(smem + C::kStageOff);
       const uint32_t aDs = smem_u32(smem + C::kDsOff);
-      auto issue_S_dP = [&](int s) {
-        const uint32_t q = aStage + s * C::kStageBytes, o = q + C::kQBytes;
+      auto issue_S = [&](int s, int b) {
+        const uint32_t q = aStage + s * C::kStageBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t offKV = (k / 4) * (BN * 128) + (k % 4) * 32;
           const uint32_t offQ = (k / 4) * C::kQBox + (k % 4) * 32;
-          mma_ss(tmem + C::kColS, sdesc_sw128(aK + offKV, 16, 1024), sdesc_sw128(q + offQ, 16, 1024), idSP, k > 0);
+          mma_ss(tmem + C::colS(b), sdesc_sw128(aK + offKV, 16, 1024), sdesc_sw128(q + offQ, 16, 1024), idSP,
+                 k > 0);
         }
+      };
+      auto issue_dP = [&](int s, int b) {
+        const uint32_t o = aStage + s * C::kStageBytes + C::kQBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t offKV = (k / 4) * (BN * 128) + (k % 4) * 32;
           const uint32_t offQ = (k / 4) * C::kQBox + (k % 4) * 32;
-          mma_ss(tmem + C::kColDP, sdesc_sw128(aV + offKV, 16, 1024), sdesc_sw128(o + offQ, 16, 1024), idSP, k > 0);
+          mma_ss(tmem + C::colDP(b), sdesc_sw128(aV + offKV, 16, 1024), sdesc_sw128(o + offQ, 16, 1024), idSP,
+                 k > 0);
         }
       };
       bool ok = mbar_wait(&ctl.kv_full, 0, p.status, abort);
-      if (ok && nq > 0) {
-        ok = mbar_wait(&ctl.stage_full[0], 0, p.status, abort);
-        if (ok) {
-          tc_fence_after();
-          issue_S_dP(0);
-          mma_commit(&ctl.s_full);
-        }
+      for (int t = 0; ok && t < C::NB && t < nq; ++t) {
+        if (!(ok = mbar_wait(&ctl.stage_full[t], 0, p.status, abort))) break;
+        tc_fence_after();
+        issue_S(t, t);
+        issue_dP(t, t);
+        mma_commit(&ctl.s_full[t]);
       }
       for (int it = 0; ok && it < nq; ++it) {
         const int s = it % C::kStages;
-        const int b = it & 1;  // dS^T buffer
+        const int b = it % C::NB;
         const uint32_t q = aStage + s * C::kStageBytes, o = q + C::kQBytes;
-        if (!(ok = mbar_wait(&ctl.sm_done, it & 1, p.status, abort))) break;
+        const uint32_t ds = aDs + (it & 1) * C::kDsBytes;
+        if (!(ok = mbar_wait(&ctl.sm_done[b], (it / C::NB) & 1, p.status, abort))) break;
         tc_fence_after();
-        // dV += P^T dO_i  (K = queries)
+        // dV += P^T dO_i and dK += dS^T Q_i (K = queries; A = packed bf16 in TMEM)
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-          mma_ts(tmem + C::kColDV, tmem + C::kColP + k * 8, sdesc_sw128(o + k * 2048, C::kQBox, 1024), idKV,
-                 (it > 0 || k > 0) ? 1u : 0u);
-        if (it + 1 < nq) {
-          const int s2 = (it + 1) % C::kStages;
-          if (!(ok = mbar_wait(&ctl.stage_full[s2], ((it + 1) / C::kStages) & 1, p.status, abort))) break;
-          tc_fence_after();
-          issue_S_dP(s2);
-          mma_commit(&ctl.s_full);
-        }
-        // dK += dS^T Q_i  (A = dS^T, K-major over queries)
-        const uint32_t ds = aDs + b * C::kDsBytes;
+          mma_ts(tmem + C::kColDV, packed_col<C::kCols>(tmem + C::colS(b), k),
+                 sdesc_sw128(o + k * 2048, C::kQBox, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-          mma_ss(tmem + C::kColDK, sdesc_sw128(ds + (k / 4) * (BN * 128) + (k % 4) * 32, 16, 1024),
+          mma_ts(tmem + C::kColDK, packed_col<C::kCols>(tmem + C::colDP(b), k),
                  sdesc_sw128(q + k * 2048, C::kQBox, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
-        // dQ partial for this query tile (K = keys)
+        // dQ partial (K = keys) over this buffer's S^T columns (P^T was read by dV, in
+        // issue order). The previous partial must have been picked up first so the two
+        // barriers of the hand-off stay one phase apart.
         if (it > 0 && !(ok = mbar_wait(&ctl.dq_empty, (it - 1) & 1, p.status, abort))) break;
-        tc_fence_after();
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           if constexpr (C::kDqT)
-            mma_ss(tmem + C::kColDQ, sdesc_sw128(aK + k * 2048, BN * 128, 1024),
+            mma_ss(tmem + C::colS(b), sdesc_sw128(aK + k * 2048, BN * 128, 1024),
                    sdesc_sw128(ds + k * 2048, BN * 128, 1024), idQ, k > 0);
           else
-            mma_ss(tmem + C::kColDQ, sdesc_sw128(ds + k * 2048, BN * 128, 1024),
+            mma_ss(tmem + C::colS(b), sdesc_sw128(ds + k * 2048, BN * 128, 1024),
                    sdesc_sw128(aK + k * 2048, BN * 128, 1024), idQ, k > 0);
         }
         mma_commit(&ctl.dq_full);
         mma_commit(&ctl.stage_empty[s]);
+        const int nxt = it + C::NB;
+        if (nxt < nq) {
+          const int s2 = nxt % C::kStages;
+          if (!(ok = mbar_wait(&ctl.stage_full[s2], (nxt / C::kStages) & 1, p.status, abort))) break;
+          tc_fence_after();
+          issue_dP(s2, b);  // dP^T columns: dS^T was read by dK above (issue order)
+          if (!(ok = mbar_wait(&ctl.dq_empty, it & 1, p.status, abort))) break;
+          tc_fence_after();
+          issue_S(s2, b);   // S^T columns: the dQ partial has been read out
+          mma_commit(&ctl.s_full[b]);
+        }
       }
       mma_commit(&ctl.kv_done);
       mma_commit(&ctl.drain);
@@ -263,44 +293,59 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
   } else if (warp < kDqWarp0) {
     // ---------------- softmax-backward warpgroups ----------------
-    constexpr int kCols = BQ / 2;  // query columns per warpgroup
+    constexpr int kCols = C::kCols;
     const int wg = warp >> 2;
     const int r = (warp & 3) * 32 + lane;         // key row in the tile = TMEM lane
     const int key = kt * BN + r;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const float sl2 = p.sl2;
+    const float2 sl2 = make_float2(p.sl2, p.sl2);
+    const float2 neg_log2e = make_float2(-kLog2e, -kLog2e);
+    const float2 minus1 = make_float2(-1.f, -1.f);
     bool ok = true;
     for (int it = 0; ok && it < nq; ++it) {
       const int s = it % C::kStages;
-      const int b = it & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full, it & 1, p.status, abort));
+      const int b = it % C::NB;
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full[b], (it / C::NB) & 1, p.status, abort));
       if (!ok) break;
       tc_fence_after();
       const float* vec = reinterpret_cast<const float*>(smem + C::kVecOff + s * C::kVecBytes);
       const int q0 = (q_first + it) * BQ;
-      uint8_t* dsrow = smem + C::kDsOff + b * C::kDsBytes + r * 128;
+      const bool diag = p.causal && q0 < kt * BN + BN;  // some key of the tile exceeds some query
+      uint8_t* dsrow = smem + C::kDsOff + (it & 1) * C::kDsBytes + r * 128;
 #pragma unroll
       for (int ch = 0; ch < kCols / 32; ++ch) {
         const int c0 = wg * kCols + ch * 32;  // first query column of this chunk
         float sv[32], dp[32];
-        tmem_ld32(tmem + lane_off + C::kColS + c0, sv);
-        tmem_ld32(tmem + lane_off + C::kColDP + c0, dp);
+        tmem_ld32x2(tmem + lane_off + C::colS(b) + c0, tmem + lane_off + C::colDP(b) + c0, sv, dp);
+        // -LSE*log2(e) and D for the 32 columns, loaded as 16-byte vectors up front
+        float2 nl[16], dv[16];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 a = *reinterpret_cast<const float4*>(vec + c0 + 4 * u);
+          const float4 b = *reinterpret_cast<const float4*>(vec + BQ + c0 + 4 * u);
+          nl[2 * u] = fmul2(make_float2(a.x, a.y), neg_log2e);
+          nl[2 * u + 1] = fmul2(make_float2(a.z, a.w), neg_log2e);
+          dv[2 * u] = make_float2(b.x, b.y);
+          dv[2 * u + 1] = make_float2(b.z, b.w);
+        }
         uint32_t pk[16], dk[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = c0 + 2 * u + e;
-            float pr = ex2(fmaf(sv[2 * u + e], sl2, -vec[c] * kLog2e));
-            if (p.causal && key > q0 + c) pr = 0.f;
-            pv[e] = pr;
-            dsv[e] = pr * (dp[2 * u + e] - vec[BQ + c]);
+          const int c = c0 + 2 * u;
+          const float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, nl[u]);
+          float2 pr = make_float2(ex2(x.x), ex2(x.y));
+          if (diag) {
+            if (key > q0 + c) pr.x = 0.f;
+            if (key > q0 + c + 1) pr.y = 0.f;
           }
-          pk[u] = pack_bf16(pv[0], pv[1]);
-          dk[u] = pack_bf16(dsv[0], dsv[1]);
+          const float2 dd = ffma2(dv[u], minus1, make_float2(dp[2 * u], dp[2 * u + 1]));
+          const float2 dsv = fmul2(pr, dd);
+          pk[u] = pack_bf16(pr.x, pr.y);
+          dk[u] = pack_bf16(dsv.x, dsv.y);
         }
-        tmem_st16(tmem + lane_off + C::kColP + c0 / 2, pk);
+        // bf16 P^T over S^T and dS^T over dP^T, in columns this warpgroup has already read
+        tmem_st16(tmem + lane_off + C::colS(b) + wg * kCols + ch * 16, pk);
+        tmem_st16(tmem + lane_off + C::colDP(b) + wg * kCols + ch * 16, dk);
         // dS^T row r, columns c0..c0+31: four 16-byte chunks of a 128-byte swizzled row
         // (atom column c0 / 64, chunk (c0 % 64) / 8 + u, XOR (r % 8)).
         uint8_t* atom = dsrow + (c0 / 64) * (BN * 128);
@@ -314,7 +359,7 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&ctl.sm_done);
+      mbar_arrive(&ctl.sm_done[b]);
     }
   } else if (warp < kLoadWarp) {
     // ---------------- dQ reduction, then the dK/dV epilogue ----------------
@@ -326,21 +371,30 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       const int q0 = row_base + (q_first + it) * BQ;
+      const uint32_t colQ = C::colS(it % C::NB);
       if constexpr (C::kDqT) {
-        // lane = head-dim index r; columns = the BQ queries of the tile
-        float v[BQ];
-#pragma unroll
-        for (int c = 0; c < BQ; c += 32) tmem_ld32(tmem + lane_off + C::kColDQ + c, *reinterpret_cast<float(*)[32]>(&v[c]));
-        tc_fence_before();
-        mbar_arrive(&ctl.dq_empty);
+        // lane = head-dim index r; columns = the BQ queries of the tile, drained in two
+        // halves of 64 (the columns are released after the second load)
         float* dst = p.dQacc + (size_t)q0 * D + r;
-#pragma unroll 8
-        for (int c = 0; c < BQ; ++c) atomicAdd(dst + (size_t)c * D, v[c]);
+#pragma unroll 1
+        for (int h = 0; h < BQ; h += 64) {
+          float v[64];
+          tmem_ld32x2(tmem + lane_off + colQ + h, tmem + lane_off + colQ + h + 32,
+                      *reinterpret_cast<float(*)[32]>(&v[0]), *reinterpret_cast<float(*)[32]>(&v[32]));
+          if (h + 64 == BQ) {
+            tc_fence_before();
+            mbar_arrive(&ctl.dq_empty);
+          }
+#pragma unroll 16
+          for (int c = 0; c < 64; ++c) atomicAdd(dst + (size_t)(h + c) * D, v[c]);
+        }
       } else {
         // lane = query row r of the tile; columns = head dim
         float v[D];
 #pragma unroll
-        for (int c = 0; c < D; c += 32) tmem_ld32(tmem + lane_off + C::kColDQ + c, *reinterpret_cast<float(*)[32]>(&v[c]));
+        for (int c = 0; c < D; c += 64)
+          tmem_ld32x2(tmem + lane_off + colQ + c, tmem + lane_off + colQ + c + 32,
+                      *reinterpret_cast<float(*)[32]>(&v[c]), *reinterpret_cast<float(*)[32]>(&v[c + 32]));
         tc_fence_before();
         mbar_arrive(&ctl.dq_empty);
         float4* dst = reinterpret_cast<float4*>(p.dQacc + (size_t)(q0 + r) * D);

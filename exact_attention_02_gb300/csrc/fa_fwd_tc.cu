@@ -241,16 +241,24 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       float sv[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<float(*)[32]>(&sv[32 * c]));
+      tmem_ld32x2(tS, tS + 32, *reinterpret_cast<float(*)[32]>(&sv[0]), *reinterpret_cast<float(*)[32]>(&sv[32]));
+      tmem_ld32x2(tS + 64, tS + 96, *reinterpret_cast<float(*)[32]>(&sv[64]),
+                  *reinterpret_cast<float(*)[32]>(&sv[96]));
       if (p.causal && j == qt0 + t) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
           if (c > r) sv[c] = -INFINITY;
       }
-      float mx = sv[0];
+      // row max: four independent chains of 3-input max
+      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, sv[c]);
+      for (int c = 4; c < BN; c += 8) {
+        mx0 = fmax3(mx0, sv[c], sv[c + 1]);
+        mx1 = fmax3(mx1, sv[c + 2], sv[c + 3]);
+        mx2 = fmax3(mx2, sv[c + 4], sv[c + 5]);
+        mx3 = fmax3(mx3, sv[c + 6], sv[c + 7]);
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       const float m_new = fmaxf(m, mx * sl2);
       const bool grow = m_new > m + kRescaleThreshold;
       if (__any_sync(0xffffffffu, grow)) {
@@ -273,22 +281,25 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
         if (grow) m = m_new;
       }
-      const float neg_m = -m;
-      float rs0 = 0.f, rs1 = 0.f;
+      const float2 sl2v = make_float2(sl2, sl2);
+      const float2 neg_m = make_float2(-m, -m);
+      float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < BN / 32; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const float p0 = ex2(fmaf(sv[32 * q + 2 * u], sl2, neg_m));
-          const float p1 = ex2(fmaf(sv[32 * q + 2 * u + 1], sl2, neg_m));
-          rs0 += p0;
-          rs1 += p1;
-          pk[u] = pack_bf16(p0, p1);
+          const float2 x = ffma2(make_float2(sv[32 * q + 2 * u], sv[32 * q + 2 * u + 1]), sl2v, neg_m);
+          const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+          if (u & 1)
+            rs1 = fadd2(rs1, pr);
+          else
+            rs0 = fadd2(rs0, pr);
+          pk[u] = pack_bf16(pr.x, pr.y);
         }
         tmem_st16(tS + 16 * q, pk);
       }
-      l += rs0 + rs1;
+      l += (rs0.x + rs0.y) + (rs1.x + rs1.y);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&ctl.p_full[t]);

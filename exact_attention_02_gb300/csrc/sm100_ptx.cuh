@@ -71,12 +71,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // kWaitLimitNs, or at once when *abort is set by another role of the CTA; on giving up
 // it records FA_ERR_DEVICE_TIMEOUT in *status, sets *abort and returns false. A null
 // `abort` means: ignore other roles and wait (still bounded), as the drain paths need.
+// The poll itself is a tight try_wait loop; the (slow) global timer and the abort flag
+// are consulted once every 256 polls so that a completed phase is noticed promptly.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (abort && *abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       if (status) atomicExch(status, kErrTimeout);
@@ -218,6 +222,54 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, float (&v)[32]) {
         "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(ta)
       : "memory");
+}
+
+// Two 32-column loads (any columns of this thread's lane) completed by one wait, so the
+// second load's latency overlaps the first's.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta0, uint32_t ta1, float (&a)[32], float (&b)[32]) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(a);
+  uint32_t* q = reinterpret_cast<uint32_t*>(b);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31]),
+        "=r"(q[0]),"=r"(q[1]),"=r"(q[2]),"=r"(q[3]),"=r"(q[4]),"=r"(q[5]),"=r"(q[6]),"=r"(q[7]),"=r"(q[8]),"=r"(q[9]),"=r"(q[10]),"=r"(q[11]),"=r"(q[12]),"=r"(q[13]),"=r"(q[14]),"=r"(q[15]),"=r"(q[16]),"=r"(q[17]),"=r"(q[18]),"=r"(q[19]),"=r"(q[20]),"=r"(q[21]),"=r"(q[22]),"=r"(q[23]),"=r"(q[24]),"=r"(q[25]),"=r"(q[26]),"=r"(q[27]),"=r"(q[28]),"=r"(q[29]),"=r"(q[30]),"=r"(q[31])
+      : "r"(ta0), "r"(ta1)
+      : "memory");
+}
+
+// Packed fp32 pairs (sm_100+): one instruction operates on both halves of a float2.
+__device__ __forceinline__ uint64_t f2_bits(float2 v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float2 bits_f2(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+// max of three (sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // 16 consecutive 32-bit columns of this thread's lane.
