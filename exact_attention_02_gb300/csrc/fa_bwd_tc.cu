@@ -236,34 +236,21 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                  k > 0);
         }
       };
-      bool ok = mbar_wait(&ctl.kv_full, 0, p.status, abort);
-      for (int t = 0; ok && t < C::NB && t < nq; ++t) {
-        if (!(ok = mbar_wait(&ctl.stage_full[t], 0, p.status, abort))) break;
-        tc_fence_after();
-        issue_S(t, t);
-        issue_dP(t, t);
-        mma_commit(&ctl.s_full[t]);
-      }
-      for (int it = 0; ok && it < nq; ++it) {
-        const int s = it % C::kStages;
-        const int b = it % C::NB;
-        const uint32_t q = aStage + s * C::kStageBytes, o = q + C::kQBytes;
-        const uint32_t ds = aDs + (it & 1) * C::kDsBytes;
-        if (!(ok = mbar_wait(&ctl.sm_done[b], (it / C::NB) & 1, p.status, abort))) break;
-        tc_fence_after();
-        // dV += P^T dO_i and dK += dS^T Q_i (K = queries; A = packed bf16 in TMEM)
+      auto issue_dV_dK = [&](int it, int b, uint32_t q, uint32_t o, bool which_dk) {
+        // dV += P^T dO_i or dK += dS^T Q_i (K = queries; A = packed bf16 in TMEM)
 #pragma unroll
-        for (int k = 0; k < BQ / 16; ++k)
-          mma_ts(tmem + C::kColDV, packed_col<C::kCols>(tmem + C::colS(b), k),
-                 sdesc_sw128(o + k * 2048, C::kQBox, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < BQ / 16; ++k)
-          mma_ts(tmem + C::kColDK, packed_col<C::kCols>(tmem + C::colDP(b), k),
-                 sdesc_sw128(q + k * 2048, C::kQBox, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < BQ / 16; ++k) {
+          if (!which_dk)
+            mma_ts(tmem + C::kColDV, packed_col<C::kCols>(tmem + C::colS(b), k),
+                   sdesc_sw128(o + k * 2048, C::kQBox, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
+          else
+            mma_ts(tmem + C::kColDK, packed_col<C::kCols>(tmem + C::colDP(b), k),
+                   sdesc_sw128(q + k * 2048, C::kQBox, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
+        }
+      };
+      auto issue_dQ = [&](int b, uint32_t ds) {
         // dQ partial (K = keys) over this buffer's S^T columns (P^T was read by dV, in
-        // issue order). The previous partial must have been picked up first so the two
-        // barriers of the hand-off stay one phase apart.
-        if (it > 0 && !(ok = mbar_wait(&ctl.dq_empty, (it - 1) & 1, p.status, abort))) break;
+        // issue order).
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           if constexpr (C::kDqT)
@@ -273,18 +260,83 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             mma_ss(tmem + C::colS(b), sdesc_sw128(ds + k * 2048, BN * 128, 1024),
                    sdesc_sw128(aK + k * 2048, BN * 128, 1024), idQ, k > 0);
         }
-        mma_commit(&ctl.dq_full);
-        mma_commit(&ctl.stage_empty[s]);
-        const int nxt = it + C::NB;
-        if (nxt < nq) {
-          const int s2 = nxt % C::kStages;
-          if (!(ok = mbar_wait(&ctl.stage_full[s2], (nxt / C::kStages) & 1, p.status, abort))) break;
+      };
+      bool ok = mbar_wait(&ctl.kv_full, 0, p.status, abort);
+      if constexpr (C::NB == 2) {
+        // Issue order per tile i (buffer b = i % 2):
+        //   dV(i), S(i+1), dK(i), dQ(i), dP(i+2)
+        // S(i+1) lands in the columns that held the partial dQ(i-1); placing dP(i+1) and
+        // dV(i) ahead of it gives the dQ warpgroup time to read that partial out, and the
+        // softmax of tile i+1 runs while dK(i), dQ(i) and dP(i+2) execute.
+        if (ok && nq > 0 && (ok = mbar_wait(&ctl.stage_full[0], 0, p.status, abort))) {
           tc_fence_after();
-          issue_dP(s2, b);  // dP^T columns: dS^T was read by dK above (issue order)
-          if (!(ok = mbar_wait(&ctl.dq_empty, it & 1, p.status, abort))) break;
+          issue_S(0, 0);
+          issue_dP(0, 0);
+          mma_commit(&ctl.s_full[0]);
+        }
+        if (ok && nq > 1 && (ok = mbar_wait(&ctl.stage_full[1], 0, p.status, abort))) {
           tc_fence_after();
-          issue_S(s2, b);   // S^T columns: the dQ partial has been read out
-          mma_commit(&ctl.s_full[b]);
+          issue_dP(1, 1);
+        }
+        for (int it = 0; ok && it < nq; ++it) {
+          const int s = it % C::kStages;
+          const int b = it & 1;
+          const uint32_t q = aStage + s * C::kStageBytes, o = q + C::kQBytes;
+          const uint32_t ds = aDs + (it & 1) * C::kDsBytes;
+          if (!(ok = mbar_wait(&ctl.sm_done[b], (it / 2) & 1, p.status, abort))) break;
+          tc_fence_after();
+          issue_dV_dK(it, b, q, o, false);
+          // The previous partial dQ(i-1) sits in buffer b^1's S^T columns; it must have been
+          // read out before S(i+1) overwrites them (and before dQ(i) is handed off, so the
+          // two hand-off barriers stay one phase apart).
+          if (it > 0 && !(ok = mbar_wait(&ctl.dq_empty, (it - 1) & 1, p.status, abort))) break;
+          tc_fence_after();
+          if (it + 1 < nq) {
+            issue_S((it + 1) % C::kStages, b ^ 1);  // stage it+1 was waited for with dP(i+1)
+            mma_commit(&ctl.s_full[b ^ 1]);
+          }
+          issue_dV_dK(it, b, q, o, true);
+          issue_dQ(b, ds);
+          mma_commit(&ctl.dq_full);
+          mma_commit(&ctl.stage_empty[s]);
+          if (it + 2 < nq) {
+            const int s2 = (it + 2) % C::kStages;
+            if (!(ok = mbar_wait(&ctl.stage_full[s2], ((it + 2) / C::kStages) & 1, p.status, abort))) break;
+            tc_fence_after();
+            issue_dP(s2, b);  // dP^T columns of buffer b: dS^T was read by dK above (issue order)
+          }
+        }
+      } else {
+        // One buffer: dV(i), dK(i), dQ(i) into the S^T columns, then dP(i+1), then S(i+1)
+        // once the partial has been read out.
+        if (ok && nq > 0 && (ok = mbar_wait(&ctl.stage_full[0], 0, p.status, abort))) {
+          tc_fence_after();
+          issue_S(0, 0);
+          issue_dP(0, 0);
+          mma_commit(&ctl.s_full[0]);
+        }
+        for (int it = 0; ok && it < nq; ++it) {
+          const int s = it % C::kStages;
+          const uint32_t q = aStage + s * C::kStageBytes, o = q + C::kQBytes;
+          const uint32_t ds = aDs + (it & 1) * C::kDsBytes;
+          if (!(ok = mbar_wait(&ctl.sm_done[0], it & 1, p.status, abort))) break;
+          tc_fence_after();
+          issue_dV_dK(it, 0, q, o, false);
+          issue_dV_dK(it, 0, q, o, true);
+          if (it > 0 && !(ok = mbar_wait(&ctl.dq_empty, (it - 1) & 1, p.status, abort))) break;
+          issue_dQ(0, ds);
+          mma_commit(&ctl.dq_full);
+          mma_commit(&ctl.stage_empty[s]);
+          if (it + 1 < nq) {
+            const int s2 = (it + 1) % C::kStages;
+            if (!(ok = mbar_wait(&ctl.stage_full[s2], ((it + 1) / C::kStages) & 1, p.status, abort))) break;
+            tc_fence_after();
+            issue_dP(s2, 0);  // dP^T columns: dS^T was read by dK above (issue order)
+            if (!(ok = mbar_wait(&ctl.dq_empty, it & 1, p.status, abort))) break;
+            tc_fence_after();
+            issue_S(s2, 0);   // S^T columns: the dQ partial has been read out
+            mma_commit(&ctl.s_full[0]);
+          }
         }
       }
       mma_commit(&ctl.kv_done);
