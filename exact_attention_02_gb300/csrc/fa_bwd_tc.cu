@@ -216,49 +216,48 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
       const uint32_t aStage = smem_u32(smem + C::kStageOff);
       const uint32_t aDs = smem_u32(smem + C::kDsOff);
+      // Base descriptors; each MMA below only advances the start address.
+      const uint64_t dK_k = sdesc_sw128(aK, 16, 1024);            // K_j, K-major (rows = keys)
+      const uint64_t dK_mn = sdesc_sw128(aK, BN * 128, 1024);     // K_j read as K_j^T / MN-major
+      const uint64_t dV_k = sdesc_sw128(aV, 16, 1024);
+      auto stage_desc = [&](int s, bool dO, bool mn) {
+        const uint32_t a = aStage + s * C::kStageBytes + (dO ? C::kQBytes : 0);
+        return mn ? sdesc_sw128(a, C::kQBox, 1024) : sdesc_sw128(a, 16, 1024);
+      };
       auto issue_S = [&](int s, int b) {
-        const uint32_t q = aStage + s * C::kStageBytes;
+        const uint64_t qd = stage_desc(s, false, false);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t offKV = (k / 4) * (BN * 128) + (k % 4) * 32;
-          const uint32_t offQ = (k / 4) * C::kQBox + (k % 4) * 32;
-          mma_ss(tmem + C::colS(b), sdesc_sw128(aK + offKV, 16, 1024), sdesc_sw128(q + offQ, 16, 1024), idSP,
-                 k > 0);
-        }
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tmem + C::colS(b), sdesc_add(dK_k, (k / 4) * (BN * 128) + (k % 4) * 32),
+                 sdesc_add(qd, (k / 4) * C::kQBox + (k % 4) * 32), idSP, k > 0);
       };
       auto issue_dP = [&](int s, int b) {
-        const uint32_t o = aStage + s * C::kStageBytes + C::kQBytes;
+        const uint64_t od = stage_desc(s, true, false);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t offKV = (k / 4) * (BN * 128) + (k % 4) * 32;
-          const uint32_t offQ = (k / 4) * C::kQBox + (k % 4) * 32;
-          mma_ss(tmem + C::colDP(b), sdesc_sw128(aV + offKV, 16, 1024), sdesc_sw128(o + offQ, 16, 1024), idSP,
-                 k > 0);
-        }
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tmem + C::colDP(b), sdesc_add(dV_k, (k / 4) * (BN * 128) + (k % 4) * 32),
+                 sdesc_add(od, (k / 4) * C::kQBox + (k % 4) * 32), idSP, k > 0);
       };
-      auto issue_dV_dK = [&](int it, int b, uint32_t q, uint32_t o, bool which_dk) {
+      auto issue_dV_dK = [&](int it, int b, int s, bool which_dk) {
         // dV += P^T dO_i or dK += dS^T Q_i (K = queries; A = packed bf16 in TMEM)
+        const uint64_t bd = stage_desc(s, !which_dk, true);
+        const uint32_t acc_col = which_dk ? C::kColDK : C::kColDV;
+        const uint32_t a_col = which_dk ? C::colDP(b) : C::colS(b);
 #pragma unroll
-        for (int k = 0; k < BQ / 16; ++k) {
-          if (!which_dk)
-            mma_ts(tmem + C::kColDV, packed_col<C::kCols>(tmem + C::colS(b), k),
-                   sdesc_sw128(o + k * 2048, C::kQBox, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
-          else
-            mma_ts(tmem + C::kColDK, packed_col<C::kCols>(tmem + C::colDP(b), k),
-                   sdesc_sw128(q + k * 2048, C::kQBox, 1024), idKV, (it > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < BQ / 16; ++k)
+          mma_ts(tmem + acc_col, packed_col<C::kCols>(tmem + a_col, k), sdesc_add(bd, k * 2048), idKV,
+                 (it > 0 || k > 0) ? 1u : 0u);
       };
-      auto issue_dQ = [&](int b, uint32_t ds) {
+      auto issue_dQ = [&](int b, int dsbuf) {
         // dQ partial (K = keys) over this buffer's S^T columns (P^T was read by dV, in
         // issue order).
+        const uint64_t dsd = sdesc_sw128(aDs + dsbuf * C::kDsBytes, BN * 128, 1024);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           if constexpr (C::kDqT)
-            mma_ss(tmem + C::colS(b), sdesc_sw128(aK + k * 2048, BN * 128, 1024),
-                   sdesc_sw128(ds + k * 2048, BN * 128, 1024), idQ, k > 0);
+            mma_ss(tmem + C::colS(b), sdesc_add(dK_mn, k * 2048), sdesc_add(dsd, k * 2048), idQ, k > 0);
           else
-            mma_ss(tmem + C::colS(b), sdesc_sw128(ds + k * 2048, BN * 128, 1024),
-                   sdesc_sw128(aK + k * 2048, BN * 128, 1024), idQ, k > 0);
+            mma_ss(tmem + C::colS(b), sdesc_add(dsd, k * 2048), sdesc_add(dK_mn, k * 2048), idQ, k > 0);
         }
       };
       bool ok = mbar_wait(&ctl.kv_full, 0, p.status, abort);
@@ -281,11 +280,9 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         for (int it = 0; ok && it < nq; ++it) {
           const int s = it % C::kStages;
           const int b = it & 1;
-          const uint32_t q = aStage + s * C::kStageBytes, o = q + C::kQBytes;
-          const uint32_t ds = aDs + (it & 1) * C::kDsBytes;
           if (!(ok = mbar_wait(&ctl.sm_done[b], (it / 2) & 1, p.status, abort))) break;
           tc_fence_after();
-          issue_dV_dK(it, b, q, o, false);
+          issue_dV_dK(it, b, s, false);
           // The previous partial dQ(i-1) sits in buffer b^1's S^T columns; it must have been
           // read out before S(i+1) overwrites them (and before dQ(i) is handed off, so the
           // two hand-off barriers stay one phase apart).
@@ -295,8 +292,8 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             issue_S((it + 1) % C::kStages, b ^ 1);  // stage it+1 was waited for with dP(i+1)
             mma_commit(&ctl.s_full[b ^ 1]);
           }
-          issue_dV_dK(it, b, q, o, true);
-          issue_dQ(b, ds);
+          issue_dV_dK(it, b, s, true);
+          issue_dQ(b, it & 1);
           mma_commit(&ctl.dq_full);
           mma_commit(&ctl.stage_empty[s]);
           if (it + 2 < nq) {
@@ -317,14 +314,12 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
         for (int it = 0; ok && it < nq; ++it) {
           const int s = it % C::kStages;
-          const uint32_t q = aStage + s * C::kStageBytes, o = q + C::kQBytes;
-          const uint32_t ds = aDs + (it & 1) * C::kDsBytes;
           if (!(ok = mbar_wait(&ctl.sm_done[0], it & 1, p.status, abort))) break;
           tc_fence_after();
-          issue_dV_dK(it, 0, q, o, false);
-          issue_dV_dK(it, 0, q, o, true);
+          issue_dV_dK(it, 0, s, false);
+          issue_dV_dK(it, 0, s, true);
           if (it > 0 && !(ok = mbar_wait(&ctl.dq_empty, (it - 1) & 1, p.status, abort))) break;
-          issue_dQ(0, ds);
+          issue_dQ(0, it & 1);
           mma_commit(&ctl.dq_full);
           mma_commit(&ctl.stage_empty[s]);
           if (it + 1 < nq) {

@@ -167,20 +167,23 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const uint32_t sQ = smem_u32(smem + C::kQOff);
       const uint32_t sK = smem_u32(smem + C::kKOff);
       const uint32_t sV = smem_u32(smem + C::kVOff);
+      // Base descriptors; each MMA below only advances the start address.
+      const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sV, kBoxBytes, 1024);
       auto issue_S = [&](int t, int s) {
-        const uint32_t qa = sQ + t * C::kBoxes * kBoxBytes, ka = sK + s * C::kBoxes * kBoxBytes;
+        const uint32_t qo = t * C::kBoxes * kBoxBytes, ko = s * C::kBoxes * kBoxBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32;
-          mma_ss(tmem + C::colS(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS,
-                 k > 0);
+          mma_ss(tmem + C::colS(t), sdesc_add(dQ0, qo + off), sdesc_add(dK0, ko + off), idS, k > 0);
         }
       };
       auto issue_PV = [&](int t, int s, bool acc) {
-        const uint32_t va = sV + s * C::kBoxes * kBoxBytes;
+        const uint32_t vo = s * C::kBoxes * kBoxBytes;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          mma_ts(tmem + C::colO(t), tmem + C::colS(t) + k * 8, sdesc_sw128(va + k * 2048, kBoxBytes, 1024), idO,
+          mma_ts(tmem + C::colO(t), tmem + C::colS(t) + k * 8, sdesc_add(dV0, vo + k * 2048), idO,
                  (acc || k > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(&ctl.q_full, 0, p.status, abort) && mbar_wait(&ctl.k_full[0], 0, p.status, abort);

@@ -67,20 +67,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete may be suspended (up to
+// kSuspendNs) until the phase completes, instead of returning at once: waiting warps then
+// leave the issue slots of their sub-partition to the warps that have work.
+constexpr uint32_t kSuspendNs = 100000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the phase with parity `parity` of `bar` has completed. Gives up after
-// kWaitLimitNs, or at once when *abort is set by another role of the CTA; on giving up
-// it records FA_ERR_DEVICE_TIMEOUT in *status, sets *abort and returns false. A null
+// kWaitLimitNs, or soon after *abort is set by another role of the CTA; on giving up it
+// records FA_ERR_DEVICE_TIMEOUT in *status, sets *abort and returns false. A null
 // `abort` means: ignore other roles and wait (still bounded), as the drain paths need.
-// The poll itself is a tight try_wait loop; the (slow) global timer and the abort flag
-// are consulted once every 256 polls so that a completed phase is noticed promptly.
+// Each poll may sleep up to kSuspendNs; the global timer and the abort flag are checked
+// every 8 polls, so the limit holds within a millisecond.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait_sleep(bar, parity)) return true;
     if (abort && *abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       if (status) atomicExch(status, kErrTimeout);
@@ -200,6 +215,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
          ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Advance a shared-memory descriptor's start address by `bytes` (a multiple of 16) with
+// one 32-bit add. The 14-bit start field holds address/16, and every address of the
+// (<= 228 KB) shared window is below 2^18 bytes, so the sum never carries into LBO.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(d));
+  lo += bytes >> 4;
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
 }
 
 // TMEM address of (lane, column).
