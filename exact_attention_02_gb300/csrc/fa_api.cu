@@ -35,7 +35,6 @@ fa_status_t check_shape(const Shape& s, int dtype, float* scale) {
   if (bh * s.N > (int64_t(1) << 50) || s.elems() > (int64_t(1) << 60)) return FA_ERR_INVALID_ARG;
   if (scale && !(isfinite(*scale) && *scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (s.d != 64 && s.d != 128) return FA_ERR_UNSUPPORTED;
-  if (dtype == FA_DTYPE_BF16 && s.N % 128 != 0) return FA_ERR_UNSUPPORTED;
   // TMA coordinates are 32-bit row indices into the [B*H*N, d] view.
   if (dtype == FA_DTYPE_BF16 && bh * s.N > INT32_MAX) return FA_ERR_UNSUPPORTED;
   if (dtype == FA_DTYPE_FP32 && s.N > 4096) return FA_ERR_UNSUPPORTED;

@@ -31,6 +31,10 @@
 //
 // CTA = 14 warps: 0-7 softmax (two warpgroups splitting the query columns), 8-11 dQ
 // reduction + dK/dV epilogue, 12 TMA producer, 13 MMA issuer.
+//
+// Any N: Q/K/V/dO are read through [heads, N, d] tensor maps (rows past the end of a head
+// arrive as zeros), queries past the end get LSE = +inf (P = 0), and dQ/dK/dV rows past
+// the end are neither accumulated nor stored.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -105,14 +109,6 @@ struct BwdParams {
   float sl2;  // scale * log2(e)
 };
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // TMEM column of the packed bf16 operand for query block k (16 queries) when each of the
 // two softmax warpgroups packs its kCols queries into the first kCols/2 columns of its
 // half of the buffer.
@@ -153,7 +149,7 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (threadIdx.x == 0) {
     mbar_init(&ctl.kv_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&ctl.stage_full[s], 1);
+      mbar_init(&ctl.stage_full[s], 2);
       mbar_init(&ctl.stage_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -177,6 +173,10 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint8_t* sV = smem + C::kVOff;
 
   if (warp == kLoadWarp) {
+    // Lane 0 drives the TMA copies and the barriers; the whole warp stages LSE_i and D_i
+    // with bounds-checked loads (queries past the end of the head get LSE = +inf, D = 0,
+    // so their P and dS are exactly zero). A stage completes after the TMA bytes, lane 0's
+    // expect_tx arrival and its second arrival once the warp's stores are done.
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
@@ -184,26 +184,37 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       prefetch_tmap(&tmdO);
       mbar_expect_tx(&ctl.kv_full, 2 * C::kKVBytes);
       for (int b = 0; b < C::kBoxes; ++b) {
-        tma_load_2d(sK + b * (BN * 128), &tmK, &ctl.kv_full, b * 64, row_base + kt * BN);
-        tma_load_2d(sV + b * (BN * 128), &tmV, &ctl.kv_full, b * 64, row_base + kt * BN);
+        tma_load_3d(sK + b * (BN * 128), &tmK, &ctl.kv_full, b * 64, kt * BN, head);
+        tma_load_3d(sV + b * (BN * 128), &tmV, &ctl.kv_full, b * 64, kt * BN, head);
       }
-      int last[3] = {-1, -1, -1};
-      for (int it = 0; it < nq; ++it) {
-        const int s = it % C::kStages;
-        if (it >= C::kStages && !mbar_wait(&ctl.stage_empty[s], ((it / C::kStages) - 1) & 1, p.status, abort))
-          break;
-        const int qrow = row_base + (q_first + it) * BQ;
-        uint8_t* st = smem + C::kStageOff + s * C::kStageBytes;
-        float* vec = reinterpret_cast<float*>(smem + C::kVecOff + s * C::kVecBytes);
-        mbar_expect_tx(&ctl.stage_full[s], C::kStageBytes + C::kVecBytes);
+    }
+    int last[3] = {-1, -1, -1};
+    for (int it = 0; it < nq; ++it) {
+      const int s = it % C::kStages;
+      bool ok = true;
+      if (lane == 0 && it >= C::kStages)
+        ok = mbar_wait(&ctl.stage_empty[s], ((it / C::kStages) - 1) & 1, p.status, abort);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      const int q0 = (q_first + it) * BQ;  // first query of the tile, within the head
+      uint8_t* st = smem + C::kStageOff + s * C::kStageBytes;
+      float* vec = reinterpret_cast<float*>(smem + C::kVecOff + s * C::kVecBytes);
+      if (lane == 0) {
+        mbar_expect_tx(&ctl.stage_full[s], C::kStageBytes);
         for (int b = 0; b < C::kBoxes; ++b) {
-          tma_load_2d(st + b * C::kQBox, &tmQ, &ctl.stage_full[s], b * 64, qrow);
-          tma_load_2d(st + C::kQBytes + b * C::kQBox, &tmdO, &ctl.stage_full[s], b * 64, qrow);
+          tma_load_3d(st + b * C::kQBox, &tmQ, &ctl.stage_full[s], b * 64, q0, head);
+          tma_load_3d(st + C::kQBytes + b * C::kQBox, &tmdO, &ctl.stage_full[s], b * 64, q0, head);
         }
-        bulk_load(vec, p.LSE + qrow, BQ * 4, &ctl.stage_full[s]);
-        bulk_load(vec + BQ, p.Dvec + qrow, BQ * 4, &ctl.stage_full[s]);
-        last[s] = it;
       }
+      for (int c = lane; c < BQ; c += 32) {
+        const bool in = q0 + c < p.N;
+        vec[c] = in ? p.LSE[row_base + q0 + c] : INFINITY;
+        vec[BQ + c] = in ? p.Dvec[row_base + q0 + c] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.stage_full[s]);
+      last[s] = it;
+    }
+    if (lane == 0) {
       mbar_wait(&ctl.kv_full, 0, p.status, nullptr);
       for (int s = 0; s < C::kStages; ++s)
         if (last[s] >= 0) mbar_wait(&ctl.stage_full[s], (last[s] / C::kStages) & 1, p.status, nullptr);
@@ -418,6 +429,7 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       const int q0 = row_base + (q_first + it) * BQ;
+      const int nvalid = p.N - (q_first + it) * BQ;  // queries of the tile inside the head
       const uint32_t colQ = C::colS(it % C::NB);
       if constexpr (C::kDqT) {
         // lane = head-dim index r; columns = the BQ queries of the tile, drained in two
@@ -433,7 +445,8 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             mbar_arrive(&ctl.dq_empty);
           }
 #pragma unroll 16
-          for (int c = 0; c < 64; ++c) atomicAdd(dst + (size_t)(h + c) * D, v[c]);
+          for (int c = 0; c < 64; ++c)
+            if (h + c < nvalid) atomicAdd(dst + (size_t)(h + c) * D, v[c]);
         }
       } else {
         // lane = query row r of the tile; columns = head dim
@@ -445,14 +458,18 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         tc_fence_before();
         mbar_arrive(&ctl.dq_empty);
         float4* dst = reinterpret_cast<float4*>(p.dQacc + (size_t)(q0 + r) * D);
+        if (r < nvalid) {
 #pragma unroll
-        for (int c = 0; c < D / 4; ++c) atomicAdd(dst + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+          for (int c = 0; c < D / 4; ++c)
+            atomicAdd(dst + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+        }
       }
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.kv_done, 0, p.status, abort));
     if (ok) {
       tc_fence_after();
       const size_t row = (size_t)row_base + kt * BN + r;
+      const bool in = kt * BN + r < p.N;  // key rows past the end of the head are not stored
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         float v[32];
@@ -462,14 +479,18 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
         uint4* dv = reinterpret_cast<uint4*>(p.dV + row * D + c0);
+        if (in) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) dv[u] = w[u];
+          for (int u = 0; u < 4; ++u) dv[u] = w[u];
+        }
         tmem_ld32(tmem + lane_off + C::kColDK + c0, v);
 #pragma unroll
         for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u] * p.scale, v[2 * u + 1] * p.scale);
         uint4* dk = reinterpret_cast<uint4*>(p.dK + row * D + c0);
+        if (in) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) dk[u] = w[u];
+          for (int u = 0; u < 4; ++u) dk[u] = w[u];
+        }
       }
     }
   }
@@ -504,9 +525,9 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
                    float scale, bool causal, int* status, cudaStream_t st) {
   using C = BwdCfg<D>;
   CUtensorMap mq, mk, mv, mdo;
-  const int64_t rows = s.rows();
-  if (!make_map_bf16_2d(&mq, Q, rows, D, C::BQ) || !make_map_bf16_2d(&mk, K, rows, D, BN) ||
-      !make_map_bf16_2d(&mv, V, rows, D, BN) || !make_map_bf16_2d(&mdo, dO, rows, D, C::BQ))
+  const int64_t heads = s.heads();
+  if (!make_map_bf16_3d(&mq, Q, heads, s.N, D, C::BQ) || !make_map_bf16_3d(&mk, K, heads, s.N, D, BN) ||
+      !make_map_bf16_3d(&mv, V, heads, s.N, D, BN) || !make_map_bf16_3d(&mdo, dO, heads, s.N, D, C::BQ))
     return cudaErrorInvalidValue;
   static bool attr = [] {
     return cudaFuncSetAttribute(fa_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -524,8 +545,8 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
   p.status = status;
   p.N = s.N;
   p.heads = (int)s.heads();
-  p.kvtiles = s.N / BN;
-  p.qtiles = s.N / C::BQ;
+  p.kvtiles = (s.N + BN - 1) / BN;
+  p.qtiles = (s.N + C::BQ - 1) / C::BQ;
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.sl2 = scale * kLog2e;

@@ -24,6 +24,8 @@
 // O and l always share the same reference max, and O / l cancels it.
 //
 // Causal: tile t sees K tiles 0..qtile_t; the diagonal tile masks key > query.
+// Any N: Q/K/V are read through [heads, N, d] tensor maps, so rows past the end of a head
+// arrive as zeros; keys past the end are masked and rows past the end are not stored.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -135,8 +137,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_expect_tx(&ctl.q_full, (act1 ? 2 : 1) * C::kTileBytes);
       for (int t = 0; t < (act1 ? 2 : 1); ++t)
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_2d(smem + C::kQOff + (t * C::kBoxes + b) * kBoxBytes, &tmQ, &ctl.q_full, b * 64,
-                      row_base + (qt0 + t) * BM);
+          tma_load_3d(smem + C::kQOff + (t * C::kBoxes + b) * kBoxBytes, &tmQ, &ctl.q_full, b * 64,
+                      (qt0 + t) * BM, head);
       int last[4] = {-1, -1, -1, -1};
       for (int j = 0; j < nkv; ++j) {
         const int s = j % C::kStages;
@@ -144,12 +146,12 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           break;
         mbar_expect_tx(&ctl.k_full[s], C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_2d(smem + C::kKOff + (s * C::kBoxes + b) * kBoxBytes, &tmK, &ctl.k_full[s], b * 64,
-                      row_base + j * BN);
+          tma_load_3d(smem + C::kKOff + (s * C::kBoxes + b) * kBoxBytes, &tmK, &ctl.k_full[s], b * 64,
+                      j * BN, head);
         mbar_expect_tx(&ctl.v_full[s], C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_2d(smem + C::kVOff + (s * C::kBoxes + b) * kBoxBytes, &tmV, &ctl.v_full[s], b * 64,
-                      row_base + j * BN);
+          tma_load_3d(smem + C::kVOff + (s * C::kBoxes + b) * kBoxBytes, &tmV, &ctl.v_full[s], b * 64,
+                      j * BN, head);
         last[s] = j;
       }
       // Every issued copy must land before the CTA may exit.
@@ -247,10 +249,16 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       tmem_ld32x2(tS, tS + 32, *reinterpret_cast<float(*)[32]>(&sv[0]), *reinterpret_cast<float(*)[32]>(&sv[32]));
       tmem_ld32x2(tS + 64, tS + 96, *reinterpret_cast<float(*)[32]>(&sv[64]),
                   *reinterpret_cast<float(*)[32]>(&sv[96]));
-      if (p.causal && j == qt0 + t) {
+      // Hidden keys: key > query on the diagonal tile (causal), and keys past the end of
+      // the head in its last, partial tile (their rows were read as zeros). Every row keeps
+      // at least key 0 of the tile visible.
+      const bool diag = p.causal && j == qt0 + t;
+      const int valid = p.N - j * BN;
+      if (diag || valid < BN) {
+        const int lim = min(diag ? r : BN - 1, valid - 1);  // keep columns c <= lim
 #pragma unroll
         for (int c = 0; c < BN; ++c)
-          if (c > r) sv[c] = -INFINITY;
+          if (c > lim) sv[c] = -INFINITY;
       }
       // row max: four independent chains of 3-input max
       float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
@@ -321,10 +329,12 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(ov[2 * u] * inv_l, ov[2 * u + 1] * inv_l);
         uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+        if (qrow < p.N) {  // rows past the end of the head belong to no query
 #pragma unroll
-        for (int u = 0; u < 4; ++u) dst[u] = w[u];
+          for (int u = 0; u < 4; ++u) dst[u] = w[u];
+        }
       }
-      p.LSE[row_base + qrow] = (m + log2f(l)) * kLn2;
+      if (qrow < p.N) p.LSE[row_base + qrow] = (m + log2f(l)) * kLn2;
     }
   }
 
@@ -341,9 +351,9 @@ cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* 
                    float scale, bool causal, int* status, cudaStream_t st) {
   using C = FwdCfg<D>;
   CUtensorMap mq, mk, mv;
-  const int64_t rows = s.rows();
-  if (!make_map_bf16_2d(&mq, Q, rows, D, BM) || !make_map_bf16_2d(&mk, K, rows, D, BN) ||
-      !make_map_bf16_2d(&mv, V, rows, D, BN))
+  const int64_t heads = s.heads();
+  if (!make_map_bf16_3d(&mq, Q, heads, s.N, D, BM) || !make_map_bf16_3d(&mk, K, heads, s.N, D, BN) ||
+      !make_map_bf16_3d(&mv, V, heads, s.N, D, BN))
     return cudaErrorInvalidValue;
   static bool attr = [] {
     return cudaFuncSetAttribute(fa_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -356,7 +366,7 @@ cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.status = status;
   p.N = s.N;
   p.heads = (int)s.heads();
-  p.qtiles = s.N / BM;
+  p.qtiles = (s.N + BM - 1) / BM;
   p.pairs = (p.qtiles + 1) / 2;
   p.causal = causal ? 1 : 0;
   p.sl2 = scale * 1.4426950408889634f;

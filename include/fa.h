@@ -18,8 +18,8 @@
  *   Layout   Q, K, V, O, dO, dQ, dK, dV: contiguous row-major [B, H, N, d]; all share
  *            one element type (dtype). LSE and D: contiguous float32 [B, H, N].
  *   dtype    FA_DTYPE_BF16 (tensor-core path) or FA_DTYPE_FP32 (exact FFMA path).
- *   Shapes   B, H, N >= 1; d in {64, 128}. bf16: N a multiple of 128.
- *            fp32: N <= 4096. B*H*N*d must fit in a signed 64-bit count and B*H < 2^31.
+ *   Shapes   B, H, N >= 1 (any N: partial last tiles are handled); d in {64, 128}.
+ *            bf16: B*H*N < 2^31. fp32: N <= 4096. B*H < 2^31.
  *   scale    finite and > 0; scores are s_ij = scale * q_i . k_j (1/sqrt(d) on the pages).
  *   causal   0: every key is visible. 1: key j is hidden from query i when j > i.
  *   Pointers device pointers (cudaMalloc or torch), 16-byte aligned, non-overlapping

@@ -93,6 +93,15 @@ SMALL = [
     Workload("bf16_n384_d128_causal", 3, 1, 384, 128, "bf16", True, seed=8),
     Workload("bf16_n640_d64_causal_qk2", 1, 2, 640, 64, "bf16", True, qk_gain=2.0, seed=9),
     Workload("bf16_n512_d128_qk4", 1, 1, 512, 128, "bf16", False, qk_gain=4.0, seed=10),
+    # partial last tiles: N not a multiple of the 128-row tile
+    Workload("bf16_n1_d64_causal", 1, 2, 1, 64, "bf16", True, seed=20),
+    Workload("bf16_n65_d64", 2, 1, 65, 64, "bf16", False, seed=21),
+    Workload("bf16_n100_d128", 1, 3, 100, 128, "bf16", False, seed=22),
+    Workload("bf16_n129_d128_causal", 1, 2, 129, 128, "bf16", True, seed=23),
+    Workload("bf16_n200_d64_causal", 2, 1, 200, 64, "bf16", True, seed=24),
+    Workload("bf16_n333_d128_causal", 2, 1, 333, 128, "bf16", True, seed=25),
+    Workload("bf16_n777_d128_qk2", 1, 2, 777, 128, "bf16", False, qk_gain=2.0, seed=26),
+    Workload("bf16_n2000_d128_causal", 1, 2, 2000, 128, "bf16", True, seed=27),
 ]
 
 

@@ -38,7 +38,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     # 2 x 16 x 8192 x 128 = 33.5 M elements > FA_NOALLOC_MAX_ELEMS (8 M)
     assert f(*ptrs, 2, 16, 8192, 128, 0.088, 1, fa.FA_DTYPE_BF16, None) == fa.FA_ERR_WORKSPACE
     # argument errors are reported as fa_bwd reports them
-    assert f(*ptrs, 1, 1, 100, 128, 0.088, 1, fa.FA_DTYPE_BF16, None) == fa.FA_ERR_UNSUPPORTED
+    assert f(*ptrs, 1, 1, 128, 96, 0.088, 1, fa.FA_DTYPE_BF16, None) == fa.FA_ERR_UNSUPPORTED
     assert f(*ptrs, 0, 1, 128, 128, 0.088, 1, fa.FA_DTYPE_BF16, None) == fa.FA_ERR_INVALID_ARG
 
 
