@@ -22,7 +22,10 @@ Readings where the pages leave a choice open:
     which packs the pages' two ledger rows (m, l) into one.
   * D_i uses the oracle's own float64 O.
   * Causal attention hides key j from query i iff j > i (queries and keys share
-    the same positions; the diagonal is always visible, so no row is empty).
+    the same positions; the diagonal is always visible, so no row is empty). With
+    fewer queries than keys (N_q < N_k, e.g. decoding against a cache) the queries are
+    the last N_q positions: query row i sits at position i + N_k - N_q and hides keys
+    j > i + N_k - N_q (bottom-right alignment; the pages only show N_q = N_k).
 
 Evaluation order: every quantity is computed from its definition, a whole row of
 scores at a time. To bound memory the rows of a head are taken in groups; rows
@@ -55,8 +58,9 @@ def scores(q, k, scale, causal, rows):
     rows = np.asarray(rows)
     s = scale * (q[rows] @ k.T)
     if causal:
+        offset = k.shape[0] - q.shape[0]  # query row i sits at key position i + offset
         j = np.arange(k.shape[0])
-        s = np.where(j[None, :] > rows[:, None], -np.inf, s)
+        s = np.where(j[None, :] > rows[:, None] + offset, -np.inf, s)
     return s
 
 

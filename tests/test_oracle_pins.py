@@ -326,6 +326,26 @@ def pin_row_sampling(m):
         assert np.allclose(Ls, L[rows], atol=1e-15)
 
 
+def pin_fewer_queries_than_keys(m):
+    """N_q < N_k (bottom-right causal alignment): the N_q queries are the last N_q
+    positions, so their outputs equal the last N_q rows of the square problem in which
+    the same queries sit at those positions; one query sees every key."""
+    Nk, Nq, d = 23, 5, 4
+    qf, k, v = (_rand((Nk, d), 500 + s) for s in range(3))
+    O_full, L_full = m.head_forward(qf, k, v, 0.5, True)
+    O, L = m.head_forward(qf[-Nq:], k, v, 0.5, True)
+    assert np.allclose(O, O_full[-Nq:], rtol=0, atol=1e-14)
+    assert np.allclose(L, L_full[-Nq:], rtol=0, atol=1e-14)
+    O1c, L1c = m.head_forward(qf[-1:], k, v, 0.5, True)
+    O1n, L1n = m.head_forward(qf[-1:], k, v, 0.5, False)
+    assert np.allclose(O1c, O1n, rtol=0, atol=1e-15) and np.allclose(L1c, L1n, rtol=0, atol=1e-15)
+    # query i of the short block sees keys 0 .. i + Nk - Nq: brute force on row 0
+    vis = Nk - Nq + 1
+    s0 = 0.5 * k[:vis] @ qf[-Nq]
+    p0 = np.exp(s0 - s0.max())
+    assert np.allclose(O[0], (p0 / p0.sum()) @ v[:vis], rtol=0, atol=1e-14)
+
+
 PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]
 
 
@@ -357,6 +377,7 @@ MUTATIONS = [
     ("dP uses K instead of V", "dP = do[r] @ v.T", "dP = do[r] @ k.T"),
     ("mask hides diagonal", "j[None, :] > rows[:, None]", "j[None, :] >= rows[:, None]"),
     ("mask keeps the future", "j[None, :] > rows[:, None]", "j[None, :] < rows[:, None]"),
+    ("top-left alignment for fewer queries", "offset = k.shape[0] - q.shape[0]", "offset = 0"),
     ("max not subtracted from LSE", "LSE[a:a + g] = m + np.log(l)", "LSE[a:a + g] = np.log(l)"),
     ("log2 in LSE", "LSE[a:a + g] = m + np.log(l)", "LSE[a:a + g] = m + np.log2(l)"),
     ("D from dO.dO", 'np.einsum("ic,ic->i", np.asarray(do, np.float64), np.asarray(o, np.float64))',
