@@ -27,6 +27,7 @@ BF16_KERNEL_BOUND = {"fa_fwd": "tensor", "fa_bwd": "tensor", "fa_bwd_preprocess"
 # cudaMemsetAsync, not a library kernel).
 BF16_KERNELS = {"fa_fwd": ["fa_fwd_tc_kernel"], "fa_bwd_preprocess": ["preprocess_kernel"],
                 "fa_bwd": ["fa_bwd_tc_kernel", "dq_convert_kernel"]}
+SPLITKV_KERNELS = ["splitkv_partial_kernel", "splitkv_merge_kernel"]
 FP32_KERNELS = {"fa_fwd": ["simt_fwd_kernel"], "fa_bwd_preprocess": ["preprocess_kernel"],
                 "fa_bwd": ["simt_bwd_dkdv_kernel", "simt_bwd_dq_kernel"]}
 
@@ -56,6 +57,10 @@ def _load():
     L.fa_bwd_workspace_size.restype = sz
     L.fa_bwd.argtypes = [vp] * 11 + [sz, i, i, i, i, f, i, i, vp]
     L.fa_bwd.restype = i
+    L.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
+    L.fa_fwd_splitkv_workspace_size.restype = sz
+    L.fa_fwd_splitkv.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, i, vp, sz, vp]
+    L.fa_fwd_splitkv.restype = i
     L.fa_get_error_string.argtypes = [i]
     L.fa_get_error_string.restype = ctypes.c_char_p
     L.fa_get_last_device_status.argtypes = []
@@ -161,6 +166,31 @@ def fa_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None, D=None
                           _p(workspace), wbytes, B, H, N, d, scale, int(bool(causal)), _dtype_code(q),
                           _stream_ptr(stream)), "fa_bwd")
     return dq, dk, dv
+
+
+def fa_fwd_splitkv(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None, workspace=None,
+                   stream=None):
+    """O, LSE for a few queries q [B,H,Nq,d] against k, v [B,H,Nk,d] (see ``fa_fwd_splitkv`` in fa.h)."""
+    import torch
+    B, H, Nq, d = _shape(q)
+    Nk = int(k.shape[2])
+    if k.shape != v.shape or tuple(k.shape[:2]) != (B, H) or int(k.shape[3]) != d:
+        raise ValueError("k and v must be [B, H, Nk, d] with the batch, heads and d of q")
+    for t in (q, k, v):
+        if not t.is_contiguous() or t.dtype != q.dtype or t.device != q.device:
+            raise ValueError("q, k, v must be contiguous and share dtype and device")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    code = _dtype_code(q)
+    need = int(_load().fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, code))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    _check(_load().fa_fwd_splitkv(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, Nq, Nk, d, scale,
+                                  int(bool(causal)), code, _p(workspace), wbytes, _stream_ptr(stream)),
+           "fa_fwd_splitkv")
+    return o, lse
 
 
 def fa_get_last_device_status() -> int:

@@ -120,6 +120,37 @@ extern "C" fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const
   return fa::from_cuda(fa::simt_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal == 1, false, st));
 }
 
+namespace {
+fa_status_t check_splitkv(int B, int H, int Nq, int Nk, int d, float scale, int causal, int dtype) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
+  if (!(isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((int64_t)B * H >= (int64_t(1) << 31) || (int64_t)B * H * Nk > (int64_t(1) << 50)) return FA_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 || (d != 64 && d != 128) || Nq > 16) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+}  // namespace
+
+extern "C" size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int dtype) {
+  if (check_splitkv(B, H, Nq, Nk, d, 1.f, 0, dtype) != FA_OK) return 0;
+  return fa::splitkv_workspace_floats((int64_t)B * H, Nq, Nk, d) * sizeof(float);
+}
+
+extern "C" fa_status_t fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                      int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                                      int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  fa_status_t r = check_splitkv(B, H, Nq, Nk, d, scale, causal, dtype);
+  if (r != FA_OK) return r;
+  if ((r = fa::check_ptrs({Q, K, V, O, LSE})) != FA_OK) return r;
+  const size_t need = fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, dtype);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (!fa::aligned16(workspace)) return FA_ERR_INVALID_ARG;
+  return fa::from_cuda(fa::splitkv_fwd(Q, K, V, O, LSE, (int64_t)B * H, Nq, Nk, d, scale, causal == 1,
+                                       static_cast<float*>(workspace), static_cast<cudaStream_t>(stream)));
+}
+
 extern "C" const char* fa_get_error_string(fa_status_t status) {
   switch (status) {
     case FA_OK: return "FA_OK";

@@ -128,6 +128,25 @@ FA_API fa_status_t fa_bwd_noalloc(const void* Q, const void* K, const void* V, c
                            int B, int H, int N, int d, float scale, int causal, int dtype,
                            void* stream);
 
+/*
+ * fa_fwd_splitkv — forward for a few queries against a long key/value sequence (a
+ * decoding step against a cache): same outputs as fa_fwd, with N_q query rows and N_k
+ * key/value rows per head. The keys are split into chunks handled in parallel, each
+ * keeping the online-softmax state (m, l, un-normalised O) of "flash-attention-v2-sram-
+ * tiling" §5; the chunk states are merged with the rule of "知识点13" §4
+ * (m = max m_s, l = sum l_s e^(m_s - m), O = sum O_s e^(m_s - m) / l).
+ * In:  Q [B,H,N_q,d], K and V [B,H,N_k,d] bf16.  Out: O [B,H,N_q,d] bf16, LSE [B,H,N_q] fp32.
+ * causal: the queries are the last N_q positions (requires N_q <= N_k): query i hides
+ *      keys j > i + N_k - N_q. causal = 0: every key is visible.
+ * Supported: bf16, d in {64, 128}, 1 <= N_q <= 16 (else FA_ERR_UNSUPPORTED); any N_k >= 1.
+ * workspace: device buffer of at least fa_fwd_splitkv_workspace_size(...) bytes (fp32
+ *      chunk states); its contents on entry do not matter.
+ */
+FA_API size_t fa_fwd_splitkv_workspace_size(int B, int H, int Nq, int Nk, int d, int dtype);
+FA_API fa_status_t fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                           int B, int H, int Nq, int Nk, int d, float scale, int causal, int dtype,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
 /* Text for a status code (static storage; never NULL). */
 FA_API const char* fa_get_error_string(fa_status_t status);
 

@@ -29,7 +29,8 @@ def _declared():
 
 def test_header_declares_the_boundary():
     assert set(_declared()) >= {"fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_bwd_workspace_size",
-                                "fa_get_error_string", "fa_get_last_device_status"}
+                                "fa_get_error_string", "fa_get_last_device_status", "fa_fwd_splitkv",
+                                "fa_fwd_splitkv_workspace_size"}
 
 
 def test_exports_every_declared_symbol(lib):
@@ -111,3 +112,26 @@ def test_binding_refuses_to_run_without_library(monkeypatch):
     monkeypatch.setattr(fa, "LIB_PATH", os.path.join(ROOT, "does_not_exist.so"))
     with pytest.raises(RuntimeError, match="not built"):
         fa.lib()
+
+
+def _splitkv(lib, ws=P, wsb=1 << 30, **kw):
+    a = dict(B=1, H=2, Nq=1, Nk=1000, d=128, scale=0.088, causal=1, dtype=0)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.fa_fwd_splitkv(vp(P), vp(P), vp(P), vp(P), vp(P), a["B"], a["H"], a["Nq"], a["Nk"], a["d"],
+                              ctypes.c_float(a["scale"]), a["causal"], a["dtype"], vp(ws), ctypes.c_size_t(wsb), None)
+
+
+def test_splitkv_workspace_and_rejects(lib):
+    import exact_attention_02_gb300 as fa
+    n = fa.lib().fa_fwd_splitkv_workspace_size(1, 2, 1, 1000, 128, 0)
+    assert n > 0 and n % 4 == 0
+    assert fa.lib().fa_fwd_splitkv_workspace_size(1, 2, 17, 1000, 128, 0) == 0
+    assert _splitkv(lib, Nq=17) == 2            # more queries than the split-KV path takes
+    assert _splitkv(lib, d=96) == 2
+    assert _splitkv(lib, dtype=1) == 2          # fp32 goes through fa_fwd
+    assert _splitkv(lib, Nq=8, Nk=4) == 1       # causal needs N_q <= N_k
+    assert _splitkv(lib, Nk=0) == 1
+    assert _splitkv(lib, scale=-1.0) == 1
+    assert _splitkv(lib, ws=0) == 5
+    assert _splitkv(lib, wsb=16) == 5

@@ -1,0 +1,72 @@
+"""Split-KV forward (few queries against a long key/value sequence) against the fp64 oracle.
+
+Tolerances as for the bf16 forward: O max-abs <= 2e-2, LSE max-abs <= 1e-3. Causal cases
+place the N_q queries at the last N_q key positions (bottom-right alignment).
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import exact_attention_02_gb300 as fa  # noqa: E402
+from exact_attention_02_gb300.workloads import round_to_bf16  # noqa: E402
+from oracle import attention as ora  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_attention_02_gb300.build import build
+    build()
+    fa.lib()
+
+
+CASES = [  # B, H, Nq, Nk, d, causal, qk_gain
+    (1, 2, 1, 1, 128, True, 1.0),
+    (1, 2, 1, 7, 64, False, 1.0),
+    (2, 3, 1, 1000, 128, True, 1.0),
+    (1, 4, 3, 4096, 128, True, 2.0),
+    (1, 2, 4, 333, 64, False, 1.0),
+    (2, 2, 5, 2048, 128, True, 1.0),
+    (1, 2, 16, 3000, 64, True, 1.0),
+    (1, 1, 16, 16, 128, True, 4.0),
+    (1, 2, 9, 40000, 128, False, 1.0),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}H{}q{}k{}d{}{}g{}".format(*c[:5], "c" if c[5] else "", c[6]))
+def test_splitkv_matches_oracle(case):
+    B, H, Nq, Nk, d, causal, gain = case
+    rng = np.random.default_rng(Nq * 1000 + Nk)
+    q = round_to_bf16(rng.standard_normal((B, H, Nq, d), dtype=np.float32) * gain)
+    k = round_to_bf16(rng.standard_normal((B, H, Nk, d), dtype=np.float32) * gain)
+    v = round_to_bf16(rng.standard_normal((B, H, Nk, d), dtype=np.float32))
+    dev = [torch.from_numpy(a).cuda().to(torch.bfloat16) for a in (q, k, v)]
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.fa_fwd_splitkv(*dev, causal, scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_status() == fa.FA_OK
+    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    for b in range(B):
+        for h in range(H):
+            O, L = ora.head_forward(q[b, h].astype(np.float64), k[b, h].astype(np.float64),
+                                    v[b, h].astype(np.float64), scale, causal)
+            assert np.abs(o[b, h] - O).max() <= 2e-2, (b, h)
+            assert np.abs(lse[b, h] - L).max() <= 1e-3, (b, h)
+
+
+def test_splitkv_agrees_with_square_forward():
+    """The last N_q rows of a square causal forward equal the split-KV forward of those queries."""
+    B, H, N, d, Nq = 1, 4, 1536, 128, 4
+    g = torch.Generator().manual_seed(5)
+    q, k, v = (torch.randn(B, H, N, d, generator=g).cuda().to(torch.bfloat16) for _ in range(3))
+    o_full, lse_full = fa.fa_fwd(q, k, v, True)
+    o, lse = fa.fa_fwd_splitkv(q[:, :, -Nq:].contiguous(), k, v, True)
+    torch.cuda.synchronize()
+    assert (o.float() - o_full[:, :, -Nq:].float()).abs().max().item() <= 1e-2
+    assert (lse - lse_full[:, :, -Nq:]).abs().max().item() <= 1e-4
