@@ -385,6 +385,62 @@ def run_ours(args, w):
     return 0
 
 
+def run_splitkv(args):
+    """Few-query forward (fa_fwd_splitkv) on [B,H,Nq,d] queries against [B,H,Nk,d] keys/values.
+
+    HBM-bound: the algorithmic bytes are one read of K and V plus Q, O and LSE; the line
+    reports them per second against the measured HBM copy bandwidth."""
+    import numpy as np
+    import torch
+
+    import exact_attention_02_gb300 as fa
+    from exact_attention_02_gb300.build import build
+    from exact_attention_02_gb300.workloads import round_to_bf16
+
+    B, H, Nq, Nk, d, c = (int(v) for v in args.splitkv.split(","))
+    build()
+    fa.lib()
+    rng = np.random.default_rng(0)
+    q, k, v = (torch.from_numpy(round_to_bf16(rng.standard_normal(shape, dtype=np.float32))).cuda().to(torch.bfloat16)
+               for shape in ((B, H, Nq, d), (B, H, Nk, d), (B, H, Nk, d)))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(16, fa.lib().fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, 0)), dtype=torch.uint8,
+                     device="cuda")
+
+    def step():
+        fa.fa_fwd_splitkv(q, k, v, bool(c), o=o, lse=lse, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    peaks, src = load_peaks()
+    nbytes = 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    flop = 4.0 * B * H * Nq * Nk * d
+    print(json.dumps({
+        "metric": "split-KV forward HBM GB/s (few queries against a long key/value sequence)",
+        "value": gbs, "unit": "GB/s", "ms_per_step": ms, "steps": args.steps, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"splitkv_b{B}h{H}_q{Nq}_k{Nk}_d{d}" + ("_causal" if c else ""),
+                   "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": bool(c),
+                   "l2": "no flush: K and V exceed the 129 MB L2" if 2 * B * H * Nk * d * 2 > 129e6 else "fits L2"},
+        "tflops": flop / (ms * 1e-3) / 1e12,
+        "roofline": {"kernel": "fa_fwd_splitkv", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "peak_source": f"HBM copy ({src})",
+                     "traffic": None},
+        "gpu_launches": 2 * args.steps, "kernels_per_step": fa.SPLITKV_KERNELS,
+    }), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -394,6 +450,8 @@ def main():
     ap.add_argument("--workload", default=None)
     ap.add_argument("--shape", default=None,
                     help="ad-hoc bf16 workload B,H,N,d,causal (e.g. for a small profiler capture)")
+    ap.add_argument("--splitkv", default=None,
+                    help="measure fa_fwd_splitkv instead: B,H,Nq,Nk,d,causal (prints its own JSON line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-count", action="store_true", help="skip the profiler launch count")
@@ -408,6 +466,8 @@ def main():
         w = WORKLOADS[args.workload or HEADLINE]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.splitkv:
+        return run_splitkv(args)
     return run_ours(args, w)
 
 
