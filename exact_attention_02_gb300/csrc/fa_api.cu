@@ -147,8 +147,10 @@ extern "C" fa_status_t fa_fwd_splitkv(const void* Q, const void* K, const void* 
   const size_t need = fa_fwd_splitkv_workspace_size(B, H, Nq, Nk, d, dtype);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if (!fa::aligned16(workspace)) return FA_ERR_INVALID_ARG;
+  int* status = fa::device_status_ptr();
+  if (!status) return FA_ERR_CUDA;
   return fa::from_cuda(fa::splitkv_fwd(Q, K, V, O, LSE, (int64_t)B * H, Nq, Nk, d, scale, causal == 1,
-                                       static_cast<float*>(workspace), static_cast<cudaStream_t>(stream)));
+                                       static_cast<float*>(workspace), status, static_cast<cudaStream_t>(stream)));
 }
 
 extern "C" const char* fa_get_error_string(fa_status_t status) {

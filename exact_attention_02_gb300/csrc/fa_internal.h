@@ -37,10 +37,10 @@ cudaError_t tc_bwd(const void* Q, const void* K, const void* V, const void* dO, 
                    float scale, bool causal, int* status, cudaStream_t st);
 
 // ---- split-KV forward for few queries (fa_splitkv.cu): bf16, d in {64, 128}, Nq <= 16 ----
-int splitkv_splits(int64_t heads, int Nk);
 size_t splitkv_workspace_floats(int64_t heads, int Nq, int Nk, int d);
 cudaError_t splitkv_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t heads,
-                        int Nq, int Nk, int d, float scale, bool causal, float* workspace, cudaStream_t st);
+                        int Nq, int Nk, int d, float scale, bool causal, float* workspace, int* status,
+                        cudaStream_t st);
 
 // ---- memory-bound helpers (fa_simt.cu) ----
 cudaError_t preprocess_d(const void* O, const void* dO, float* D, const Shape& s, bool bf16,

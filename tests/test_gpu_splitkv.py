@@ -36,6 +36,14 @@ CASES = [  # B, H, Nq, Nk, d, causal, qk_gain
     (1, 2, 16, 3000, 64, True, 1.0),
     (1, 1, 16, 16, 128, True, 4.0),
     (1, 2, 9, 40000, 128, False, 1.0),
+    # CTA key ranges that end inside a head and cover the next head's start
+    (4, 16, 1, 300, 128, True, 1.0),
+    (2, 8, 7, 777, 64, True, 1.0),
+    # one head spread over ~150 CTAs, merged from ~150 partial states
+    (1, 1, 1, 100000, 128, False, 1.0),
+    # 1000 heads of 5 keys: dozens of short segments per CTA
+    (10, 100, 2, 5, 128, True, 1.0),
+    (1, 2, 12, 4096, 128, True, 2.0),
 ]
 
 
