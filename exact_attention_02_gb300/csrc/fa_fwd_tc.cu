@@ -74,7 +74,7 @@ struct FwdParams {
 
 struct FwdCtl {
   uint64_t q_full;
-  uint64_t k_full[4], v_full[4], kv_empty[4];
+  uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -111,7 +111,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&ctl.k_full[s], 1);
       mbar_init(&ctl.v_full[s], 1);
-      mbar_init(&ctl.kv_empty[s], 1);
+      mbar_init(&ctl.k_empty[s], 1);
+      mbar_init(&ctl.v_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ctl.s_full[t], 1);
@@ -139,28 +140,31 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         for (int b = 0; b < C::kBoxes; ++b)
           tma_load_3d(smem + C::kQOff + (t * C::kBoxes + b) * kBoxBytes, &tmQ, &ctl.q_full, b * 64,
                       (qt0 + t) * BM, head);
-      int last[4] = {-1, -1, -1, -1};
+      int last_k[4] = {-1, -1, -1, -1}, last_v[4] = {-1, -1, -1, -1};
+      // K_j's slot frees once the S products that read K_{j-stages} have run, V_j's once
+      // the PV products have: K is read a whole tile earlier than V, so it loads earlier.
       for (int j = 0; j < nkv; ++j) {
         const int s = j % C::kStages;
-        if (j >= C::kStages && !mbar_wait(&ctl.kv_empty[s], ((j / C::kStages) - 1) & 1, p.status, abort))
-          break;
+        const uint32_t ph = ((j / C::kStages) - 1) & 1;
+        if (j >= C::kStages && !mbar_wait(&ctl.k_empty[s], ph, p.status, abort)) break;
         mbar_expect_tx(&ctl.k_full[s], C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
           tma_load_3d(smem + C::kKOff + (s * C::kBoxes + b) * kBoxBytes, &tmK, &ctl.k_full[s], b * 64,
                       j * BN, head);
+        last_k[s] = j;
+        if (j >= C::kStages && !mbar_wait(&ctl.v_empty[s], ph, p.status, abort)) break;
         mbar_expect_tx(&ctl.v_full[s], C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
           tma_load_3d(smem + C::kVOff + (s * C::kBoxes + b) * kBoxBytes, &tmV, &ctl.v_full[s], b * 64,
                       j * BN, head);
-        last[s] = j;
+        last_v[s] = j;
       }
       // Every issued copy must land before the CTA may exit.
       mbar_wait(&ctl.q_full, 0, p.status, nullptr);
-      for (int s = 0; s < C::kStages; ++s)
-        if (last[s] >= 0) {
-          mbar_wait(&ctl.k_full[s], (last[s] / C::kStages) & 1, p.status, nullptr);
-          mbar_wait(&ctl.v_full[s], (last[s] / C::kStages) & 1, p.status, nullptr);
-        }
+      for (int s = 0; s < C::kStages; ++s) {
+        if (last_k[s] >= 0) mbar_wait(&ctl.k_full[s], (last_k[s] / C::kStages) & 1, p.status, nullptr);
+        if (last_v[s] >= 0) mbar_wait(&ctl.v_full[s], (last_v[s] / C::kStages) & 1, p.status, nullptr);
+      }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -197,6 +201,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           issue_S(1, 0);
           mma_commit(&ctl.s_full[1]);
         }
+        mma_commit(&ctl.k_empty[0]);
       }
       for (int j = 0; ok && j < nkv; ++j) {
         const int s = j % C::kStages;
@@ -221,7 +226,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             mma_commit(&ctl.o_full[t]);
           }
         }
-        mma_commit(&ctl.kv_empty[s]);
+        if (k_next) mma_commit(&ctl.k_empty[(j + 1) % C::kStages]);  // every S of K_{j+1} issued
+        mma_commit(&ctl.v_empty[s]);
       }
       // All MMAs must retire before TMEM is released.
       mma_commit(&ctl.drain);
