@@ -50,11 +50,16 @@ template <int D>
 struct FwdCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = BM * D * 2;
-  static constexpr int kStages = D == 128 ? 2 : 4;
+  // Ring depths. A third K (or V) stage at d=128 measured slower than two of each: the
+  // loads are limited by L2-to-SM bandwidth, not by how far ahead they are issued.
+  static constexpr int kKStages = D == 128 ? 2 : 4;
+  static constexpr int kVStages = D == 128 ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kSmemBytes = kVOff + kStages * kTileBytes + 1024;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kSmemBytes = kVOff + kVStages * kTileBytes + 1024;
+  static_assert(kKStages <= 4 && kVStages <= 4, "barrier arrays");
+  static_assert(kSmemBytes + 256 <= 227 * 1024, "shared memory per CTA");
   __device__ static constexpr uint32_t colS(int t) { return t ? 128u : 0u; }
   __device__ static constexpr uint32_t colO(int t) { return t ? 256u + D : 256u; }
   static constexpr uint32_t kTmemCols = 512;
@@ -108,7 +113,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl.q_full, 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < 4; ++s) {
       mbar_init(&ctl.k_full[s], 1);
       mbar_init(&ctl.v_full[s], 1);
       mbar_init(&ctl.k_empty[s], 1);
@@ -144,26 +149,27 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       // K_j's slot frees once the S products that read K_{j-stages} have run, V_j's once
       // the PV products have: K is read a whole tile earlier than V, so it loads earlier.
       for (int j = 0; j < nkv; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t ph = ((j / C::kStages) - 1) & 1;
-        if (j >= C::kStages && !mbar_wait(&ctl.k_empty[s], ph, p.status, abort)) break;
-        mbar_expect_tx(&ctl.k_full[s], C::kTileBytes);
+        const int sk = j % C::kKStages, sv = j % C::kVStages;
+        if (j >= C::kKStages && !mbar_wait(&ctl.k_empty[sk], ((j / C::kKStages) - 1) & 1, p.status, abort))
+          break;
+        mbar_expect_tx(&ctl.k_full[sk], C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(smem + C::kKOff + (s * C::kBoxes + b) * kBoxBytes, &tmK, &ctl.k_full[s], b * 64,
+          tma_load_3d(smem + C::kKOff + (sk * C::kBoxes + b) * kBoxBytes, &tmK, &ctl.k_full[sk], b * 64,
                       j * BN, head);
-        last_k[s] = j;
-        if (j >= C::kStages && !mbar_wait(&ctl.v_empty[s], ph, p.status, abort)) break;
-        mbar_expect_tx(&ctl.v_full[s], C::kTileBytes);
+        last_k[sk] = j;
+        if (j >= C::kVStages && !mbar_wait(&ctl.v_empty[sv], ((j / C::kVStages) - 1) & 1, p.status, abort))
+          break;
+        mbar_expect_tx(&ctl.v_full[sv], C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(smem + C::kVOff + (s * C::kBoxes + b) * kBoxBytes, &tmV, &ctl.v_full[s], b * 64,
+          tma_load_3d(smem + C::kVOff + (sv * C::kBoxes + b) * kBoxBytes, &tmV, &ctl.v_full[sv], b * 64,
                       j * BN, head);
-        last_v[s] = j;
+        last_v[sv] = j;
       }
       // Every issued copy must land before the CTA may exit.
       mbar_wait(&ctl.q_full, 0, p.status, nullptr);
-      for (int s = 0; s < C::kStages; ++s) {
-        if (last_k[s] >= 0) mbar_wait(&ctl.k_full[s], (last_k[s] / C::kStages) & 1, p.status, nullptr);
-        if (last_v[s] >= 0) mbar_wait(&ctl.v_full[s], (last_v[s] / C::kStages) & 1, p.status, nullptr);
+      for (int s = 0; s < 4; ++s) {
+        if (last_k[s] >= 0) mbar_wait(&ctl.k_full[s], (last_k[s] / C::kKStages) & 1, p.status, nullptr);
+        if (last_v[s] >= 0) mbar_wait(&ctl.v_full[s], (last_v[s] / C::kVStages) & 1, p.status, nullptr);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -204,8 +210,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         mma_commit(&ctl.k_empty[0]);
       }
       for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % C::kStages;
-        ok = mbar_wait(&ctl.v_full[s], (j / C::kStages) & 1, p.status, abort);
+        const int s = j % C::kVStages;
+        ok = mbar_wait(&ctl.v_full[s], (j / C::kVStages) & 1, p.status, abort);
         bool k_next = false;
         for (int t = 0; ok && t < 2; ++t) {
           const int nk = t ? nkv1 : nkv0;
@@ -215,18 +221,18 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           issue_PV(t, s, j > 0);
           if (j + 1 < nk) {
             if (!k_next) {
-              const int s2 = (j + 1) % C::kStages;
-              if (!(ok = mbar_wait(&ctl.k_full[s2], ((j + 1) / C::kStages) & 1, p.status, abort))) break;
+              const int s2 = (j + 1) % C::kKStages;
+              if (!(ok = mbar_wait(&ctl.k_full[s2], ((j + 1) / C::kKStages) & 1, p.status, abort))) break;
               tc_fence_after();
               k_next = true;
             }
-            issue_S(t, (j + 1) % C::kStages);
+            issue_S(t, (j + 1) % C::kKStages);
             mma_commit(&ctl.s_full[t]);
           } else {
             mma_commit(&ctl.o_full[t]);
           }
         }
-        if (k_next) mma_commit(&ctl.k_empty[(j + 1) % C::kStages]);  // every S of K_{j+1} issued
+        if (k_next) mma_commit(&ctl.k_empty[(j + 1) % C::kKStages]);  // every S of K_{j+1} issued
         mma_commit(&ctl.v_empty[s]);
       }
       // All MMAs must retire before TMEM is released.
