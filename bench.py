@@ -441,6 +441,59 @@ def run_splitkv(args):
     return 0
 
 
+def run_fp8(args):
+    """Forward on e4m3 inputs (fa_fwd_fp8) for a B,H,N,d,causal shape (d = 128).
+
+    Tensor-bound like the bf16 forward and counted with the same FLOP convention; the
+    peak is the measured dense bf16 rate times 2, the nominal fp8/bf16 ratio of the part
+    (4.5 / 2.25 PFLOP/s), taken sustained because the forward runs in a long loop."""
+    import torch
+
+    import exact_attention_02_gb300 as fa
+    from exact_attention_02_gb300.build import build
+    from exact_attention_02_gb300.workloads import make_fp8_inputs
+
+    B, H, N, d, c = (int(v) for v in args.fp8.split(","))
+    build()
+    fa.lib()
+    (q8, k8, v8), desc = make_fp8_inputs(B, H, N, d, seed=0)
+    q, k, v = (torch.from_numpy(x).cuda() for x in (q8, k8, v8))
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+
+    def step():
+        fa.fa_fwd_fp8(q, k, v, desc, bool(c), o=o, lse=lse)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    peaks, src = load_peaks()
+    flop = 4.0 * B * H * N * N * d / (2 if c else 1)
+    tf = flop / (ms * 1e-3) / 1e12
+    peak = 2 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    in_bytes = 3 * B * H * N * d
+    print(json.dumps({
+        "metric": "attention fwd TFLOP/s on e4m3 inputs (fa_fwd_fp8)", "value": tf, "unit": "TFLOP/s",
+        "ms_per_step": ms, "steps": args.steps, "higher_is_better": True, "dtype": "e4m3 (fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": f"fp8_b{B}h{H}_n{N}_d{d}" + ("_causal" if c else ""), "B": B, "H": H, "N": N,
+                   "d": d, "causal": bool(c),
+                   "l2": "no flush: inputs and output exceed the 129 MB L2" if in_bytes * 3 > 129e6 else "fits L2"},
+        "roofline": {"kernel": "fa_fwd_tc_kernel<128, e4m3>", "bound": "tensor", "achieved": tf, "peak": peak,
+                     "unit": "TFLOP/s", "frac": tf / peak,
+                     "peak_source": f"2 x dense bf16 sustained ({src}); nominal fp8/bf16 ratio", "traffic": None},
+        "gpu_launches": args.steps, "kernels_per_step": fa.FP8_KERNELS,
+    }), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -452,6 +505,8 @@ def main():
                     help="ad-hoc bf16 workload B,H,N,d,causal (e.g. for a small profiler capture)")
     ap.add_argument("--splitkv", default=None,
                     help="measure fa_fwd_splitkv instead: B,H,Nq,Nk,d,causal (prints its own JSON line)")
+    ap.add_argument("--fp8", default=None,
+                    help="measure fa_fwd_fp8 instead: B,H,N,d,causal (prints its own JSON line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-count", action="store_true", help="skip the profiler launch count")
@@ -468,6 +523,8 @@ def main():
         return run_reference(args, w)
     if args.splitkv:
         return run_splitkv(args)
+    if args.fp8:
+        return run_fp8(args)
     return run_ours(args, w)
 
 

@@ -28,6 +28,7 @@ BF16_KERNEL_BOUND = {"fa_fwd": "tensor", "fa_bwd": "tensor", "fa_bwd_preprocess"
 BF16_KERNELS = {"fa_fwd": ["fa_fwd_tc_kernel"], "fa_bwd_preprocess": ["preprocess_kernel"],
                 "fa_bwd": ["fa_bwd_tc_kernel", "dq_convert_kernel"]}
 SPLITKV_KERNELS = ["splitkv_partial_kernel", "splitkv_merge_kernel"]
+FP8_KERNELS = ["fa_fwd_tc_kernel"]  # the e4m3 instance of the forward kernel
 FP32_KERNELS = {"fa_fwd": ["simt_fwd_kernel"], "fa_bwd_preprocess": ["preprocess_kernel"],
                 "fa_bwd": ["simt_bwd_dkdv_kernel", "simt_bwd_dq_kernel"]}
 
@@ -61,6 +62,8 @@ def _load():
     L.fa_fwd_splitkv_workspace_size.restype = sz
     L.fa_fwd_splitkv.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, i, vp, sz, vp]
     L.fa_fwd_splitkv.restype = i
+    L.fa_fwd_fp8.argtypes = [vp] * 5 + [i, i, i, i, f, i, f, f, f, vp]
+    L.fa_fwd_fp8.restype = i
     L.fa_get_error_string.argtypes = [i]
     L.fa_get_error_string.restype = ctypes.c_char_p
     L.fa_get_last_device_status.argtypes = []
@@ -190,6 +193,24 @@ def fa_fwd_splitkv(q, k, v, causal: bool, scale: float | None = None, o=None, ls
     _check(_load().fa_fwd_splitkv(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, Nq, Nk, d, scale,
                                   int(bool(causal)), code, _p(workspace), wbytes, _stream_ptr(stream)),
            "fa_fwd_splitkv")
+    return o, lse
+
+
+def fa_fwd_fp8(q8, k8, v8, descale, causal: bool, scale: float | None = None, o=None, lse=None, stream=None):
+    """O (bf16), LSE for e4m3 q8, k8, v8 [B,H,N,d] with dequantisation factors
+    descale = (q, k, v) (see ``fa_fwd_fp8`` in fa.h). The byte tensors may be uint8 or
+    float8_e4m3fn; only their bytes are passed."""
+    import torch
+    B, H, N, d = _shape(q8)
+    for t in (q8, k8, v8):
+        if t.shape != q8.shape or t.element_size() != 1 or not t.is_contiguous() or t.device != q8.device:
+            raise ValueError("q8, k8, v8 must be contiguous one-byte [B, H, N, d] tensors on one device")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    qd, kd, vd = (float(x) for x in descale)
+    _check(_load().fa_fwd_fp8(_p(q8), _p(k8), _p(v8), _p(o), _p(lse), B, H, N, d, scale, int(bool(causal)),
+                              qd, kd, vd, _stream_ptr(stream)), "fa_fwd_fp8")
     return o, lse
 
 

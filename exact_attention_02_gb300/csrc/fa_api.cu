@@ -71,6 +71,24 @@ extern "C" fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void*
   return fa::from_cuda(fa::simt_fwd(Q, K, V, O, LSE, s, scale, causal == 1, false, st));
 }
 
+extern "C" fa_status_t fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                  int B, int H, int N, int d, float scale, int causal, float q_descale,
+                                  float k_descale, float v_descale, void* stream) {
+  const Shape s{B, H, N, d};
+  // The bf16 checks cover sizes, scale and the 32-bit row limit; d is narrower here.
+  fa_status_t r = fa::check_shape(s, FA_DTYPE_BF16, &scale);
+  if (r != FA_OK) return r;
+  for (float f : {q_descale, k_descale, v_descale})
+    if (!(isfinite(f) && f > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((r = fa::check_ptrs({Q, K, V, O, LSE})) != FA_OK) return r;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  int* status = fa::device_status_ptr();
+  if (!status) return FA_ERR_CUDA;
+  return fa::from_cuda(fa::tc_fwd_fp8(Q, K, V, O, LSE, s, scale, causal == 1, q_descale, k_descale, v_descale,
+                                      status, static_cast<cudaStream_t>(stream)));
+}
+
 extern "C" fa_status_t fa_bwd_preprocess(const void* O, const void* dO, float* D, int B, int H,
                                          int N, int d, int dtype, void* stream) {
   const Shape s{B, H, N, d};

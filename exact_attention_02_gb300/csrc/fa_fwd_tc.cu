@@ -23,6 +23,14 @@
 // units); otherwise P uses the stale max (values <= 2^8). The result is exact because
 // O and l always share the same reference max, and O / l cancels it.
 //
+// FP8 (e4m3) instance: Q, K and V arrive as e4m3 bytes with one dequantisation factor per
+// tensor. S = Q K^T and O += P V run as kind::f8f6f4 MMAs (K = 32 per instruction); the
+// factors of Q and K are folded into the exponent multiplier and V's into the epilogue.
+// P is rounded to e4m3 (4 per TMEM column). Its rescale threshold is 4 and it is stored
+// as 16 p, so the stored values stay in (0, 256] and every p >= 2^-10 of the running
+// max lies in e4m3's normal range (relative rounding error <= 2^-4); the factor 16 cancels
+// in O / l and is taken out of the LSE.
+//
 // Causal: tile t sees K tiles 0..qtile_t; the diagonal tile masks key > query.
 // Any N: Q/K/V are read through [heads, N, d] tensor maps, so rows past the end of a head
 // arrive as zeros; keys past the end are masked and rows past the end are not stored.
@@ -42,18 +50,26 @@ constexpr int BN = 128;  // keys per K/V tile
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
-constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kBoxBytes = BM * 128;  // one [128 rows x 64 bf16] swizzled box
+constexpr int kBoxBytes = BM * 128;  // one [128 rows x 128 bytes] swizzled box
 
-template <int D>
+// F8: e4m3 operands (1 byte) instead of bf16 (2 bytes).
+template <int D, bool F8>
 struct FwdCfg {
-  static constexpr int kBoxes = D / 64;
-  static constexpr int kTileBytes = BM * D * 2;
-  // Ring depths. A third K (or V) stage at d=128 measured slower than two of each: the
-  // loads are limited by L2-to-SM bandwidth, not by how far ahead they are issued.
-  static constexpr int kKStages = D == 128 ? 2 : 4;
-  static constexpr int kVStages = D == 128 ? 2 : 4;
+  static constexpr int kRowBytes = D * (F8 ? 1 : 2);
+  static_assert(kRowBytes % 128 == 0, "rows are whole 128-byte swizzle lines");
+  static constexpr int kBoxes = kRowBytes / 128;
+  static constexpr int kBoxElems = F8 ? 128 : 64;  // elements per 128-byte box row
+  static constexpr int kTileBytes = BM * kRowBytes;
+  static constexpr int kKStep = F8 ? 32 : 16;  // K elements per MMA = 32 bytes of a row
+  static constexpr int kSSteps = D / kKStep;   // MMAs per S tile (K = head dim)
+  static constexpr int kPVSteps = BN / kKStep; // MMAs per PV (K = keys)
+  static constexpr float kThreshold = F8 ? 4.f : 8.f;  // lazy-rescale threshold (log2 units)
+  static constexpr float kPShift = F8 ? 4.f : 0.f;     // P is stored as 2^kPShift p
+  // Ring depths. A third K (or V) stage with 256-byte rows measured slower than two of
+  // each: the loads are limited by L2-to-SM bandwidth, not by how far ahead they start.
+  static constexpr int kKStages = kRowBytes == 256 ? 2 : 4;
+  static constexpr int kVStages = kRowBytes == 256 ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
@@ -74,7 +90,8 @@ struct FwdParams {
   int qtiles;
   int pairs;
   int causal;
-  float sl2;  // scale * log2(e)
+  float sl2;      // scale * log2(e) (* the Q and K factors for e4m3)
+  float o_scale;  // V's factor for e4m3, else 1
 };
 
 struct FwdCtl {
@@ -86,11 +103,11 @@ struct FwdCtl {
   int abort;
 };
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -143,7 +160,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_expect_tx(&ctl.q_full, (act1 ? 2 : 1) * C::kTileBytes);
       for (int t = 0; t < (act1 ? 2 : 1); ++t)
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(smem + C::kQOff + (t * C::kBoxes + b) * kBoxBytes, &tmQ, &ctl.q_full, b * 64,
+          tma_load_3d(smem + C::kQOff + (t * C::kBoxes + b) * kBoxBytes, &tmQ, &ctl.q_full, b * C::kBoxElems,
                       (qt0 + t) * BM, head);
       int last_k[4] = {-1, -1, -1, -1}, last_v[4] = {-1, -1, -1, -1};
       // K_j's slot frees once the S products that read K_{j-stages} have run, V_j's once
@@ -154,14 +171,14 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           break;
         mbar_expect_tx(&ctl.k_full[sk], C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(smem + C::kKOff + (sk * C::kBoxes + b) * kBoxBytes, &tmK, &ctl.k_full[sk], b * 64,
+          tma_load_3d(smem + C::kKOff + (sk * C::kBoxes + b) * kBoxBytes, &tmK, &ctl.k_full[sk], b * C::kBoxElems,
                       j * BN, head);
         last_k[sk] = j;
         if (j >= C::kVStages && !mbar_wait(&ctl.v_empty[sv], ((j / C::kVStages) - 1) & 1, p.status, abort))
           break;
         mbar_expect_tx(&ctl.v_full[sv], C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(smem + C::kVOff + (sv * C::kBoxes + b) * kBoxBytes, &tmV, &ctl.v_full[sv], b * 64,
+          tma_load_3d(smem + C::kVOff + (sv * C::kBoxes + b) * kBoxBytes, &tmV, &ctl.v_full[sv], b * C::kBoxElems,
                       j * BN, head);
         last_v[sv] = j;
       }
@@ -174,8 +191,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(BM, BN, false, false);
-      constexpr uint32_t idO = idesc_bf16(BM, D, false, true);
+      constexpr uint32_t idS = F8 ? idesc_e4m3(BM, BN, false, false) : idesc_bf16(BM, BN, false, false);
+      constexpr uint32_t idO = F8 ? idesc_e4m3(BM, D, false, true) : idesc_bf16(BM, D, false, true);
       const uint32_t sQ = smem_u32(smem + C::kQOff);
       const uint32_t sK = smem_u32(smem + C::kKOff);
       const uint32_t sV = smem_u32(smem + C::kVOff);
@@ -186,17 +203,26 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       auto issue_S = [&](int t, int s) {
         const uint32_t qo = t * C::kBoxes * kBoxBytes, ko = s * C::kBoxes * kBoxBytes;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
+        for (int k = 0; k < C::kSSteps; ++k) {  // 32 bytes of each row per step
           const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32;
-          mma_ss(tmem + C::colS(t), sdesc_add(dQ0, qo + off), sdesc_add(dK0, ko + off), idS, k > 0);
+          if constexpr (F8)
+            mma_ss_f8(tmem + C::colS(t), sdesc_add(dQ0, qo + off), sdesc_add(dK0, ko + off), idS, k > 0);
+          else
+            mma_ss(tmem + C::colS(t), sdesc_add(dQ0, qo + off), sdesc_add(dK0, ko + off), idS, k > 0);
         }
       };
       auto issue_PV = [&](int t, int s, bool acc) {
         const uint32_t vo = s * C::kBoxes * kBoxBytes;
+        // K step = kKStep keys: 8 TMEM columns of packed P, kKStep 128-byte rows of V
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          mma_ts(tmem + C::colO(t), tmem + C::colS(t) + k * 8, sdesc_add(dV0, vo + k * 2048), idO,
-                 (acc || k > 0) ? 1u : 0u);
+        for (int k = 0; k < C::kPVSteps; ++k) {
+          if constexpr (F8)
+            mma_ts_f8(tmem + C::colO(t), tmem + C::colS(t) + k * 8, sdesc_add(dV0, vo + k * C::kKStep * 128), idO,
+                      (acc || k > 0) ? 1u : 0u);
+          else
+            mma_ts(tmem + C::colO(t), tmem + C::colS(t) + k * 8, sdesc_add(dV0, vo + k * C::kKStep * 128), idO,
+                   (acc || k > 0) ? 1u : 0u);
+        }
       };
       bool ok = mbar_wait(&ctl.q_full, 0, p.status, abort) && mbar_wait(&ctl.k_full[0], 0, p.status, abort);
       if (ok) {
@@ -283,7 +309,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
       const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       const float m_new = fmaxf(m, mx * sl2);
-      const bool grow = m_new > m + kRescaleThreshold;
+      const bool grow = m_new > m + C::kThreshold;
       if (__any_sync(0xffffffffu, grow)) {
         const float corr = grow ? ex2(m - m_new) : 1.f;
         l *= corr;
@@ -305,22 +331,41 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (grow) m = m_new;
       }
       const float2 sl2v = make_float2(sl2, sl2);
-      const float2 neg_m = make_float2(-m, -m);
+      const float2 neg_m = make_float2(C::kPShift - m, C::kPShift - m);
       float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
+      if constexpr (!F8) {
 #pragma unroll
-      for (int q = 0; q < BN / 32; ++q) {
-        uint32_t pk[16];
+        for (int q = 0; q < BN / 32; ++q) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float2 x = ffma2(make_float2(sv[32 * q + 2 * u], sv[32 * q + 2 * u + 1]), sl2v, neg_m);
-          const float2 pr = make_float2(ex2(x.x), ex2(x.y));
-          if (u & 1)
-            rs1 = fadd2(rs1, pr);
-          else
-            rs0 = fadd2(rs0, pr);
-          pk[u] = pack_bf16(pr.x, pr.y);
+          for (int u = 0; u < 16; ++u) {
+            const float2 x = ffma2(make_float2(sv[32 * q + 2 * u], sv[32 * q + 2 * u + 1]), sl2v, neg_m);
+            const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+            if (u & 1)
+              rs1 = fadd2(rs1, pr);
+            else
+              rs0 = fadd2(rs0, pr);
+            pk[u] = pack_bf16(pr.x, pr.y);
+          }
+          tmem_st16(tS + 16 * q, pk);
         }
-        tmem_st16(tS + 16 * q, pk);
+      } else {
+#pragma unroll
+        for (int q = 0; q < BN / 64; ++q) {
+          uint32_t pk[16];  // 64 keys, four e4m3 per column
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const float* v4 = &sv[64 * q + 4 * u];
+            const float2 x0 = ffma2(make_float2(v4[0], v4[1]), sl2v, neg_m);
+            const float2 x1 = ffma2(make_float2(v4[2], v4[3]), sl2v, neg_m);
+            const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+            const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+            rs0 = fadd2(rs0, p0);
+            rs1 = fadd2(rs1, p1);
+            pk[u] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
+          }
+          tmem_st16(tS + 16 * q, pk);
+        }
       }
       l += (rs0.x + rs0.y) + (rs1.x + rs1.y);
       tmem_wait_st();
@@ -330,7 +375,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.o_full[t], 0, p.status, abort));
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = p.o_scale / l;
       __nv_bfloat16* orow = p.O + (size_t)(row_base + qrow) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -346,7 +391,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           for (int u = 0; u < 4; ++u) dst[u] = w[u];
         }
       }
-      if (qrow < p.N) p.LSE[row_base + qrow] = (m + log2f(l)) * kLn2;
+      if (qrow < p.N) p.LSE[row_base + qrow] = (m - C::kPShift + log2f(l)) * kLn2;
     }
   }
 
@@ -358,17 +403,22 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   }
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
-                   float scale, bool causal, int* status, cudaStream_t st) {
-  using C = FwdCfg<D>;
+                   float sl2, float o_scale, bool causal, int* status, cudaStream_t st) {
+  using C = FwdCfg<D, F8>;
   CUtensorMap mq, mk, mv;
   const int64_t heads = s.heads();
-  if (!make_map_bf16_3d(&mq, Q, heads, s.N, D, BM) || !make_map_bf16_3d(&mk, K, heads, s.N, D, BN) ||
-      !make_map_bf16_3d(&mv, V, heads, s.N, D, BN))
-    return cudaErrorInvalidValue;
+  bool maps;
+  if constexpr (F8)
+    maps = make_map_u8_3d(&mq, Q, heads, s.N, D, BM) && make_map_u8_3d(&mk, K, heads, s.N, D, BN) &&
+           make_map_u8_3d(&mv, V, heads, s.N, D, BN);
+  else
+    maps = make_map_bf16_3d(&mq, Q, heads, s.N, D, BM) && make_map_bf16_3d(&mk, K, heads, s.N, D, BN) &&
+           make_map_bf16_3d(&mv, V, heads, s.N, D, BN);
+  if (!maps) return cudaErrorInvalidValue;
   static bool attr = [] {
-    return cudaFuncSetAttribute(fa_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(fa_fwd_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes) == cudaSuccess;
   }();
   if (!attr) return cudaErrorInvalidConfiguration;
@@ -381,18 +431,28 @@ cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.qtiles = (s.N + BM - 1) / BM;
   p.pairs = (p.qtiles + 1) / 2;
   p.causal = causal ? 1 : 0;
-  p.sl2 = scale * 1.4426950408889634f;
+  p.sl2 = sl2;
+  p.o_scale = o_scale;
   const int64_t grid = (int64_t)p.pairs * p.heads;
-  fa_fwd_tc_kernel<D><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p);
+  fa_fwd_tc_kernel<D, F8><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
+
+constexpr float kLog2e = 1.4426950408889634f;
 
 }  // namespace
 
 cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st) {
-  return s.d == 64 ? launch<64>(Q, K, V, O, LSE, s, scale, causal, status, st)
-                   : launch<128>(Q, K, V, O, LSE, s, scale, causal, status, st);
+  return s.d == 64 ? launch<64, false>(Q, K, V, O, LSE, s, scale * kLog2e, 1.f, causal, status, st)
+                   : launch<128, false>(Q, K, V, O, LSE, s, scale * kLog2e, 1.f, causal, status, st);
+}
+
+cudaError_t tc_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                       float scale, bool causal, float q_descale, float k_descale, float v_descale,
+                       int* status, cudaStream_t st) {
+  return launch<128, true>(Q, K, V, O, LSE, s, scale * kLog2e * q_descale * k_descale, v_descale, causal,
+                           status, st);
 }
 
 }  // namespace fa

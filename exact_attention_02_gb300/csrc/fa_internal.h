@@ -31,6 +31,10 @@ cudaError_t simt_bwd(const void* Q, const void* K, const void* V, const void* dO
 // ---- tcgen05 tensor-core path (bf16, d in {64, 128}, N % 128 == 0) ----
 cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st);
+// e4m3 Q, K, V (d = 128) with per-tensor dequantisation factors; O bf16, LSE fp32.
+cudaError_t tc_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                       float scale, bool causal, float q_descale, float k_descale, float v_descale,
+                       int* status, cudaStream_t st);
 // dQacc: fp32 [B*H*N, d] workspace; zeroed, accumulated and converted inside the call.
 cudaError_t tc_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                    const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,

@@ -52,4 +52,19 @@ inline bool make_map_bf16_3d(CUtensorMap* map, const void* base, int64_t heads, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [heads x N x cols] bytes (8-bit elements, e.g. e4m3), loaded as boxes of 128 columns x
+// box_rows rows of one head with the 128-byte swizzle; rows past N read as zeros.
+inline bool make_map_u8_3d(CUtensorMap* map, const void* base, int64_t heads, int64_t N, int64_t cols,
+                           int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)N, (cuuint64_t)heads};
+  cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)N * cols};
+  cuuint32_t box[3] = {128, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace fa

@@ -70,6 +70,34 @@ WORKLOADS: dict[str, Workload] = {
 HEADLINE = "b2h16_n8192_d128_bf16_causal"
 
 
+def quantize_e4m3(x: np.ndarray) -> tuple[np.ndarray, float]:
+    """Encode float32 values as e4m3 bytes with one factor for the whole array.
+
+    The factor is amax / 448, so the largest magnitude maps to e4m3's largest finite
+    value; each x / factor is rounded to the nearest e4m3 value (ties to even) by
+    PyTorch's float8_e4m3fn conversion. Returns (uint8 bytes, factor): the value of byte
+    b is factor * e4m3(b). This only encodes inputs; both the CUDA path and the oracle
+    read the same bytes.
+    """
+    import torch
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    amax = float(np.abs(x).max()) if x.size else 0.0
+    factor = amax / 448.0 if amax > 0 else 1.0
+    t = torch.from_numpy(x / np.float32(factor)).clamp_(-448.0, 448.0)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy(), factor
+
+
+def make_fp8_inputs(B: int, H: int, N: int, d: int, seed: int, qk_gain: float = 1.0):
+    """Q, K, V drawn as in the recipe above (N(0, 1) float32, Q and K times qk_gain),
+    then each encoded by ``quantize_e4m3``: returns ((q8, k8, v8), (q, k, v factors))."""
+    rng = np.random.default_rng(seed)
+    xs = [rng.standard_normal((B, H, N, d), dtype=np.float32) for _ in range(3)]
+    xs[0] *= np.float32(qk_gain)
+    xs[1] *= np.float32(qk_gain)
+    enc = [quantize_e4m3(x) for x in xs]
+    return tuple(e[0] for e in enc), tuple(e[1] for e in enc)
+
+
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bfloat16 (ties to even); returns float32."""
     x = np.ascontiguousarray(x, dtype=np.float32)

@@ -30,7 +30,7 @@ def _declared():
 def test_header_declares_the_boundary():
     assert set(_declared()) >= {"fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_bwd_workspace_size",
                                 "fa_get_error_string", "fa_get_last_device_status", "fa_fwd_splitkv",
-                                "fa_fwd_splitkv_workspace_size"}
+                                "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8"}
 
 
 def test_exports_every_declared_symbol(lib):
@@ -135,3 +135,23 @@ def test_splitkv_workspace_and_rejects(lib):
     assert _splitkv(lib, scale=-1.0) == 1
     assert _splitkv(lib, ws=0) == 5
     assert _splitkv(lib, wsb=16) == 5
+
+
+def test_fp8_rejects_before_launch(lib):
+    """Host-side checks of fa_fwd_fp8 (dummy pointers; nothing is launched)."""
+    import exact_attention_02_gb300 as fa
+    vp, f = ctypes.c_void_p, ctypes.c_float
+    L = fa.lib()
+
+    def call(B=1, H=1, N=128, d=128, scale=0.088, causal=0, qd=1.0, kd=1.0, vd=1.0, ptr=P):
+        return L.fa_fwd_fp8(vp(ptr), vp(P), vp(P), vp(P), vp(P), B, H, N, d, f(scale), causal, f(qd), f(kd), f(vd),
+                            None)
+    assert call(d=64) == fa.FA_ERR_UNSUPPORTED        # e4m3 path is d = 128 only
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(qd=0.0) == fa.FA_ERR_INVALID_ARG
+    assert call(vd=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert call(kd=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert call(scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert call(causal=2) == fa.FA_ERR_INVALID_ARG
+    assert call(N=0) == fa.FA_ERR_INVALID_ARG
+    assert call(ptr=P + 8) == fa.FA_ERR_INVALID_ARG    # misaligned
