@@ -21,6 +21,11 @@ Readings where the pages leave a choice open:
   * The saved statistic is LSE_i = m_i + ln(l_i) (natural log, scaled scores),
     which packs the pages' two ledger rows (m, l) into one.
   * D_i uses the oracle's own float64 O.
+  * An additive mask M (optional; [N_q, N_k] per head, finite or -inf) is added to the
+    scaled scores, s_ij = scale * q_i . k_j + M_ij, before the causal rule applies; it is
+    the "mask" that "知识点13" section 7 (算子融合优化) fuses into the softmax step. A row
+    whose every key is hidden (all -inf) has no softmax: its weights are taken as 0, so
+    O_i = 0, LSE_i = -inf and the row contributes nothing to any gradient.
   * Causal attention hides key j from query i iff j > i (queries and keys share
     the same positions; the diagonal is always visible, so no row is empty). With
     fewer queries than keys (N_q < N_k, e.g. decoding against a cache) the queries are
@@ -50,13 +55,16 @@ def _group_rows(N: int) -> int:
     return max(1, min(N, _GROUP_ELEMS // max(N, 1)))
 
 
-def scores(q, k, scale, causal, rows):
-    """s_ij = scale * q_i . k_j for the query rows ``rows``; hidden keys get -inf.
+def scores(q, k, scale, causal, rows, mask=None):
+    """s_ij = scale * q_i . k_j (+ M_ij) for the query rows ``rows``; hidden keys get -inf.
 
-    [BWD] 显存困境 (S_ij = Q_i.K_j / sqrt(d)); [KP13] 代码手撕 (mask j > i).
+    [BWD] 显存困境 (S_ij = Q_i.K_j / sqrt(d)); [KP13] 代码手撕 (mask j > i) and section 7
+    (the mask fused into the softmax step).
     """
     rows = np.asarray(rows)
     s = scale * (q[rows] @ k.T)
+    if mask is not None:
+        s = s + np.asarray(mask, np.float64)[rows]
     if causal:
         offset = k.shape[0] - q.shape[0]  # query row i sits at key position i + offset
         j = np.arange(k.shape[0])
@@ -68,19 +76,24 @@ def softmax_rows(s):
     """Row softmax with the row maximum subtracted first: returns (P, m, l).
 
     [BWD] 前向台账: m_i = max_j s_ij, l_i = sum_j exp(s_ij - m_i),
-    P_ij = exp(s_ij - m_i) / l_i; hidden keys (s = -inf) get P = 0.
+    P_ij = exp(s_ij - m_i) / l_i; hidden keys (s = -inf) get P = 0. A row with every key
+    hidden has m = -inf, l = 0 and P = 0.
     """
     m = s.max(axis=1)
-    e = np.exp(s - m[:, None])
+    m_ref = np.where(np.isfinite(m), m, 0.0)
+    e = np.exp(s - m_ref[:, None])
     l = e.sum(axis=1)
-    return e / l[:, None], m, l
+    with np.errstate(invalid="ignore", divide="ignore"):
+        P = np.where(l[:, None] > 0, e / l[:, None], 0.0)
+    return P, m, l
 
 
-def head_forward(q, k, v, scale, causal, rows=None):
+def head_forward(q, k, v, scale, causal, rows=None, mask=None):
     """O and LSE of one head for query ``rows`` (default: all rows).
 
-    q, k, v: [N, d] float64. Returns O [len(rows), d] and LSE [len(rows)], where
-    O_i = sum_j P_ij v_j ([FA2] section 1) and LSE_i = m_i + ln l_i.
+    q, k, v: [N, d] float64; mask: optional [N_q, N_k] additive mask. Returns O
+    [len(rows), d] and LSE [len(rows)], where O_i = sum_j P_ij v_j ([FA2] section 1) and
+    LSE_i = m_i + ln l_i (-inf for a row with no visible key).
     """
     q, k, v = (np.asarray(a, dtype=np.float64) for a in (q, k, v))
     N = q.shape[0]
@@ -90,9 +103,10 @@ def head_forward(q, k, v, scale, causal, rows=None):
     g = _group_rows(k.shape[0])
     for a in range(0, rows.size, g):
         r = rows[a:a + g]
-        P, m, l = softmax_rows(scores(q, k, scale, causal, r))
+        P, m, l = softmax_rows(scores(q, k, scale, causal, r, mask))
         O[a:a + g] = P @ v
-        LSE[a:a + g] = m + np.log(l)
+        with np.errstate(divide="ignore"):
+            LSE[a:a + g] = m + np.log(l)
     return O, LSE
 
 
@@ -101,7 +115,7 @@ def row_dot(do, o):
     return np.einsum("ic,ic->i", np.asarray(do, np.float64), np.asarray(o, np.float64))
 
 
-def head_backward(q, k, v, do, scale, causal, return_ds=False):
+def head_backward(q, k, v, do, scale, causal, return_ds=False, mask=None):
     """All outputs of one head: O, LSE, D, dQ, dK, dV (and dS when asked, small N only).
 
     [BWD] 反向总览 / Softmax梯度 / QKV梯度:
@@ -110,7 +124,7 @@ def head_backward(q, k, v, do, scale, causal, return_ds=False):
     """
     q, k, v, do = (np.asarray(a, dtype=np.float64) for a in (q, k, v, do))
     N, d = q.shape
-    O, LSE = head_forward(q, k, v, scale, causal)
+    O, LSE = head_forward(q, k, v, scale, causal, mask=mask)
     D = row_dot(do, O)
     dQ = np.empty_like(q)
     dK = np.zeros_like(k)
@@ -119,7 +133,7 @@ def head_backward(q, k, v, do, scale, causal, return_ds=False):
     g = _group_rows(N)
     for a in range(0, N, g):
         r = np.arange(a, min(N, a + g))
-        P, _, _ = softmax_rows(scores(q, k, scale, causal, r))
+        P, _, _ = softmax_rows(scores(q, k, scale, causal, r, mask))
         dV += P.T @ do[r]
         dP = do[r] @ v.T
         dS = P * (dP - D[r, None])
@@ -133,19 +147,29 @@ def head_backward(q, k, v, do, scale, causal, return_ds=False):
     return out
 
 
-def forward(q, k, v, scale, causal):
-    """Whole-tensor forward over [B, H, N, d] inputs: O [B,H,N,d], LSE [B,H,N]."""
+def _head_mask(mask, b, h):
+    """The [N_q, N_k] slice of a mask broadcastable to [B, H, N_q, N_k] (None stays None)."""
+    if mask is None:
+        return None
+    mask = np.asarray(mask)
+    return mask[b if mask.shape[0] > 1 else 0, h if mask.shape[1] > 1 else 0]
+
+
+def forward(q, k, v, scale, causal, mask=None):
+    """Whole-tensor forward over [B, H, N, d] inputs: O [B,H,N,d], LSE [B,H,N].
+    mask: optional additive mask of shape [B or 1, H or 1, N, N]."""
     B, H, N, d = q.shape
     O = np.empty((B, H, N, v.shape[-1]))
     LSE = np.empty((B, H, N))
     for b in range(B):
         for h in range(H):
-            O[b, h], LSE[b, h] = head_forward(q[b, h], k[b, h], v[b, h], scale, causal)
+            O[b, h], LSE[b, h] = head_forward(q[b, h], k[b, h], v[b, h], scale, causal,
+                                              mask=_head_mask(mask, b, h))
     return O, LSE
 
 
-def backward(q, k, v, do, scale, causal):
-    """Whole-tensor forward + backward over [B, H, N, d] inputs.
+def backward(q, k, v, do, scale, causal, mask=None):
+    """Whole-tensor forward + backward over [B, H, N, d] inputs (mask as in ``forward``).
 
     Returns a dict of float64 arrays: o, lse, d, dq, dk, dv.
     """
@@ -153,7 +177,7 @@ def backward(q, k, v, do, scale, causal):
     res = None
     for b in range(B):
         for h in range(H):
-            r = head_backward(q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
+            r = head_backward(q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, mask=_head_mask(mask, b, h))
             if res is None:
                 res = {n: np.empty((B, H) + a.shape) for n, a in r.items()}
             for n, a in r.items():

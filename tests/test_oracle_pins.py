@@ -346,6 +346,129 @@ def pin_fewer_queries_than_keys(m):
     assert np.allclose(O[0], (p0 / p0.sum()) @ v[:vis], rtol=0, atol=1e-14)
 
 
+# -- the additive mask ("知识点13" section 7: the mask fused into the softmax step) ---------
+def _mask(N, seed, p_hide=0.2):
+    """A random finite mask with about p_hide of its entries -inf; the diagonal stays
+    finite, so no row is wholly hidden, causal or not."""
+    rng = np.random.default_rng(seed)
+    M = rng.standard_normal((N, N)) * 1.5
+    hide = rng.random((N, N)) < p_hide
+    hide[np.arange(N), np.arange(N)] = False
+    return np.where(hide, -np.inf, M)
+
+
+def pin_mask_zero_and_triangle(m):
+    """A zero mask changes nothing; an upper-triangular -inf mask is the causal rule."""
+    N, d = 10, 4
+    q, k, v, do = (_rand((N, d), 700 + s) for s in range(4))
+    ref = m.head_backward(q, k, v, do, 0.5, False)
+    zero = m.head_backward(q, k, v, do, 0.5, False, mask=np.zeros((N, N)))
+    tri = np.where(np.triu(np.ones((N, N), bool), 1), -np.inf, 0.0)
+    caus = m.head_backward(q, k, v, do, 0.5, True)
+    by_mask = m.head_backward(q, k, v, do, 0.5, False, mask=tri)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        assert np.allclose(ref[n], zero[n], rtol=0, atol=1e-14), n
+        assert np.allclose(caus[n], by_mask[n], rtol=0, atol=1e-14), n
+
+
+def pin_mask_brute_force(m):
+    """O_i = sum_j w_ij e^{s_ij} v_j / sum_j w_ij e^{s_ij} with M_ij = ln w_ij, by loops."""
+    N, d, scale = 5, 3, 0.6
+    q, k, v = (_rand((N, d), 710 + s) for s in range(3))
+    w = np.random.default_rng(713).random((N, N)) + 0.05
+    w[1, 3] = w[4, 0] = 0.0  # -inf entries
+    with np.errstate(divide="ignore"):
+        M = np.log(w)
+    O, L = m.head_forward(q, k, v, scale, False, mask=M)
+    for i in range(N):
+        num = [0.0] * d
+        den = 0.0
+        for j in range(N):
+            e = w[i, j] * math.exp(scale * sum(q[i, c] * k[j, c] for c in range(d)))
+            den += e
+            for c in range(d):
+                num[c] += e * v[j, c]
+        for c in range(d):
+            assert abs(O[i, c] - num[c] / den) < 1e-12, (i, c)
+        assert abs(L[i] - math.log(den)) < 1e-12
+
+
+def pin_mask_row_shift(m):
+    """Adding c_i to every entry of row i leaves O and the gradients unchanged and moves
+    LSE_i by c_i (softmax shift invariance)."""
+    N, d = 9, 4
+    q, k, v, do = (_rand((N, d), 720 + s) for s in range(4))
+    M = _mask(N, 724)
+    c = np.linspace(-3, 5, N)
+    a = m.head_backward(q, k, v, do, 0.4, True, mask=M)
+    b = m.head_backward(q, k, v, do, 0.4, True, mask=M + c[:, None])
+    for n in ("o", "dq", "dk", "dv"):
+        assert np.allclose(a[n], b[n], rtol=0, atol=1e-12), n
+    assert np.allclose(b["lse"] - a["lse"], c, rtol=0, atol=1e-12)
+
+
+def pin_mask_finite_differences(m):
+    """Central differences of <O, dO> with a random finite mask with -inf entries."""
+    h = 1e-5
+    for N, d, causal, seed in ((6, 3, False, 730), (9, 4, True, 731)):
+        q, k, v, do = (_rand((N, d), seed + s) for s in range(4))
+        M = _mask(N, seed + 9)
+        r = m.head_backward(q, k, v, do, 0.5, causal, mask=M)
+
+        def loss(qq, kk, vv):
+            return float((m.head_forward(qq, kk, vv, 0.5, causal, mask=M)[0] * do).sum())
+        for pos, name in enumerate(("dq", "dk", "dv")):
+            x = [q, k, v][pos]
+            g = np.empty_like(x)
+            for idx in np.ndindex(*x.shape):
+                args_p, args_m = [q, k, v], [q, k, v]
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p[pos], args_m[pos] = xp, xm
+                g[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            err = np.abs(g - r[name]).max() / max(1e-300, np.abs(g).max())
+            assert err < 1e-7, (name, N, causal, err)
+
+
+def pin_mask_torch_sdpa(m):
+    """PyTorch's CPU float64 scaled_dot_product_attention with an additive float mask."""
+    torch = pytest.importorskip("torch")
+    B, H, N, d = 2, 2, 13, 5
+    arrs = [_rand((B, H, N, d), 740 + s) for s in range(4)]
+    M = np.stack([np.stack([_mask(N, 750 + 2 * b + h) for h in range(H)]) for b in range(B)])
+    t = [torch.tensor(a, dtype=torch.float64, requires_grad=(i < 3)) for i, a in enumerate(arrs)]
+    o = torch.nn.functional.scaled_dot_product_attention(t[0], t[1], t[2], attn_mask=torch.tensor(M), scale=0.3)
+    (o * t[3]).sum().backward()
+    r = m.backward(*arrs, 0.3, False, mask=M)
+    assert np.allclose(r["o"], o.detach().numpy(), rtol=0, atol=1e-12)
+    for name, ten in zip(("dq", "dk", "dv"), t[:3]):
+        assert np.allclose(r[name], ten.grad.numpy(), rtol=0, atol=1e-12), name
+    # a mask broadcast over batch and heads
+    M1 = M[:1, :1]
+    o1 = torch.nn.functional.scaled_dot_product_attention(t[0].detach(), t[1].detach(), t[2].detach(),
+                                                          attn_mask=torch.tensor(M1), scale=0.3)
+    assert np.allclose(m.forward(*arrs[:3], 0.3, False, mask=M1)[0], o1.numpy(), rtol=0, atol=1e-12)
+
+
+def pin_mask_hidden_row(m):
+    """A row with every key hidden: O = 0, LSE = -inf, no gradient through it, and the
+    other rows as without that row's queries."""
+    N, d = 7, 3
+    q, k, v, do = (_rand((N, d), 760 + s) for s in range(4))
+    M = _mask(N, 765)
+    M[3] = -np.inf
+    r = m.head_backward(q, k, v, do, 0.5, False, mask=M)
+    assert np.all(r["o"][3] == 0) and r["lse"][3] == -np.inf and np.all(r["dq"][3] == 0)
+    for n in ("o", "dq", "dk", "dv", "lse"):
+        assert not np.isnan(r[n]).any(), n
+    keep = np.array([i for i in range(N) if i != 3])
+    rk = m.head_backward(q[keep], k, v, do[keep], 0.5, False, mask=M[keep])
+    assert np.allclose(r["o"][keep], rk["o"], rtol=0, atol=1e-13)
+    assert np.allclose(r["dk"], rk["dk"], rtol=0, atol=1e-13)
+    assert np.allclose(r["dv"], rk["dv"], rtol=0, atol=1e-13)
+
+
 PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]
 
 
@@ -383,7 +506,12 @@ MUTATIONS = [
     ("D from dO.dO", 'np.einsum("ic,ic->i", np.asarray(do, np.float64), np.asarray(o, np.float64))',
      'np.einsum("ic,ic->i", np.asarray(do, np.float64), np.asarray(do, np.float64))'),
     ("scale missing on scores", "s = scale * (q[rows] @ k.T)", "s = q[rows] @ k.T"),
-    ("no normalisation", "return e / l[:, None], m, l", "return e, m, l"),
+    ("no normalisation", "P = np.where(l[:, None] > 0, e / l[:, None], 0.0)", "P = np.where(l[:, None] > 0, e, 0.0)"),
+    ("mask subtracted", "s = s + np.asarray(mask, np.float64)[rows]", "s = s - np.asarray(mask, np.float64)[rows]"),
+    ("mask transposed", "s = s + np.asarray(mask, np.float64)[rows]", "s = s + np.asarray(mask, np.float64).T[rows]"),
+    ("mask scaled", "s = s + np.asarray(mask, np.float64)[rows]", "s = s + scale * np.asarray(mask, np.float64)[rows]"),
+    ("mask ignored", "s = s + np.asarray(mask, np.float64)[rows]", "s = s + 0.0"),
+    ("no guard for a wholly hidden row", "P = np.where(l[:, None] > 0, e / l[:, None], 0.0)", "P = e / l[:, None]"),
 ]
 
 
