@@ -62,6 +62,11 @@ def _load():
     L.fa_fwd_splitkv_workspace_size.restype = sz
     L.fa_fwd_splitkv.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, i, vp, sz, vp]
     L.fa_fwd_splitkv.restype = i
+    ll = ctypes.c_longlong
+    L.fa_fwd_masked.argtypes = [vp] * 6 + [ll, ll, ll, i, i, i, i, f, i, i, vp]
+    L.fa_fwd_masked.restype = i
+    L.fa_bwd_masked.argtypes = [vp] * 11 + [ll, ll, ll, vp, sz, i, i, i, i, f, i, i, vp]
+    L.fa_bwd_masked.restype = i
     L.fa_fwd_fp8.argtypes = [vp] * 5 + [i, i, i, i, f, i, f, f, f, vp]
     L.fa_fwd_fp8.restype = i
     L.fa_get_error_string.argtypes = [i]
@@ -121,14 +126,49 @@ def _same(ref, *ts):
             raise ValueError("tensors must be contiguous")
 
 
-def fa_fwd(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None, stream=None):
-    """O, LSE = attention forward of [B, H, N, d] CUDA tensors (see ``fa_fwd`` in fa.h)."""
+def padded_mask(mask):
+    """A copy of a [B|1, H|1, N, N] bf16 mask whose rows are padded to a multiple of 8
+    elements (the layout ``fa_fwd_masked`` reads); returns a view of the first N columns."""
+    import torch
+    n = int(mask.shape[-1])
+    cols = (n + 7) // 8 * 8
+    out = torch.zeros(tuple(mask.shape[:-1]) + (cols,), dtype=torch.bfloat16, device=mask.device)
+    out[..., :n] = mask
+    return out[..., :n]
+
+
+def _mask_args(mask, q):
+    """Pointer and element strides (batch, head, row) of an additive mask for q's shape."""
+    import torch
+    B, H, N, _ = _shape(q)
+    if mask.dim() != 4 or mask.dtype != torch.bfloat16 or mask.device != q.device:
+        raise ValueError("mask must be a bf16 [B or 1, H or 1, N, N] tensor on q's device")
+    mb, mh, mn, mc = (int(x) for x in mask.shape)
+    if mb not in (1, B) or mh not in (1, H) or mn != N or mc != N or mask.stride(3) != 1:
+        raise ValueError("mask must be [B or 1, H or 1, N, N] with contiguous rows")
+    srow = int(mask.stride(2))
+    sb = 0 if mb == 1 else int(mask.stride(0))
+    sh = 0 if mh == 1 else int(mask.stride(1))
+    if srow % 8 or sb % 8 or sh % 8 or srow < (N + 7) // 8 * 8:
+        raise ValueError("mask rows must start 16-byte aligned: use padded_mask(mask)")
+    return _p(mask), sb, sh, srow
+
+
+def fa_fwd(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None, stream=None, mask=None):
+    """O, LSE = attention forward of [B, H, N, d] CUDA tensors (see ``fa_fwd`` in fa.h).
+    With ``mask`` (bf16 [B|1, H|1, N, N], added to the scaled scores) it calls
+    ``fa_fwd_masked``."""
     import torch
     B, H, N, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _same(q, k, v, o)
+    if mask is not None:
+        mp, sb, sh, srow = _mask_args(mask, q)
+        _check(_load().fa_fwd_masked(_p(q), _p(k), _p(v), _p(o), _p(lse), mp, sb, sh, srow, B, H, N, d, scale,
+                                     int(bool(causal)), _dtype_code(q), _stream_ptr(stream)), "fa_fwd_masked")
+        return o, lse
     _check(_load().fa_fwd(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d, scale, int(bool(causal)),
                           _dtype_code(q), _stream_ptr(stream)), "fa_fwd")
     return o, lse
@@ -152,8 +192,9 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int, dtype) -> int:
 
 
 def fa_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None, D=None,
-           dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """dQ, dK, dV of attention from the forward's O and LSE (see ``fa_bwd`` in fa.h)."""
+           dq=None, dk=None, dv=None, workspace=None, stream=None, mask=None):
+    """dQ, dK, dV of attention from the forward's O and LSE (see ``fa_bwd`` in fa.h);
+    with ``mask`` (the forward's additive mask) it calls ``fa_bwd_masked``."""
     import torch
     B, H, N, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -165,6 +206,12 @@ def fa_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None, D=None
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if mask is not None:
+        mp, sb, sh, srow = _mask_args(mask, q)
+        _check(_load().fa_bwd_masked(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(D), _p(dq), _p(dk), _p(dv),
+                                     mp, sb, sh, srow, _p(workspace), wbytes, B, H, N, d, scale, int(bool(causal)),
+                                     _dtype_code(q), _stream_ptr(stream)), "fa_bwd_masked")
+        return dq, dk, dv
     _check(_load().fa_bwd(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(D), _p(dq), _p(dk), _p(dv),
                           _p(workspace), wbytes, B, H, N, d, scale, int(bool(causal)), _dtype_code(q),
                           _stream_ptr(stream)), "fa_bwd")

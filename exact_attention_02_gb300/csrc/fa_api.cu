@@ -105,37 +105,98 @@ extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d, int dtype) {
   return dtype == FA_DTYPE_BF16 ? (size_t)s.elems() * sizeof(float) : 0;
 }
 
-extern "C" fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O,
-                              const void* dO, const float* LSE, const float* D, void* dQ,
-                              void* dK, void* dV, void* workspace, size_t workspace_bytes, int B,
-                              int H, int N, int d, float scale, int causal, int dtype,
-                              void* stream) {
+namespace fa {
+namespace {
+
+struct Mask {
+  const void* ptr;
+  int64_t sb, sh, srow;
+};
+
+// The mask's rows are read in 16-byte pieces: the base must be 16-byte aligned, every
+// stride a non-negative multiple of 8 elements, and each row must hold N rounded up to 8.
+fa_status_t check_mask(const Mask& m, const Shape& s, int dtype) {
+  if (!m.ptr || !aligned16(m.ptr)) return FA_ERR_INVALID_ARG;
+  if (m.sb < 0 || m.sh < 0 || m.sb % 8 || m.sh % 8 || m.srow % 8) return FA_ERR_INVALID_ARG;
+  if (m.srow < ((int64_t)s.N + 7) / 8 * 8) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status_t bwd_common(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                       const float* LSE, const float* D, void* dQ, void* dK, void* dV, void* workspace,
+                       size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal, int dtype,
+                       const Mask* mask, void* stream) {
   const Shape s{B, H, N, d};
-  fa_status_t r = fa::check_shape(s, dtype, &scale);
+  fa_status_t r = check_shape(s, dtype, &scale);
   if (r != FA_OK) return r;
-  if ((r = fa::check_ptrs({Q, K, V, O, dO, LSE, dQ, dK, dV})) != FA_OK) return r;
-  if (D && !fa::aligned16(D)) return FA_ERR_INVALID_ARG;
+  if ((r = check_ptrs({Q, K, V, O, dO, LSE, dQ, dK, dV})) != FA_OK) return r;
+  if (D && !aligned16(D)) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (mask && (r = check_mask(*mask, s, dtype)) != FA_OK) return r;
   const size_t need = fa_bwd_workspace_size(B, H, N, d, dtype);
   const size_t need_d = D ? 0 : (size_t)s.rows() * sizeof(float);
   if (need + need_d > 0) {
     if (!workspace || workspace_bytes < need + need_d) return FA_ERR_WORKSPACE;
-    if (!fa::aligned16(workspace)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return FA_ERR_INVALID_ARG;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf16 = dtype == FA_DTYPE_BF16;
   if (!D) {
     float* Dw = reinterpret_cast<float*>(static_cast<char*>(workspace) + need);
-    if ((r = fa::from_cuda(fa::preprocess_d(O, dO, Dw, s, bf16, st))) != FA_OK) return r;
+    if ((r = from_cuda(preprocess_d(O, dO, Dw, s, bf16, st))) != FA_OK) return r;
     D = Dw;
   }
   if (bf16) {
-    int* status = fa::device_status_ptr();
+    int* status = device_status_ptr();
     if (!status) return FA_ERR_CUDA;
-    return fa::from_cuda(fa::tc_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, static_cast<float*>(workspace), s,
-                                    scale, causal == 1, status, st));
+    float* acc = static_cast<float*>(workspace);
+    if (mask)
+      return from_cuda(tc_bwd_masked(Q, K, V, dO, LSE, D, dQ, dK, dV, acc, s, scale, causal == 1, mask->ptr,
+                                     mask->sb, mask->sh, mask->srow, status, st));
+    return from_cuda(tc_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, acc, s, scale, causal == 1, status, st));
   }
-  return fa::from_cuda(fa::simt_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal == 1, false, st));
+  return from_cuda(simt_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal == 1, false, st));
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const void* O,
+                              const void* dO, const float* LSE, const float* D, void* dQ,
+                              void* dK, void* dV, void* workspace, size_t workspace_bytes, int B,
+                              int H, int N, int d, float scale, int causal, int dtype,
+                              void* stream) {
+  return fa::bwd_common(Q, K, V, O, dO, LSE, D, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, scale, causal,
+                        dtype, nullptr, stream);
+}
+
+extern "C" fa_status_t fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                     const void* mask, long long mask_stride_b, long long mask_stride_h,
+                                     long long mask_stride_row, int B, int H, int N, int d, float scale,
+                                     int causal, int dtype, void* stream) {
+  const Shape s{B, H, N, d};
+  fa_status_t r = fa::check_shape(s, dtype, &scale);
+  if (r != FA_OK) return r;
+  if ((r = fa::check_ptrs({Q, K, V, O, LSE})) != FA_OK) return r;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  const fa::Mask m{mask, mask_stride_b, mask_stride_h, mask_stride_row};
+  if ((r = fa::check_mask(m, s, dtype)) != FA_OK) return r;
+  int* status = fa::device_status_ptr();
+  if (!status) return FA_ERR_CUDA;
+  return fa::from_cuda(fa::tc_fwd_masked(Q, K, V, O, LSE, s, scale, causal == 1, mask, m.sb, m.sh, m.srow, status,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" fa_status_t fa_bwd_masked(const void* Q, const void* K, const void* V, const void* O,
+                                     const void* dO, const float* LSE, const float* D, void* dQ, void* dK,
+                                     void* dV, const void* mask, long long mask_stride_b,
+                                     long long mask_stride_h, long long mask_stride_row, void* workspace,
+                                     size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                                     int dtype, void* stream) {
+  const fa::Mask m{mask, mask_stride_b, mask_stride_h, mask_stride_row};
+  return fa::bwd_common(Q, K, V, O, dO, LSE, D, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, scale, causal,
+                        dtype, &m, stream);
 }
 
 namespace {

@@ -107,6 +107,10 @@ struct BwdParams {
   int causal;
   float scale;
   float sl2;  // scale * log2(e)
+  // additive mask (kMask): element (b, h, i, j) at mask[b*mask_sb + h*mask_sh + i*mask_srow + j]
+  const __nv_bfloat16* mask;
+  int64_t mask_sb, mask_sh, mask_srow;
+  int H;
 };
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -127,7 +131,7 @@ __device__ __forceinline__ uint32_t packed_col(uint32_t base, int k) {
 
 // kTail: N is not a multiple of the tiles, so the partial-tile guards are compiled in; the
 // instance for whole tiles carries none of them.
-template <int D, bool kTail>
+template <int D, bool kTail, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -393,6 +397,21 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
       for (int ch = 0; ch < kCols / 32; ++ch) {
         const int c0 = wg * kCols + ch * 32;  // first query column of this chunk
+        // kMask: M(query, this key) * log2(e) for the chunk's 32 queries; across the warp
+        // each load reads 32 consecutive keys of one mask row. Issued before the TMEM loads
+        // so that their latency overlaps.
+        float mk[kMask ? 32 : 1];
+        if constexpr (kMask) {
+          const __nv_bfloat16* mcol = p.mask + (int64_t)(head / p.H) * p.mask_sb +
+                                      (int64_t)(head % p.H) * p.mask_sh + key;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int q = q0 + c0 + c;
+            mk[c] = (!kTail || (key < p.N && q < p.N))
+                        ? __bfloat162float(mcol[(int64_t)q * p.mask_srow]) * kLog2e
+                        : 0.f;
+          }
+        }
         float sv[32], dp[32];
         tmem_ld32x2(tmem + lane_off + C::colS(b) + c0, tmem + lane_off + C::colDP(b) + c0, sv, dp);
         // -LSE*log2(e) and D for the 32 columns, loaded as 16-byte vectors up front
@@ -403,6 +422,12 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           const float4 b = *reinterpret_cast<const float4*>(vec + BQ + c0 + 4 * u);
           nl[2 * u] = fmul2(make_float2(a.x, a.y), neg_log2e);
           nl[2 * u + 1] = fmul2(make_float2(a.z, a.w), neg_log2e);
+          if constexpr (kMask) {  // a query with no visible key (LSE = -inf) has P = 0
+            if (a.x == -INFINITY) nl[2 * u].x = -INFINITY;
+            if (a.y == -INFINITY) nl[2 * u].y = -INFINITY;
+            if (a.z == -INFINITY) nl[2 * u + 1].x = -INFINITY;
+            if (a.w == -INFINITY) nl[2 * u + 1].y = -INFINITY;
+          }
           dv[2 * u] = make_float2(b.x, b.y);
           dv[2 * u + 1] = make_float2(b.z, b.w);
         }
@@ -410,7 +435,8 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int c = c0 + 2 * u;
-          const float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, nl[u]);
+          float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, nl[u]);
+          if constexpr (kMask) x = fadd2(x, make_float2(mk[2 * u], mk[2 * u + 1]));
           float2 pr = make_float2(ex2(x.x), ex2(x.y));
           if (diag) {
             if (key > q0 + c) pr.x = 0.f;
@@ -546,10 +572,15 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
   reinterpret_cast<uint4*>(dq)[i] = w;
 }
 
-template <int D>
+struct MaskArg {
+  const void* ptr = nullptr;
+  int64_t sb = 0, sh = 0, srow = 0;
+};
+
+template <int D, bool kMask>
 cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                    const float* Dv, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
-                   float scale, bool causal, int* status, cudaStream_t st) {
+                   float scale, bool causal, const MaskArg& mask, int* status, cudaStream_t st) {
   using C = BwdCfg<D>;
   CUtensorMap mq, mk, mv, mdo;
   const int64_t heads = s.heads();
@@ -557,9 +588,9 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
       !make_map_bf16_3d(&mv, V, heads, s.N, D, BN) || !make_map_bf16_3d(&mdo, dO, heads, s.N, D, C::BQ))
     return cudaErrorInvalidValue;
   static bool attr = [] {
-    return cudaFuncSetAttribute(fa_bwd_tc_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(fa_bwd_tc_kernel<D, false, kMask>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes) == cudaSuccess &&
-           cudaFuncSetAttribute(fa_bwd_tc_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+           cudaFuncSetAttribute(fa_bwd_tc_kernel<D, true, kMask>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes) == cudaSuccess;
   }();
   if (!attr) return cudaErrorInvalidConfiguration;
@@ -579,11 +610,16 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.sl2 = scale * kLog2e;
+  p.mask = static_cast<const __nv_bfloat16*>(mask.ptr);
+  p.mask_sb = mask.sb;
+  p.mask_sh = mask.sh;
+  p.mask_srow = mask.srow;
+  p.H = s.H;
   const int64_t grid = (int64_t)p.kvtiles * p.heads;
   if (s.N % 128 != 0)
-    fa_bwd_tc_kernel<D, true><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
+    fa_bwd_tc_kernel<D, true, kMask><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
   else
-    fa_bwd_tc_kernel<D, false><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
+    fa_bwd_tc_kernel<D, false, kMask><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t n8 = s.elems() / 8;
   dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(dQacc, static_cast<__nv_bfloat16*>(dQ),
@@ -596,8 +632,22 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
 cudaError_t tc_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                    const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st) {
-  return s.d == 64 ? launch<64>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, status, st)
-                   : launch<128>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, status, st);
+  const MaskArg none;
+  return s.d == 64 ? launch<64, false>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, none, status, st)
+                   : launch<128, false>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, none, status, st);
+}
+
+cudaError_t tc_bwd_masked(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                          const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
+                          float scale, bool causal, const void* mask, int64_t mask_sb, int64_t mask_sh,
+                          int64_t mask_srow, int* status, cudaStream_t st) {
+  MaskArg m;
+  m.ptr = mask;
+  m.sb = mask_sb;
+  m.sh = mask_sh;
+  m.srow = mask_srow;
+  return s.d == 64 ? launch<64, true>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, m, status, st)
+                   : launch<128, true>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, m, status, st);
 }
 
 }  // namespace fa

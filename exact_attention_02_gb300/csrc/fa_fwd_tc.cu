@@ -31,6 +31,14 @@
 // max lies in e4m3's normal range (relative rounding error <= 2^-4); the factor 16 cancels
 // in O / l and is taken out of the LSE.
 //
+// Additive mask instance (kMask): an [N, N] bf16 mask M per head (broadcast over batch or
+// heads by zero strides) is added to the scaled scores ("知识点13" section 7 fuses the mask
+// into the softmax step). Each softmax thread streams its row's 128 mask values for the
+// next K tile into registers while the current tile is processed, and folds them into S
+// as S + M / scale, so the exponent multiplier turns them into (scale q.k + M) log2 e.
+// Rows with no visible key so far keep m = -inf and exponentiate against 0; a row with
+// no visible key at all stores O = 0 and LSE = -inf.
+//
 // Causal: tile t sees K tiles 0..qtile_t; the diagonal tile masks key > query.
 // Any N: Q/K/V are read through [heads, N, d] tensor maps, so rows past the end of a head
 // arrive as zeros; keys past the end are masked and rows past the end are not stored.
@@ -92,6 +100,11 @@ struct FwdParams {
   int causal;
   float sl2;      // scale * log2(e) (* the Q and K factors for e4m3)
   float o_scale;  // V's factor for e4m3, else 1
+  // additive mask (kMask): element (b, h, i, j) at mask[b*mask_sb + h*mask_sh + i*mask_srow + j]
+  const __nv_bfloat16* mask;
+  int64_t mask_sb, mask_sh, mask_srow;
+  int H;
+  float inv_scale;  // 1 / scale: M joins the raw scores as M / scale
 };
 
 struct FwdCtl {
@@ -103,7 +116,7 @@ struct FwdCtl {
   int abort;
 };
 
-template <int D, bool F8>
+template <int D, bool F8, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -277,6 +290,19 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const float sl2 = p.sl2;
     float m = -INFINITY, l = 0.f;
     bool ok = nk > 0;
+    // kMask: this row's mask values for the K tile about to be processed, 8 bf16 per
+    // 16-byte load (rows of the mask are 16-byte aligned and padded to a multiple of 8);
+    // rows and columns past the end of the head load nothing.
+    uint4 mreg[kMask ? BN / 8 : 1];
+    const __nv_bfloat16* mrow = nullptr;
+    if constexpr (kMask) {
+      if (qrow < p.N)
+        mrow = p.mask + (int64_t)(head / p.H) * p.mask_sb + (int64_t)(head % p.H) * p.mask_sh +
+               (int64_t)qrow * p.mask_srow;
+#pragma unroll
+      for (int c8 = 0; c8 < BN / 8; ++c8)
+        mreg[c8] = (mrow && 8 * c8 < p.N && nk > 0) ? ld_global_v4_ordered(mrow + 8 * c8) : make_uint4(0, 0, 0, 0);
+    }
     // tcgen05.ld/st are warp-collective (.sync.aligned): every branch that guards one
     // is made uniform across the warp, including the outcome of each bounded wait.
     for (int j = 0; ok && j < nk; ++j) {
@@ -284,9 +310,29 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       float sv[BN];
-      tmem_ld32x2(tS, tS + 32, *reinterpret_cast<float(*)[32]>(&sv[0]), *reinterpret_cast<float(*)[32]>(&sv[32]));
-      tmem_ld32x2(tS + 64, tS + 96, *reinterpret_cast<float(*)[32]>(&sv[64]),
-                  *reinterpret_cast<float(*)[32]>(&sv[96]));
+      if constexpr (!kMask) {
+        tmem_ld32x2(tS, tS + 32, *reinterpret_cast<float(*)[32]>(&sv[0]), *reinterpret_cast<float(*)[32]>(&sv[32]));
+        tmem_ld32x2(tS + 64, tS + 96, *reinterpret_cast<float(*)[32]>(&sv[64]),
+                    *reinterpret_cast<float(*)[32]>(&sv[96]));
+      } else {
+        // 32 columns at a time, each folded with its mask values at once, so the mask
+        // registers free up as the scores arrive (the row and the prefetched mask do not
+        // fit in registers together)
+#pragma unroll
+        for (int q = 0; q < BN / 32; ++q) {
+          tmem_ld32(tS + 32 * q, *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+#pragma unroll
+          for (int c8 = 4 * q; c8 < 4 * q + 4; ++c8) {  // s += M / scale
+            const uint32_t w[4] = {mreg[c8].x, mreg[c8].y, mreg[c8].z, mreg[c8].w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float lo = __uint_as_float(w[u] << 16), hi = __uint_as_float(w[u] & 0xFFFF0000u);
+              sv[8 * c8 + 2 * u] = fmaf(lo, p.inv_scale, sv[8 * c8 + 2 * u]);
+              sv[8 * c8 + 2 * u + 1] = fmaf(hi, p.inv_scale, sv[8 * c8 + 2 * u + 1]);
+            }
+          }
+        }
+      }
       // Hidden keys: key > query on the diagonal tile (causal), and keys past the end of
       // the head in its last, partial tile (their rows were read as zeros). Every row keeps
       // at least key 0 of the tile visible.
@@ -331,7 +377,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (grow) m = m_new;
       }
       const float2 sl2v = make_float2(sl2, sl2);
-      const float2 neg_m = make_float2(C::kPShift - m, C::kPShift - m);
+      // a row with no visible key so far (only possible with a mask) exponentiates
+      // against 0: its scores are all -inf, so every p is 0
+      const float m_use = (kMask && m == -INFINITY) ? 0.f : m;
+      const float2 neg_m = make_float2(C::kPShift - m_use, C::kPShift - m_use);
       float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
       if constexpr (!F8) {
 #pragma unroll
@@ -368,6 +417,13 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
       l += (rs0.x + rs0.y) + (rs1.x + rs1.y);
+      if constexpr (kMask) {  // the next tile's mask lands while its S is computed
+#pragma unroll
+        for (int c8 = 0; c8 < BN / 8; ++c8) {
+          const int col = (j + 1) * BN + 8 * c8;
+          mreg[c8] = (mrow && col < p.N && j + 1 < nk) ? ld_global_v4_ordered(mrow + col) : make_uint4(0, 0, 0, 0);
+        }
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&ctl.p_full[t]);
@@ -375,7 +431,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.o_full[t], 0, p.status, abort));
     if (ok) {
       tc_fence_after();
-      const float inv_l = p.o_scale / l;
+      const float inv_l = (!kMask || l > 0.f) ? p.o_scale / l : 0.f;  // no visible key: O = 0
       __nv_bfloat16* orow = p.O + (size_t)(row_base + qrow) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -403,9 +459,15 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   }
 }
 
-template <int D, bool F8>
+struct MaskArg {
+  const void* ptr = nullptr;
+  int64_t sb = 0, sh = 0, srow = 0;
+};
+
+template <int D, bool F8, bool kMask>
 cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
-                   float sl2, float o_scale, bool causal, int* status, cudaStream_t st) {
+                   float scale, float sl2, float o_scale, bool causal, const MaskArg& mask, int* status,
+                   cudaStream_t st) {
   using C = FwdCfg<D, F8>;
   CUtensorMap mq, mk, mv;
   const int64_t heads = s.heads();
@@ -418,7 +480,7 @@ cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* 
            make_map_bf16_3d(&mv, V, heads, s.N, D, BN);
   if (!maps) return cudaErrorInvalidValue;
   static bool attr = [] {
-    return cudaFuncSetAttribute(fa_fwd_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(fa_fwd_tc_kernel<D, F8, kMask>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes) == cudaSuccess;
   }();
   if (!attr) return cudaErrorInvalidConfiguration;
@@ -433,8 +495,14 @@ cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.causal = causal ? 1 : 0;
   p.sl2 = sl2;
   p.o_scale = o_scale;
+  p.mask = static_cast<const __nv_bfloat16*>(mask.ptr);
+  p.mask_sb = mask.sb;
+  p.mask_sh = mask.sh;
+  p.mask_srow = mask.srow;
+  p.H = s.H;
+  p.inv_scale = 1.f / scale;
   const int64_t grid = (int64_t)p.pairs * p.heads;
-  fa_fwd_tc_kernel<D, F8><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p);
+  fa_fwd_tc_kernel<D, F8, kMask><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -444,15 +512,30 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st) {
-  return s.d == 64 ? launch<64, false>(Q, K, V, O, LSE, s, scale * kLog2e, 1.f, causal, status, st)
-                   : launch<128, false>(Q, K, V, O, LSE, s, scale * kLog2e, 1.f, causal, status, st);
+  const MaskArg none;
+  return s.d == 64 ? launch<64, false, false>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, none, status, st)
+                   : launch<128, false, false>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, none, status,
+                                               st);
+}
+
+cudaError_t tc_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                          float scale, bool causal, const void* mask, int64_t mask_sb, int64_t mask_sh,
+                          int64_t mask_srow, int* status, cudaStream_t st) {
+  MaskArg m;
+  m.ptr = mask;
+  m.sb = mask_sb;
+  m.sh = mask_sh;
+  m.srow = mask_srow;
+  return s.d == 64 ? launch<64, false, true>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, m, status, st)
+                   : launch<128, false, true>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, m, status, st);
 }
 
 cudaError_t tc_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                        float scale, bool causal, float q_descale, float k_descale, float v_descale,
                        int* status, cudaStream_t st) {
-  return launch<128, true>(Q, K, V, O, LSE, s, scale * kLog2e * q_descale * k_descale, v_descale, causal,
-                           status, st);
+  const MaskArg none;
+  return launch<128, true, false>(Q, K, V, O, LSE, s, scale, scale * kLog2e * q_descale * k_descale, v_descale,
+                                  causal, none, status, st);
 }
 
 }  // namespace fa

@@ -31,6 +31,11 @@ cudaError_t simt_bwd(const void* Q, const void* K, const void* V, const void* dO
 // ---- tcgen05 tensor-core path (bf16, d in {64, 128}, N % 128 == 0) ----
 cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st);
+// bf16 forward with an additive bf16 mask: element (b, h, i, j) at
+// mask[b*mask_sb + h*mask_sh + i*mask_srow + j] (strides in elements, multiples of 8).
+cudaError_t tc_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                          float scale, bool causal, const void* mask, int64_t mask_sb, int64_t mask_sh,
+                          int64_t mask_srow, int* status, cudaStream_t st);
 // e4m3 Q, K, V (d = 128) with per-tensor dequantisation factors; O bf16, LSE fp32.
 cudaError_t tc_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                        float scale, bool causal, float q_descale, float k_descale, float v_descale,
@@ -39,6 +44,12 @@ cudaError_t tc_fwd_fp8(const void* Q, const void* K, const void* V, void* O, flo
 cudaError_t tc_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                    const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st);
+
+// The backward with the additive mask of tc_fwd_masked.
+cudaError_t tc_bwd_masked(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                          const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
+                          float scale, bool causal, const void* mask, int64_t mask_sb, int64_t mask_sh,
+                          int64_t mask_srow, int* status, cudaStream_t st);
 
 // ---- split-KV forward for few queries (fa_splitkv.cu): bf16, d in {64, 128}, Nq <= 16 ----
 size_t splitkv_workspace_floats(int64_t heads, int Nq, int Nk, int d);

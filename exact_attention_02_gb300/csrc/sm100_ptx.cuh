@@ -377,6 +377,17 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, fl
   return r;
 }
 
+// 16-byte global load that the compiler may not move across other memory operations or
+// volatile asm (used to place a prefetch exactly where its registers are free).
+__device__ __forceinline__ uint4 ld_global_v4_ordered(const void* ptr) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(ptr)
+               : "memory");
+  return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -148,6 +148,34 @@ FA_API fa_status_t fa_fwd_splitkv(const void* Q, const void* K, const void* V, v
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_fwd_masked / fa_bwd_masked — fa_fwd / fa_bwd with an additive mask M added to the
+ * scaled scores ("知识点13 FlashAttention深度攻略" §7 算子融合优化: the mask is applied inside
+ * the fused softmax step):
+ *      s_ij = scale * q_i . k_j + M_ij,   then the causal rule (if causal) as for fa_fwd.
+ * mask: bf16 (dtype must be FA_DTYPE_BF16, else FA_ERR_UNSUPPORTED), device pointer,
+ *      16-byte aligned. Element M(b, h, i, j) is read at
+ *      mask[b * mask_stride_b + h * mask_stride_h + i * mask_stride_row + j]
+ *      (strides in elements; 0 broadcasts over batch or heads). Every stride must be a
+ *      non-negative multiple of 8 and mask_stride_row >= N rounded up to 8 (rows are read
+ *      in 16-byte pieces; the padding is never used). The caller owns the mask; it is read
+ *      by both calls and never written. Entries are finite or -inf (-inf hides the key).
+ * A query whose every key is hidden has no softmax: it gets O = 0 and LSE = -inf, and it
+ *      contributes nothing to dK or dV (its dQ row is 0).
+ * The remaining arguments, layouts, workspace and errors are those of fa_fwd and fa_bwd;
+ *      pass the same mask, scale and causal flag to both.
+ */
+FA_API fa_status_t fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                 const void* mask, long long mask_stride_b, long long mask_stride_h,
+                                 long long mask_stride_row, int B, int H, int N, int d, float scale,
+                                 int causal, int dtype, void* stream);
+FA_API fa_status_t fa_bwd_masked(const void* Q, const void* K, const void* V, const void* O,
+                                 const void* dO, const float* LSE, const float* D, void* dQ, void* dK,
+                                 void* dV, const void* mask, long long mask_stride_b,
+                                 long long mask_stride_h, long long mask_stride_row, void* workspace,
+                                 size_t workspace_bytes, int B, int H, int N, int d, float scale,
+                                 int causal, int dtype, void* stream);
+
+/*
  * fa_fwd_fp8 — the forward of fa_fwd on 8-bit inputs ("flash-attention" (data.6616ai.com),
  * 参考答案: FlashAttention-3 runs on FP8; "知识点13" 前沿研究方向: mixed precision with FP8).
  * In:  Q, K, V [B,H,N,d] as e4m3 bytes (OCP FP8 E4M3: 1 sign, 4 exponent bits with bias 7,

@@ -30,7 +30,7 @@ def _declared():
 def test_header_declares_the_boundary():
     assert set(_declared()) >= {"fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_bwd_workspace_size",
                                 "fa_get_error_string", "fa_get_last_device_status", "fa_fwd_splitkv",
-                                "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8"}
+                                "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked"}
 
 
 def test_exports_every_declared_symbol(lib):
@@ -155,3 +155,23 @@ def test_fp8_rejects_before_launch(lib):
     assert call(causal=2) == fa.FA_ERR_INVALID_ARG
     assert call(N=0) == fa.FA_ERR_INVALID_ARG
     assert call(ptr=P + 8) == fa.FA_ERR_INVALID_ARG    # misaligned
+
+
+def test_masked_rejects_before_launch(lib):
+    """Host-side checks of the mask arguments (dummy pointers; nothing is launched)."""
+    import exact_attention_02_gb300 as fa
+    vp, f, ll = ctypes.c_void_p, ctypes.c_float, ctypes.c_longlong
+    L = fa.lib()
+    L.fa_fwd_masked.argtypes = [vp] * 6 + [ll, ll, ll] + [ctypes.c_int] * 4 + [f, ctypes.c_int, ctypes.c_int, vp]
+
+    def call(mask=P, sb=0, sh=0, srow=128, N=128, dtype=0, d=64):
+        return L.fa_fwd_masked(vp(P), vp(P), vp(P), vp(P), vp(P), vp(mask), ll(sb), ll(sh), ll(srow), 1, 1, N, d,
+                               f(0.125), 0, dtype, None)
+    assert call(mask=0) == fa.FA_ERR_INVALID_ARG            # no mask
+    assert call(mask=P + 8) == fa.FA_ERR_INVALID_ARG        # misaligned
+    assert call(srow=120) == fa.FA_ERR_INVALID_ARG          # row shorter than N
+    assert call(N=100, srow=100) == fa.FA_ERR_INVALID_ARG   # rows not padded to a multiple of 8
+    assert call(sb=-8) == fa.FA_ERR_INVALID_ARG
+    assert call(sh=4) == fa.FA_ERR_INVALID_ARG
+    assert call(dtype=1) == fa.FA_ERR_UNSUPPORTED           # the fp32 path has no mask
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
