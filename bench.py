@@ -171,6 +171,12 @@ def count_launches(step):
         return None, [f"profiler unavailable: {e}"]
 
 
+class _Named:
+    """A workload known only by name (the split-KV and FP8 lines)."""
+    def __init__(self, name):
+        self.name = name
+
+
 def recorded_traffic(kernel, w):
     """DRAM bytes per launch from profiles/traffic.json, if recorded for this workload and the
     kernel's sources are unchanged since the capture; else None."""
@@ -425,17 +431,18 @@ def run_splitkv(args):
     nbytes = 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
     gbs = nbytes / (ms * 1e-3) / 1e9
     flop = 4.0 * B * H * Nq * Nk * d
+    workload = f"splitkv_b{B}h{H}_q{Nq}_k{Nk}_d{d}" + ("_causal" if c else "")
     print(json.dumps({
         "metric": "split-KV forward HBM GB/s (few queries against a long key/value sequence)",
         "value": gbs, "unit": "GB/s", "ms_per_step": ms, "steps": args.steps, "higher_is_better": True,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"splitkv_b{B}h{H}_q{Nq}_k{Nk}_d{d}" + ("_causal" if c else ""),
+        "config": {"workload": workload,
                    "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": bool(c),
                    "l2": "no flush: K and V exceed the 129 MB L2" if 2 * B * H * Nk * d * 2 > 129e6 else "fits L2"},
         "tflops": flop / (ms * 1e-3) / 1e12,
         "roofline": {"kernel": "fa_fwd_splitkv", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "peak_source": f"HBM copy ({src})",
-                     "traffic": None},
+                     "traffic": recorded_traffic("fa_fwd_splitkv", _Named(workload))},
         "gpu_launches": 2 * args.steps, "kernels_per_step": fa.SPLITKV_KERNELS,
     }), flush=True)
     return 0
@@ -479,16 +486,18 @@ def run_fp8(args):
     tf = flop / (ms * 1e-3) / 1e12
     peak = 2 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     in_bytes = 3 * B * H * N * d
+    workload = f"fp8_b{B}h{H}_n{N}_d{d}" + ("_causal" if c else "")
     print(json.dumps({
         "metric": "attention fwd TFLOP/s on e4m3 inputs (fa_fwd_fp8)", "value": tf, "unit": "TFLOP/s",
         "ms_per_step": ms, "steps": args.steps, "higher_is_better": True, "dtype": "e4m3 (fp32 accumulate)",
         "data": "synthetic",
-        "config": {"workload": f"fp8_b{B}h{H}_n{N}_d{d}" + ("_causal" if c else ""), "B": B, "H": H, "N": N,
+        "config": {"workload": workload, "B": B, "H": H, "N": N,
                    "d": d, "causal": bool(c),
                    "l2": "no flush: inputs and output exceed the 129 MB L2" if in_bytes * 3 > 129e6 else "fits L2"},
         "roofline": {"kernel": "fa_fwd_tc_kernel<128, e4m3>", "bound": "tensor", "achieved": tf, "peak": peak,
                      "unit": "TFLOP/s", "frac": tf / peak,
-                     "peak_source": f"2 x dense bf16 sustained ({src}); nominal fp8/bf16 ratio", "traffic": None},
+                     "peak_source": f"2 x dense bf16 sustained ({src}); nominal fp8/bf16 ratio",
+                     "traffic": recorded_traffic("fa_fwd_fp8", _Named(workload))},
         "gpu_launches": args.steps, "kernels_per_step": fa.FP8_KERNELS,
     }), flush=True)
     return 0
