@@ -26,6 +26,11 @@ Readings where the pages leave a choice open:
     the "mask" that "知识点13" section 7 (算子融合优化) fuses into the softmax step. A row
     whose every key is hidden (all -inf) has no softmax: its weights are taken as 0, so
     O_i = 0, LSE_i = -inf and the row contributes nothing to any gradient.
+  * Dropout (optional; "知识点13" section 7 lists it with the mask inside the fused
+    softmax step) multiplies each weight by keep_ij * c after the softmax: O = (P o K c) V
+    with K a 0/1 keep matrix and c = keep_scale. LSE stays the softmax's. The backward
+    follows from L(O): dV = (P o K c)^T dO, dP = (dO V^T) o K c, dS = P o (dP - D) with
+    D_i = dO_i . O_i of the dropped O. The keep matrix comes from oracle/philox.py.
   * Causal attention hides key j from query i iff j > i (queries and keys share
     the same positions; the diagonal is always visible, so no row is empty). With
     fewer queries than keys (N_q < N_k, e.g. decoding against a cache) the queries are
@@ -88,10 +93,11 @@ def softmax_rows(s):
     return P, m, l
 
 
-def head_forward(q, k, v, scale, causal, rows=None, mask=None):
+def head_forward(q, k, v, scale, causal, rows=None, mask=None, keep=None, keep_scale=1.0):
     """O and LSE of one head for query ``rows`` (default: all rows).
 
-    q, k, v: [N, d] float64; mask: optional [N_q, N_k] additive mask. Returns O
+    q, k, v: [N, d] float64; mask: optional [N_q, N_k] additive mask; keep: optional
+    [N_q, N_k] 0/1 dropout keep matrix with its scale keep_scale. Returns O
     [len(rows), d] and LSE [len(rows)], where O_i = sum_j P_ij v_j ([FA2] section 1) and
     LSE_i = m_i + ln l_i (-inf for a row with no visible key).
     """
@@ -104,6 +110,8 @@ def head_forward(q, k, v, scale, causal, rows=None, mask=None):
     for a in range(0, rows.size, g):
         r = rows[a:a + g]
         P, m, l = softmax_rows(scores(q, k, scale, causal, r, mask))
+        if keep is not None:
+            P = P * (np.asarray(keep, np.float64)[r] * keep_scale)
         O[a:a + g] = P @ v
         with np.errstate(divide="ignore"):
             LSE[a:a + g] = m + np.log(l)
@@ -115,7 +123,7 @@ def row_dot(do, o):
     return np.einsum("ic,ic->i", np.asarray(do, np.float64), np.asarray(o, np.float64))
 
 
-def head_backward(q, k, v, do, scale, causal, return_ds=False, mask=None):
+def head_backward(q, k, v, do, scale, causal, return_ds=False, mask=None, keep=None, keep_scale=1.0):
     """All outputs of one head: O, LSE, D, dQ, dK, dV (and dS when asked, small N only).
 
     [BWD] 反向总览 / Softmax梯度 / QKV梯度:
@@ -124,7 +132,7 @@ def head_backward(q, k, v, do, scale, causal, return_ds=False, mask=None):
     """
     q, k, v, do = (np.asarray(a, dtype=np.float64) for a in (q, k, v, do))
     N, d = q.shape
-    O, LSE = head_forward(q, k, v, scale, causal, mask=mask)
+    O, LSE = head_forward(q, k, v, scale, causal, mask=mask, keep=keep, keep_scale=keep_scale)
     D = row_dot(do, O)
     dQ = np.empty_like(q)
     dK = np.zeros_like(k)
@@ -134,8 +142,9 @@ def head_backward(q, k, v, do, scale, causal, return_ds=False, mask=None):
     for a in range(0, N, g):
         r = np.arange(a, min(N, a + g))
         P, _, _ = softmax_rows(scores(q, k, scale, causal, r, mask))
-        dV += P.T @ do[r]
-        dP = do[r] @ v.T
+        Kc = 1.0 if keep is None else np.asarray(keep, np.float64)[r] * keep_scale
+        dV += (P * Kc).T @ do[r]
+        dP = (do[r] @ v.T) * Kc
         dS = P * (dP - D[r, None])
         dQ[r] = scale * (dS @ k)
         dK += scale * (dS.T @ q[r])

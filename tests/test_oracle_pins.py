@@ -469,6 +469,63 @@ def pin_mask_hidden_row(m):
     assert np.allclose(r["dv"], rk["dv"], rtol=0, atol=1e-13)
 
 
+# -- dropout ("知识点13" section 7): O = (P o K c) V with a fixed 0/1 keep matrix K -------
+def _keep(N, seed, p=0.3):
+    return np.random.default_rng(seed).random((N, N)) >= p
+
+
+def pin_dropout_keep_all(m):
+    """Keeping every weight with scale 1 is no dropout."""
+    N, d = 8, 3
+    q, k, v, do = (_rand((N, d), 800 + s) for s in range(4))
+    a = m.head_backward(q, k, v, do, 0.5, True)
+    b = m.head_backward(q, k, v, do, 0.5, True, keep=np.ones((N, N), bool), keep_scale=1.0)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        assert np.allclose(a[n], b[n], rtol=0, atol=1e-14), n
+
+
+def pin_dropout_finite_differences(m):
+    """Central differences of <O, dO> with the keep matrix held fixed."""
+    h = 1e-5
+    for N, d, causal, seed in ((6, 3, False, 810), (9, 4, True, 811)):
+        q, k, v, do = (_rand((N, d), seed + s) for s in range(4))
+        K, c = _keep(N, seed + 9), 1.0 / 0.7
+        r = m.head_backward(q, k, v, do, 0.5, causal, keep=K, keep_scale=c)
+
+        def loss(qq, kk, vv):
+            return float((m.head_forward(qq, kk, vv, 0.5, causal, keep=K, keep_scale=c)[0] * do).sum())
+        for pos, name in enumerate(("dq", "dk", "dv")):
+            x = [q, k, v][pos]
+            g = np.empty_like(x)
+            for idx in np.ndindex(*x.shape):
+                ap, am = [q, k, v], [q, k, v]
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                ap[pos], am[pos] = xp, xm
+                g[idx] = (loss(*ap) - loss(*am)) / (2 * h)
+            err = np.abs(g - r[name]).max() / max(1e-300, np.abs(g).max())
+            assert err < 1e-7, (name, N, causal, err)
+
+
+def pin_dropout_torch_autograd(m):
+    """PyTorch float64 autograd of O = (softmax(S) * K * c) V, and LSE of the undropped S."""
+    torch = pytest.importorskip("torch")
+    N, d, scale = 12, 5, 0.4
+    arrs = [_rand((N, d), 820 + s) for s in range(4)]
+    K, c = _keep(N, 825), 1.0 / 0.75
+    t = [torch.tensor(a, dtype=torch.float64, requires_grad=(i < 3)) for i, a in enumerate(arrs)]
+    s = scale * t[0] @ t[1].T
+    s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+    o = (torch.softmax(s, -1) * torch.tensor(K, dtype=torch.float64) * c) @ t[2]
+    (o * t[3]).sum().backward()
+    r = m.head_backward(*arrs, scale, True, keep=K, keep_scale=c)
+    assert np.allclose(r["o"], o.detach().numpy(), rtol=0, atol=1e-12)
+    assert np.allclose(r["lse"], torch.logsumexp(s, -1).detach().numpy(), rtol=0, atol=1e-12)
+    for name, ten in zip(("dq", "dk", "dv"), t[:3]):
+        assert np.allclose(r[name], ten.grad.numpy(), rtol=0, atol=1e-12), name
+
+
 PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_")]
 
 
@@ -494,10 +551,14 @@ MUTATIONS = [
     ("wrong sign in dS", "dS = P * (dP - D[r, None])", "dS = P * (D[r, None] - dP)"),
     ("scale missing on dK", "dK += scale * (dS.T @ q[r])", "dK += dS.T @ q[r]"),
     ("scale missing on dQ", "dQ[r] = scale * (dS @ k)", "dQ[r] = dS @ k"),
-    ("dV uses V instead of dO", "dV += P.T @ do[r]", "dV += P.T @ v[r]"),
-    ("dV without the transpose", "dV += P.T @ do[r]", "dV += P @ do[r]"),
+    ("dV uses V instead of dO", "dV += (P * Kc).T @ do[r]", "dV += (P * Kc).T @ v[r]"),
+    ("dV without the transpose", "dV += (P * Kc).T @ do[r]", "dV += (P * Kc) @ do[r]"),
     ("dQ uses Q instead of K", "dQ[r] = scale * (dS @ k)", "dQ[r] = scale * (dS @ q)"),
-    ("dP uses K instead of V", "dP = do[r] @ v.T", "dP = do[r] @ k.T"),
+    ("dP uses K instead of V", "dP = (do[r] @ v.T) * Kc", "dP = (do[r] @ k.T) * Kc"),
+    ("dropout scale missing in O", "P = P * (np.asarray(keep, np.float64)[r] * keep_scale)",
+     "P = P * np.asarray(keep, np.float64)[r]"),
+    ("dropout not applied to dP", "dP = (do[r] @ v.T) * Kc", "dP = do[r] @ v.T"),
+    ("dropout not applied to dV", "dV += (P * Kc).T @ do[r]", "dV += P.T @ do[r]"),
     ("mask hides diagonal", "j[None, :] > rows[:, None]", "j[None, :] >= rows[:, None]"),
     ("mask keeps the future", "j[None, :] > rows[:, None]", "j[None, :] < rows[:, None]"),
     ("top-left alignment for fewer queries", "offset = k.shape[0] - q.shape[0]", "offset = 0"),
