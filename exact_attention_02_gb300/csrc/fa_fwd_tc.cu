@@ -39,12 +39,18 @@
 // Rows with no visible key so far keep m = -inf and exponentiate against 0; a row with
 // no visible key at all stores O = 0 and LSE = -inf.
 //
+// Dropout instance (kVar == 2): the same section of "知识点13" fuses dropout into the
+// softmax step. Each softmax thread draws the keep bits of its row for the next K tile
+// (16 Philox calls, see philox.cuh) while the tile's S is being computed, stores p only
+// for kept keys (row sums l still take every p) and scales O by 65536 / (65536 - t).
+//
 // Causal: tile t sees K tiles 0..qtile_t; the diagonal tile masks key > query.
 // Any N: Q/K/V are read through [heads, N, d] tensor maps, so rows past the end of a head
 // arrive as zeros; keys past the end are masked and rows past the end are not stored.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
+#include "philox.cuh"
 #include "sm100_ptx.cuh"
 #include "tma_host.h"
 
@@ -105,6 +111,9 @@ struct FwdParams {
   int64_t mask_sb, mask_sh, mask_srow;
   int H;
   float inv_scale;  // 1 / scale: M joins the raw scores as M / scale
+  // dropout (kVar == 2): Philox key, keep threshold and the scale of a kept weight
+  uint32_t seed_lo, seed_hi, drop_t;
+  float drop_scale;
 };
 
 struct FwdCtl {
@@ -116,11 +125,15 @@ struct FwdCtl {
   int abort;
 };
 
-template <int D, bool F8, bool kMask>
+// kVar: 0 plain, 1 additive mask, 2 dropout.
+template <int D, bool F8, int kVar>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D, F8>;
+  constexpr bool kMask = kVar == 1;
+  constexpr bool kDrop = kVar == 2;
+  static_assert(!(F8 && kVar), "the e4m3 instance has no mask or dropout");
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -306,6 +319,18 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // tcgen05.ld/st are warp-collective (.sync.aligned): every branch that guards one
     // is made uniform across the warp, including the outcome of each bounded wait.
     for (int j = 0; ok && j < nk; ++j) {
+      // kDrop: keep bits of this row against the tile's 128 keys (bit c of word c / 32),
+      // drawn before waiting for S so that the work overlaps the S product
+      uint32_t keep[kDrop ? BN / 32 : 1];
+      if constexpr (kDrop) {
+#pragma unroll
+        for (int w = 0; w < BN / 32; ++w) keep[w] = 0;
+#pragma unroll
+        for (int c8 = 0; c8 < BN / 8; ++c8)
+          keep[c8 / 4] |= rng::keep8((uint32_t)(j * (BN / 8) + c8), (uint32_t)qrow, (uint32_t)head, p.seed_lo,
+                                     p.seed_hi, p.drop_t)
+                          << (8 * (c8 % 4));
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full[t], j & 1, p.status, abort));
       if (!ok) break;
       tc_fence_after();
@@ -344,10 +369,12 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         for (int c = 0; c < BN; ++c)
           if (c > lim) sv[c] = -INFINITY;
       }
-      // row max: four independent chains of 3-input max
-      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+      // row max: four independent chains of 3-input max over columns 0..BN-1
+      static_assert(BN % 8 == 0, "the chains take 8 columns per step");
+      float mx0 = fmaxf(sv[0], sv[1]), mx1 = fmaxf(sv[2], sv[3]), mx2 = fmaxf(sv[4], sv[5]),
+            mx3 = fmaxf(sv[6], sv[7]);
 #pragma unroll
-      for (int c = 4; c < BN; c += 8) {
+      for (int c = 8; c < BN; c += 8) {
         mx0 = fmax3(mx0, sv[c], sv[c + 1]);
         mx1 = fmax3(mx1, sv[c + 2], sv[c + 3]);
         mx2 = fmax3(mx2, sv[c + 4], sv[c + 5]);
@@ -394,7 +421,12 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               rs1 = fadd2(rs1, pr);
             else
               rs0 = fadd2(rs0, pr);
-            pk[u] = pack_bf16(pr.x, pr.y);
+            if constexpr (kDrop) {  // dropped keys contribute no weight to O
+              const uint32_t kb = keep[q] >> (2 * u);
+              pk[u] = pack_bf16((kb & 1u) ? pr.x : 0.f, (kb & 2u) ? pr.y : 0.f);
+            } else {
+              pk[u] = pack_bf16(pr.x, pr.y);
+            }
           }
           tmem_st16(tS + 16 * q, pk);
         }
@@ -431,7 +463,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.o_full[t], 0, p.status, abort));
     if (ok) {
       tc_fence_after();
-      const float inv_l = (!kMask || l > 0.f) ? p.o_scale / l : 0.f;  // no visible key: O = 0
+      const float inv_l = (!kMask || l > 0.f) ? (kDrop ? p.drop_scale : p.o_scale) / l : 0.f;  // no visible key: O = 0
       __nv_bfloat16* orow = p.O + (size_t)(row_base + qrow) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -464,10 +496,15 @@ struct MaskArg {
   int64_t sb = 0, sh = 0, srow = 0;
 };
 
-template <int D, bool F8, bool kMask>
+struct DropArg {
+  uint64_t seed = 0;
+  uint32_t t = 0;
+};
+
+template <int D, bool F8, int kVar>
 cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
-                   float scale, float sl2, float o_scale, bool causal, const MaskArg& mask, int* status,
-                   cudaStream_t st) {
+                   float scale, float sl2, float o_scale, bool causal, const MaskArg& mask, const DropArg& drop,
+                   int* status, cudaStream_t st) {
   using C = FwdCfg<D, F8>;
   CUtensorMap mq, mk, mv;
   const int64_t heads = s.heads();
@@ -480,7 +517,7 @@ cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* 
            make_map_bf16_3d(&mv, V, heads, s.N, D, BN);
   if (!maps) return cudaErrorInvalidValue;
   static bool attr = [] {
-    return cudaFuncSetAttribute(fa_fwd_tc_kernel<D, F8, kMask>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(fa_fwd_tc_kernel<D, F8, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes) == cudaSuccess;
   }();
   if (!attr) return cudaErrorInvalidConfiguration;
@@ -501,8 +538,12 @@ cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.mask_srow = mask.srow;
   p.H = s.H;
   p.inv_scale = 1.f / scale;
+  p.seed_lo = (uint32_t)(drop.seed & 0xFFFFFFFFu);
+  p.seed_hi = (uint32_t)(drop.seed >> 32);
+  p.drop_t = drop.t;
+  p.drop_scale = (float)(65536.0 / (65536.0 - (double)drop.t));
   const int64_t grid = (int64_t)p.pairs * p.heads;
-  fa_fwd_tc_kernel<D, F8, kMask><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p);
+  fa_fwd_tc_kernel<D, F8, kVar><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -513,9 +554,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st) {
   const MaskArg none;
-  return s.d == 64 ? launch<64, false, false>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, none, status, st)
-                   : launch<128, false, false>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, none, status,
-                                               st);
+  const DropArg nodrop;
+  return s.d == 64
+             ? launch<64, false, 0>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, none, nodrop, status, st)
+             : launch<128, false, 0>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, none, nodrop, status, st);
 }
 
 cudaError_t tc_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
@@ -526,16 +568,31 @@ cudaError_t tc_fwd_masked(const void* Q, const void* K, const void* V, void* O, 
   m.sb = mask_sb;
   m.sh = mask_sh;
   m.srow = mask_srow;
-  return s.d == 64 ? launch<64, false, true>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, m, status, st)
-                   : launch<128, false, true>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, m, status, st);
+  const DropArg nodrop;
+  return s.d == 64
+             ? launch<64, false, 1>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, m, nodrop, status, st)
+             : launch<128, false, 1>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, m, nodrop, status, st);
+}
+
+cudaError_t tc_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                           float scale, bool causal, uint64_t seed, uint32_t threshold, int* status,
+                           cudaStream_t st) {
+  const MaskArg none;
+  DropArg dr;
+  dr.seed = seed;
+  dr.t = threshold;
+  return s.d == 64
+             ? launch<64, false, 2>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, none, dr, status, st)
+             : launch<128, false, 2>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, none, dr, status, st);
 }
 
 cudaError_t tc_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                        float scale, bool causal, float q_descale, float k_descale, float v_descale,
                        int* status, cudaStream_t st) {
   const MaskArg none;
-  return launch<128, true, false>(Q, K, V, O, LSE, s, scale, scale * kLog2e * q_descale * k_descale, v_descale,
-                                  causal, none, status, st);
+  const DropArg nodrop;
+  return launch<128, true, 0>(Q, K, V, O, LSE, s, scale, scale * kLog2e * q_descale * k_descale, v_descale,
+                              causal, none, nodrop, status, st);
 }
 
 }  // namespace fa

@@ -16,7 +16,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import exact_attention_02_gb300 as fa  # noqa: E402
-from exact_attention_02_gb300.workloads import WORKLOADS, Workload, make_inputs  # noqa: E402
+from exact_attention_02_gb300.workloads import round_to_bf16, WORKLOADS, Workload, make_inputs  # noqa: E402
 from oracle import attention as ora  # noqa: E402
 
 pytestmark = pytest.mark.gpu
@@ -146,6 +146,28 @@ def test_first_causal_row_sees_only_itself():
     assert np.abs(got["o"][0, 0, 0] - x["v"][0, 0, 0]).max() < 1e-2
     s00 = w.scale * float(np.dot(x["q"][0, 0, 0].astype(np.float64), x["k"][0, 0, 0]))
     assert abs(got["lse"][0, 0, 0] - s00) < 1e-3
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_first_causal_row_is_exactly_v0_for_any_score(d):
+    """Causal row 0 has one visible key, so its weight is exactly 1 and O_0 must equal the
+    bf16 row V_0 bit for bit, whatever the score's sign or size. A row max taken over
+    anything but that row's visible scores would make the stored weight 2^-delta, whose
+    bf16 rounding shows up here (it once did, for very negative scores)."""
+    torch = pytest.importorskip("torch")
+    import exact_attention_02_gb300 as fa
+    N = 256
+    rng = np.random.default_rng(40 + d)
+    k = round_to_bf16(rng.standard_normal((1, 1, N, d), dtype=np.float32))
+    v = round_to_bf16(rng.uniform(1, 2, (1, 1, N, d)).astype(np.float32))
+    for target in (-60.0, -40.0, -16.0, -12.0, -10.0, -3.0, 0.0, 5.0, 30.0):
+        q = rng.standard_normal((1, 1, N, d)).astype(np.float32)
+        k0 = k[0, 0, 0].astype(np.float64)
+        q[0, 0, 0] = (k0 * target / (k0 @ k0)).astype(np.float32)
+        q = round_to_bf16(q)
+        o, lse = fa.fa_fwd(*[torch.from_numpy(a).cuda().to(torch.bfloat16) for a in (q, k, v)], True)
+        torch.cuda.synchronize()
+        assert np.array_equal(o[0, 0, 0].float().cpu().numpy(), v[0, 0, 0]), target
 
 
 def test_repeat_runs_are_deterministic_for_fwd():
