@@ -67,6 +67,11 @@ def _load():
     L.fa_fwd_masked.restype = i
     L.fa_bwd_masked.argtypes = [vp] * 11 + [ll, ll, ll, vp, sz, i, i, i, i, f, i, i, vp]
     L.fa_bwd_masked.restype = i
+    ull = ctypes.c_ulonglong
+    L.fa_fwd_dropout.argtypes = [vp] * 5 + [i, i, i, i, f, i, f, ull, i, vp]
+    L.fa_fwd_dropout.restype = i
+    L.fa_bwd_dropout.argtypes = [vp] * 11 + [sz, i, i, i, i, f, i, f, ull, i, vp]
+    L.fa_bwd_dropout.restype = i
     L.fa_fwd_fp8.argtypes = [vp] * 5 + [i, i, i, i, f, i, f, f, f, vp]
     L.fa_fwd_fp8.restype = i
     L.fa_get_error_string.argtypes = [i]
@@ -154,16 +159,24 @@ def _mask_args(mask, q):
     return _p(mask), sb, sh, srow
 
 
-def fa_fwd(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None, stream=None, mask=None):
+def fa_fwd(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None, stream=None, mask=None,
+           dropout: tuple[float, int] | None = None):
     """O, LSE = attention forward of [B, H, N, d] CUDA tensors (see ``fa_fwd`` in fa.h).
     With ``mask`` (bf16 [B|1, H|1, N, N], added to the scaled scores) it calls
-    ``fa_fwd_masked``."""
+    ``fa_fwd_masked``; with ``dropout = (p, seed)`` it calls ``fa_fwd_dropout``."""
     import torch
     B, H, N, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _same(q, k, v, o)
+    if mask is not None and dropout is not None:
+        raise ValueError("a mask and dropout in one call are not supported")
+    if dropout is not None:
+        pd, seed = float(dropout[0]), int(dropout[1]) & 0xFFFFFFFFFFFFFFFF
+        _check(_load().fa_fwd_dropout(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d, scale, int(bool(causal)), pd,
+                                      seed, _dtype_code(q), _stream_ptr(stream)), "fa_fwd_dropout")
+        return o, lse
     if mask is not None:
         mp, sb, sh, srow = _mask_args(mask, q)
         _check(_load().fa_fwd_masked(_p(q), _p(k), _p(v), _p(o), _p(lse), mp, sb, sh, srow, B, H, N, d, scale,
@@ -192,9 +205,11 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int, dtype) -> int:
 
 
 def fa_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None, D=None,
-           dq=None, dk=None, dv=None, workspace=None, stream=None, mask=None):
+           dq=None, dk=None, dv=None, workspace=None, stream=None, mask=None,
+           dropout: tuple[float, int] | None = None):
     """dQ, dK, dV of attention from the forward's O and LSE (see ``fa_bwd`` in fa.h);
-    with ``mask`` (the forward's additive mask) it calls ``fa_bwd_masked``."""
+    with ``mask`` (the forward's additive mask) it calls ``fa_bwd_masked``, with
+    ``dropout`` (the forward's (p, seed)) ``fa_bwd_dropout``."""
     import torch
     B, H, N, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -206,6 +221,14 @@ def fa_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None, D=None
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if mask is not None and dropout is not None:
+        raise ValueError("a mask and dropout in one call are not supported")
+    if dropout is not None:
+        pd, seed = float(dropout[0]), int(dropout[1]) & 0xFFFFFFFFFFFFFFFF
+        _check(_load().fa_bwd_dropout(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(D), _p(dq), _p(dk), _p(dv),
+                                      _p(workspace), wbytes, B, H, N, d, scale, int(bool(causal)), pd, seed,
+                                      _dtype_code(q), _stream_ptr(stream)), "fa_bwd_dropout")
+        return dq, dk, dv
     if mask is not None:
         mp, sb, sh, srow = _mask_args(mask, q)
         _check(_load().fa_bwd_masked(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(D), _p(dq), _p(dk), _p(dv),

@@ -123,10 +123,24 @@ fa_status_t check_mask(const Mask& m, const Shape& s, int dtype) {
   return FA_OK;
 }
 
+struct Drop {
+  uint64_t seed;
+  uint32_t t;  // keep iff the 16-bit uniform >= t
+};
+
+// Dropout probability p in [0, 1) -> 16-bit keep threshold round(p * 65536), at most 65535.
+fa_status_t drop_threshold(float p, int dtype, uint32_t* t) {
+  if (!(isfinite(p) && p >= 0.f && p < 1.f)) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+  const double r = floor((double)p * 65536.0 + 0.5);
+  *t = (uint32_t)(r > 65535.0 ? 65535.0 : r);
+  return FA_OK;
+}
+
 fa_status_t bwd_common(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                        const float* LSE, const float* D, void* dQ, void* dK, void* dV, void* workspace,
                        size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal, int dtype,
-                       const Mask* mask, void* stream) {
+                       const Mask* mask, const Drop* drop, void* stream) {
   const Shape s{B, H, N, d};
   fa_status_t r = check_shape(s, dtype, &scale);
   if (r != FA_OK) return r;
@@ -154,6 +168,9 @@ fa_status_t bwd_common(const void* Q, const void* K, const void* V, const void* 
     if (mask)
       return from_cuda(tc_bwd_masked(Q, K, V, dO, LSE, D, dQ, dK, dV, acc, s, scale, causal == 1, mask->ptr,
                                      mask->sb, mask->sh, mask->srow, status, st));
+    if (drop)
+      return from_cuda(tc_bwd_dropout(Q, K, V, dO, LSE, D, dQ, dK, dV, acc, s, scale, causal == 1, drop->seed,
+                                      drop->t, status, st));
     return from_cuda(tc_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, acc, s, scale, causal == 1, status, st));
   }
   return from_cuda(simt_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal == 1, false, st));
@@ -168,7 +185,7 @@ extern "C" fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const
                               int H, int N, int d, float scale, int causal, int dtype,
                               void* stream) {
   return fa::bwd_common(Q, K, V, O, dO, LSE, D, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, scale, causal,
-                        dtype, nullptr, stream);
+                        dtype, nullptr, nullptr, stream);
 }
 
 extern "C" fa_status_t fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE,
@@ -196,7 +213,35 @@ extern "C" fa_status_t fa_bwd_masked(const void* Q, const void* K, const void* V
                                      int dtype, void* stream) {
   const fa::Mask m{mask, mask_stride_b, mask_stride_h, mask_stride_row};
   return fa::bwd_common(Q, K, V, O, dO, LSE, D, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, scale, causal,
-                        dtype, &m, stream);
+                        dtype, &m, nullptr, stream);
+}
+
+extern "C" fa_status_t fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                                      int H, int N, int d, float scale, int causal, float p_drop,
+                                      unsigned long long seed, int dtype, void* stream) {
+  const Shape s{B, H, N, d};
+  fa_status_t r = fa::check_shape(s, dtype, &scale);
+  if (r != FA_OK) return r;
+  if ((r = fa::check_ptrs({Q, K, V, O, LSE})) != FA_OK) return r;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  uint32_t t = 0;
+  if ((r = fa::drop_threshold(p_drop, dtype, &t)) != FA_OK) return r;
+  int* status = fa::device_status_ptr();
+  if (!status) return FA_ERR_CUDA;
+  return fa::from_cuda(fa::tc_fwd_dropout(Q, K, V, O, LSE, s, scale, causal == 1, (uint64_t)seed, t, status,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" fa_status_t fa_bwd_dropout(const void* Q, const void* K, const void* V, const void* O,
+                                      const void* dO, const float* LSE, const float* D, void* dQ, void* dK,
+                                      void* dV, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                                      float scale, int causal, float p_drop, unsigned long long seed, int dtype,
+                                      void* stream) {
+  fa::Drop dr{(uint64_t)seed, 0};
+  const fa_status_t r = fa::drop_threshold(p_drop, dtype, &dr.t);
+  if (r != FA_OK) return r;
+  return fa::bwd_common(Q, K, V, O, dO, LSE, D, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, scale, causal,
+                        dtype, nullptr, &dr, stream);
 }
 
 namespace {

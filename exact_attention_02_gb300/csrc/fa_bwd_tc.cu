@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
+#include "philox.cuh"
 #include "sm100_ptx.cuh"
 #include "tma_host.h"
 
@@ -111,6 +112,9 @@ struct BwdParams {
   const __nv_bfloat16* mask;
   int64_t mask_sb, mask_sh, mask_srow;
   int H;
+  // dropout (kVar == 2): Philox key, keep threshold and the scale of a kept weight
+  uint32_t seed_lo, seed_hi, drop_t;
+  float drop_scale;
 };
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -131,12 +135,15 @@ __device__ __forceinline__ uint32_t packed_col(uint32_t base, int k) {
 
 // kTail: N is not a multiple of the tiles, so the partial-tile guards are compiled in; the
 // instance for whole tiles carries none of them.
-template <int D, bool kTail, bool kMask>
+// kVar: 0 plain, 1 additive mask, 2 dropout.
+template <int D, bool kTail, int kVar>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                  const BwdParams p) {
   using C = BwdCfg<D>;
+  constexpr bool kMask = kVar == 1;
+  constexpr bool kDrop = kVar == 2;
   constexpr int BQ = C::BQ;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -412,6 +419,24 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                         : 0.f;
           }
         }
+        // kDrop: keep bits of this thread's key against the chunk's 32 queries. Lane L draws
+        // the bits of query (chunk start + L) against the warp's 32 keys (4 Philox blocks of
+        // 8 keys); 32 ballots transpose that 32 x 32 bit block, so lane T ends up with bit c
+        // = keep(query c, key T).
+        uint32_t kbits = 0;
+        if constexpr (kDrop) {
+          const uint32_t i = (uint32_t)(q0 + c0 + lane);
+          const uint32_t blk0 = (uint32_t)((kt * BN + (warp & 3) * 32) >> 3);
+          uint32_t row = 0;
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb)
+            row |= rng::keep8(blk0 + bb, i, (uint32_t)head, p.seed_lo, p.seed_hi, p.drop_t) << (8 * bb);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const uint32_t col = __ballot_sync(0xffffffffu, (row >> e) & 1u);
+            if (lane == e) kbits = col;
+          }
+        }
         float sv[32], dp[32];
         tmem_ld32x2(tmem + lane_off + C::colS(b) + c0, tmem + lane_off + C::colDP(b) + c0, sv, dp);
         // -LSE*log2(e) and D for the 32 columns, loaded as 16-byte vectors up front
@@ -442,9 +467,17 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             if (key > q0 + c) pr.x = 0.f;
             if (key > q0 + c + 1) pr.y = 0.f;
           }
-          const float2 dd = ffma2(dv[u], minus1, make_float2(dp[2 * u], dp[2 * u + 1]));
+          float2 dd;
+          if constexpr (kDrop) {  // dP of a dropped key is 0; a kept one is scaled
+            const bool k0 = (kbits >> (2 * u)) & 1u, k1 = (kbits >> (2 * u + 1)) & 1u;
+            dd = make_float2(k0 ? fmaf(dp[2 * u], p.drop_scale, -dv[u].x) : -dv[u].x,
+                             k1 ? fmaf(dp[2 * u + 1], p.drop_scale, -dv[u].y) : -dv[u].y);
+            pk[u] = pack_bf16(k0 ? pr.x : 0.f, k1 ? pr.y : 0.f);  // dV takes the kept weights
+          } else {
+            dd = ffma2(dv[u], minus1, make_float2(dp[2 * u], dp[2 * u + 1]));
+            pk[u] = pack_bf16(pr.x, pr.y);
+          }
           const float2 dsv = fmul2(pr, dd);
-          pk[u] = pack_bf16(pr.x, pr.y);
           dk[u] = pack_bf16(dsv.x, dsv.y);
         }
         // bf16 P^T over S^T and dS^T over dP^T, in columns this warpgroup has already read
@@ -529,8 +562,9 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         uint4 w[4];
         uint32_t* wu = reinterpret_cast<uint32_t*>(w);
         tmem_ld32(tmem + lane_off + C::kColDV + c0, v);
+        const float vs = kDrop ? p.drop_scale : 1.f;  // kept weights entered dV unscaled
 #pragma unroll
-        for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
+        for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u] * vs, v[2 * u + 1] * vs);
         uint4* dv = reinterpret_cast<uint4*>(p.dV + row * D + c0);
         if (in) {
 #pragma unroll
@@ -577,10 +611,16 @@ struct MaskArg {
   int64_t sb = 0, sh = 0, srow = 0;
 };
 
-template <int D, bool kMask>
+struct DropArg {
+  uint64_t seed = 0;
+  uint32_t t = 0;
+};
+
+template <int D, int kVar>
 cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                    const float* Dv, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
-                   float scale, bool causal, const MaskArg& mask, int* status, cudaStream_t st) {
+                   float scale, bool causal, const MaskArg& mask, const DropArg& drop, int* status,
+                   cudaStream_t st) {
   using C = BwdCfg<D>;
   CUtensorMap mq, mk, mv, mdo;
   const int64_t heads = s.heads();
@@ -588,9 +628,9 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
       !make_map_bf16_3d(&mv, V, heads, s.N, D, BN) || !make_map_bf16_3d(&mdo, dO, heads, s.N, D, C::BQ))
     return cudaErrorInvalidValue;
   static bool attr = [] {
-    return cudaFuncSetAttribute(fa_bwd_tc_kernel<D, false, kMask>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(fa_bwd_tc_kernel<D, false, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes) == cudaSuccess &&
-           cudaFuncSetAttribute(fa_bwd_tc_kernel<D, true, kMask>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+           cudaFuncSetAttribute(fa_bwd_tc_kernel<D, true, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes) == cudaSuccess;
   }();
   if (!attr) return cudaErrorInvalidConfiguration;
@@ -615,11 +655,15 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
   p.mask_sh = mask.sh;
   p.mask_srow = mask.srow;
   p.H = s.H;
+  p.seed_lo = (uint32_t)(drop.seed & 0xFFFFFFFFu);
+  p.seed_hi = (uint32_t)(drop.seed >> 32);
+  p.drop_t = drop.t;
+  p.drop_scale = (float)(65536.0 / (65536.0 - (double)drop.t));
   const int64_t grid = (int64_t)p.kvtiles * p.heads;
   if (s.N % 128 != 0)
-    fa_bwd_tc_kernel<D, true, kMask><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
+    fa_bwd_tc_kernel<D, true, kVar><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
   else
-    fa_bwd_tc_kernel<D, false, kMask><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
+    fa_bwd_tc_kernel<D, false, kVar><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t n8 = s.elems() / 8;
   dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(dQacc, static_cast<__nv_bfloat16*>(dQ),
@@ -633,8 +677,10 @@ cudaError_t tc_bwd(const void* Q, const void* K, const void* V, const void* dO, 
                    const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st) {
   const MaskArg none;
-  return s.d == 64 ? launch<64, false>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, none, status, st)
-                   : launch<128, false>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, none, status, st);
+  const DropArg nodrop;
+  return s.d == 64
+             ? launch<64, 0>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, none, nodrop, status, st)
+             : launch<128, 0>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, none, nodrop, status, st);
 }
 
 cudaError_t tc_bwd_masked(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
@@ -646,8 +692,23 @@ cudaError_t tc_bwd_masked(const void* Q, const void* K, const void* V, const voi
   m.sb = mask_sb;
   m.sh = mask_sh;
   m.srow = mask_srow;
-  return s.d == 64 ? launch<64, true>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, m, status, st)
-                   : launch<128, true>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, m, status, st);
+  const DropArg nodrop;
+  return s.d == 64
+             ? launch<64, 1>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, m, nodrop, status, st)
+             : launch<128, 1>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, m, nodrop, status, st);
+}
+
+cudaError_t tc_bwd_dropout(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                           const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
+                           float scale, bool causal, uint64_t seed, uint32_t threshold, int* status,
+                           cudaStream_t st) {
+  const MaskArg none;
+  DropArg dr;
+  dr.seed = seed;
+  dr.t = threshold;
+  return s.d == 64
+             ? launch<64, 2>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, none, dr, status, st)
+             : launch<128, 2>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, none, dr, status, st);
 }
 
 }  // namespace fa

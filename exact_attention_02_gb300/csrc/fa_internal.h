@@ -36,6 +36,11 @@ cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* 
 cudaError_t tc_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                           float scale, bool causal, const void* mask, int64_t mask_sb, int64_t mask_sh,
                           int64_t mask_srow, int* status, cudaStream_t st);
+// bf16 forward with dropout: Philox-4x32-10 keep bits keyed by `seed`, kept iff the 16-bit
+// uniform is >= threshold; kept weights scaled by 65536 / (65536 - threshold).
+cudaError_t tc_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                           float scale, bool causal, uint64_t seed, uint32_t threshold, int* status,
+                           cudaStream_t st);
 // e4m3 Q, K, V (d = 128) with per-tensor dequantisation factors; O bf16, LSE fp32.
 cudaError_t tc_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                        float scale, bool causal, float q_descale, float k_descale, float v_descale,
@@ -50,6 +55,12 @@ cudaError_t tc_bwd_masked(const void* Q, const void* K, const void* V, const voi
                           const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
                           float scale, bool causal, const void* mask, int64_t mask_sb, int64_t mask_sh,
                           int64_t mask_srow, int* status, cudaStream_t st);
+
+// The backward with the dropout of tc_fwd_dropout (same seed and threshold).
+cudaError_t tc_bwd_dropout(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                           const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
+                           float scale, bool causal, uint64_t seed, uint32_t threshold, int* status,
+                           cudaStream_t st);
 
 // ---- split-KV forward for few queries (fa_splitkv.cu): bf16, d in {64, 128}, Nq <= 16 ----
 size_t splitkv_workspace_floats(int64_t heads, int Nq, int Nk, int d);

@@ -176,6 +176,30 @@ FA_API fa_status_t fa_bwd_masked(const void* Q, const void* K, const void* V, co
                                  int causal, int dtype, void* stream);
 
 /*
+ * fa_fwd_dropout / fa_bwd_dropout — fa_fwd / fa_bwd with dropout on the attention weights
+ * ("知识点13 FlashAttention深度攻略" §7 算子融合优化: dropout is fused into the softmax step):
+ *      O = (P o K c) V,  P = softmax of the scores, K the 0/1 keep matrix, c its scale.
+ * LSE is the undropped softmax's. The backward is the exact gradient of that O for the
+ *      same K: pass the same p_drop and seed to both calls (and D from the dropped O).
+ * Keep bits: Philox-4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3",
+ *      SC 2011). Element (query i, key j) of head h = b*H + head takes the 16-bit half
+ *      j % 2 of word (j % 8) / 2 of Philox(counter (j / 8, i, h, 0), key (seed & 0xffffffff,
+ *      seed >> 32)); the key is kept iff that value >= t = min(65535, round(p_drop * 65536)),
+ *      and c = 65536 / (65536 - t): the probability is quantised to a multiple of 2^-16
+ *      and every weight keeps its expected value exactly.
+ * p_drop: finite, 0 <= p_drop < 1 (else FA_ERR_INVALID_ARG); dtype must be FA_DTYPE_BF16
+ *      (else FA_ERR_UNSUPPORTED). The remaining arguments are those of fa_fwd / fa_bwd.
+ */
+FA_API fa_status_t fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                                  int H, int N, int d, float scale, int causal, float p_drop,
+                                  unsigned long long seed, int dtype, void* stream);
+FA_API fa_status_t fa_bwd_dropout(const void* Q, const void* K, const void* V, const void* O,
+                                  const void* dO, const float* LSE, const float* D, void* dQ, void* dK,
+                                  void* dV, void* workspace, size_t workspace_bytes, int B, int H, int N,
+                                  int d, float scale, int causal, float p_drop, unsigned long long seed,
+                                  int dtype, void* stream);
+
+/*
  * fa_fwd_fp8 — the forward of fa_fwd on 8-bit inputs ("flash-attention" (data.6616ai.com),
  * 参考答案: FlashAttention-3 runs on FP8; "知识点13" 前沿研究方向: mixed precision with FP8).
  * In:  Q, K, V [B,H,N,d] as e4m3 bytes (OCP FP8 E4M3: 1 sign, 4 exponent bits with bias 7,

@@ -30,7 +30,8 @@ def _declared():
 def test_header_declares_the_boundary():
     assert set(_declared()) >= {"fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_bwd_workspace_size",
                                 "fa_get_error_string", "fa_get_last_device_status", "fa_fwd_splitkv",
-                                "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked"}
+                                "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked",
+                                "fa_fwd_dropout", "fa_bwd_dropout"}
 
 
 def test_exports_every_declared_symbol(lib):
@@ -174,4 +175,20 @@ def test_masked_rejects_before_launch(lib):
     assert call(sb=-8) == fa.FA_ERR_INVALID_ARG
     assert call(sh=4) == fa.FA_ERR_INVALID_ARG
     assert call(dtype=1) == fa.FA_ERR_UNSUPPORTED           # the fp32 path has no mask
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_dropout_rejects_before_launch(lib):
+    """Host-side checks of the dropout rate (dummy pointers; nothing is launched)."""
+    import exact_attention_02_gb300 as fa
+    vp, f, i = ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+    L = fa.lib()
+
+    def call(p=0.1, dtype=0, d=64):
+        return L.fa_fwd_dropout(vp(P), vp(P), vp(P), vp(P), vp(P), 1, 1, 128, d, f(0.125), 0, f(p),
+                                ctypes.c_ulonglong(1), dtype, None)
+    assert call(p=1.0) == fa.FA_ERR_INVALID_ARG
+    assert call(p=-0.1) == fa.FA_ERR_INVALID_ARG
+    assert call(p=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert call(dtype=1) == fa.FA_ERR_UNSUPPORTED
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
