@@ -72,6 +72,10 @@ def _load():
     L.fa_fwd_dropout.restype = i
     L.fa_bwd_dropout.argtypes = [vp] * 11 + [sz, i, i, i, i, f, i, f, ull, i, vp]
     L.fa_bwd_dropout.restype = i
+    L.fa_fwd_bwd_host_workspace_size.argtypes = [i, i, i, i, i, i]
+    L.fa_fwd_bwd_host_workspace_size.restype = sz
+    L.fa_fwd_bwd_host.argtypes = [vp] * 10 + [sz, i, i, i, i, f, i, i, i, vp]
+    L.fa_fwd_bwd_host.restype = i
     L.fa_fwd_fp8.argtypes = [vp] * 5 + [i, i, i, i, f, i, f, f, f, vp]
     L.fa_fwd_fp8.restype = i
     L.fa_get_error_string.argtypes = [i]
@@ -282,6 +286,38 @@ def fa_fwd_fp8(q8, k8, v8, descale, causal: bool, scale: float | None = None, o=
     _check(_load().fa_fwd_fp8(_p(q8), _p(k8), _p(v8), _p(o), _p(lse), B, H, N, d, scale, int(bool(causal)),
                               qd, kd, vd, _stream_ptr(stream)), "fa_fwd_fp8")
     return o, lse
+
+
+def fa_fwd_bwd_host_workspace_size(B: int, H: int, N: int, d: int, chunks: int = 0) -> int:
+    return int(_load().fa_fwd_bwd_host_workspace_size(B, H, N, d, FA_DTYPE_BF16, chunks))
+
+
+def fa_fwd_bwd_host(q, k, v, do, causal: bool, scale: float | None = None, out=None, chunks: int = 0,
+                    workspace=None, stream=None):
+    """Forward + backward of host-resident bf16 tensors q, k, v, do [B,H,N,d] (page-locked
+    for overlap; see ``fa_fwd_bwd_host`` in fa.h). Returns host (o, lse, dq, dk, dv); they
+    hold the results once ``stream`` (default: the current stream) has been synchronised.
+    ``out`` may pass preallocated host tensors in that order."""
+    import torch
+    B, H, N, d = _shape(q)
+    for t in (q, k, v, do):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("q, k, v, do must be contiguous bf16 host tensors of one shape")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        pin = torch.cuda.is_available()
+        out = (torch.empty_like(q, pin_memory=pin), torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin),
+               torch.empty_like(q, pin_memory=pin), torch.empty_like(q, pin_memory=pin),
+               torch.empty_like(q, pin_memory=pin))
+    need = fa_fwd_bwd_host_workspace_size(B, H, N, d, chunks)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    wbytes = workspace.numel() * workspace.element_size()
+    o, lse, dq, dk, dv = out
+    _check(_load().fa_fwd_bwd_host(_p(q), _p(k), _p(v), _p(do), _p(o), _p(lse), _p(dq), _p(dk), _p(dv), _p(workspace),
+                                   wbytes, B, H, N, d, scale, int(bool(causal)), FA_DTYPE_BF16, int(chunks),
+                                   _stream_ptr(stream)), "fa_fwd_bwd_host")
+    return out
 
 
 def fa_get_last_device_status() -> int:

@@ -219,6 +219,31 @@ FA_API fa_status_t fa_fwd_fp8(const void* Q, const void* K, const void* V, void*
                               int B, int H, int N, int d, float scale, int causal, float q_descale,
                               float k_descale, float v_descale, void* stream);
 
+/*
+ * fa_fwd_bwd_host — forward and backward of tensors that live in host memory: the
+ * copies to and from the device overlap the kernels. The heads (independent of one
+ * another) are cut into `chunks` contiguous groups (0 = 4; at most 16 and at most B*H);
+ * each group is copied in (Q, K, V, dO), run through fa_fwd, fa_bwd_preprocess and fa_bwd,
+ * and copied out (O, LSE, dQ, dK, dV) on three internal streams, with two device slots
+ * in `workspace` alternating, so one group's copies run while another's kernels do.
+ * In:  Q, K, V, dO host [B,H,N,d] bf16 (page-locked memory, e.g. cudaHostAlloc, lets
+ *      the copies run asynchronously; pageable memory works but serialises them).
+ * Out: O host [B,H,N,d] bf16, LSE host [B,H,N] fp32, dQ, dK, dV host [B,H,N,d] bf16.
+ * workspace: device buffer of at least fa_fwd_bwd_host_workspace_size(...) bytes,
+ *      256-byte aligned; its contents on entry do not matter.
+ * stream: the work starts after what is already queued on `stream`, and `stream` waits
+ *      for all of it: the outputs are in host memory once `stream` has been synchronised.
+ *      The call itself does not block.
+ * Supported: bf16, d in {64, 128}, causal 0/1, B*H*N < 2^31 (else FA_ERR_UNSUPPORTED).
+ * Errors: as for fa_fwd / fa_bwd; a failure returned after some work was enqueued leaves
+ *      that work running: synchronise the device before reusing the buffers.
+ */
+FA_API size_t fa_fwd_bwd_host_workspace_size(int B, int H, int N, int d, int dtype, int chunks);
+FA_API fa_status_t fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const void* dO, void* O,
+                                   float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                                   size_t workspace_bytes, int B, int H, int N, int d, float scale,
+                                   int causal, int dtype, int chunks, void* stream);
+
 /* Text for a status code (static storage; never NULL). */
 FA_API const char* fa_get_error_string(fa_status_t status);
 
