@@ -44,6 +44,14 @@ CASES = [  # B, H, Nq, Nk, d, causal, qk_gain
     # 1000 heads of 5 keys: dozens of short segments per CTA
     (10, 100, 2, 5, 128, True, 1.0),
     (1, 2, 12, 4096, 128, True, 2.0),
+    # d = 128 with 2..64 queries: the tensor-core partial kernel
+    (1, 4, 32, 4096, 128, True, 1.0),
+    (2, 2, 64, 3000, 128, False, 1.0),
+    (1, 2, 2, 1000, 128, True, 2.0),
+    (1, 1, 40, 257, 128, True, 1.0),
+    (4, 8, 8, 600, 128, True, 4.0),      # peaky scores: the running max moves often
+    (1, 1, 64, 100000, 128, True, 1.0),  # one head over ~150 CTAs
+    (10, 100, 3, 5, 128, True, 1.0),     # dozens of short segments per CTA
 ]
 
 
