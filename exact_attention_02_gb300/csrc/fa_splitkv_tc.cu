@@ -48,10 +48,10 @@ constexpr int kTileBytes = 2 * kBoxBytes;     // one K or V tile (d = 128)
 constexpr int kQBox = NQP * 128;              // [64 rows x 64 bf16]
 constexpr int kQBytes = 2 * kQBox;
 constexpr int kPBytes = BN * NQP * 2;         // P^T [128 keys x 64 queries] bf16
-constexpr int kStages = 2;
+constexpr int kKStages = 3, kVStages = 2;  // K is read a tile before V, so it gets the deeper ring
 constexpr int kKOff = 0;
-constexpr int kVOff = kKOff + kStages * kTileBytes;
-constexpr int kQOff = kVOff + kStages * kTileBytes;
+constexpr int kVOff = kKOff + kKStages * kTileBytes;
+constexpr int kQOff = kVOff + kVStages * kTileBytes;
 constexpr int kPOff = kQOff + kQBytes;
 constexpr int kCorrOff = kPOff + 2 * kPBytes;       // float[64] rescale factors
 constexpr int kMOff = kCorrOff + 4 * NQP;           // float[64] running max per query (log2 units)
@@ -89,7 +89,7 @@ struct TcParams {
 };
 
 struct Ctl {
-  uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
+  uint64_t k_full[kKStages], v_full[kVStages], k_empty[kKStages], v_empty[kVStages];
   uint64_t q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_free, drain;
   uint32_t tmem_base;
   int abort;
@@ -122,10 +122,12 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   const int64_t g_end = min(p.total, g_begin + p.L);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&ctl.k_full[s], 1);
-      mbar_init(&ctl.v_full[s], 1);
       mbar_init(&ctl.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&ctl.v_full[s], 1);
       mbar_init(&ctl.v_empty[s], 1);
     }
     mbar_init(&ctl.q_full, 1);
@@ -156,7 +158,9 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       prefetch_tmap(&tmQ);
       SegIter it{g_begin, g_end, p.Nk};
       int64_t h;
-      int k0, k1, seg = 0, t = 0, last_k[kStages] = {-1, -1}, last_v[kStages] = {-1, -1}, last_q = -1;
+      int k0, k1, seg = 0, t = 0, last_k[kKStages], last_v[kVStages], last_q = -1;
+      for (int s = 0; s < kKStages; ++s) last_k[s] = -1;
+      for (int s = 0; s < kVStages; ++s) last_v[s] = -1;
       bool ok = true;
       while (ok && it.next(h, k0, k1)) {
         // Q of this head, once the previous segment's S products have read the old one
@@ -165,27 +169,28 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         for (int b = 0; b < 2; ++b) tma_load_3d(smem + kQOff + b * kQBox, &tmQ, &ctl.q_full, b * 64, 0, (int)h);
         last_q = seg;
         for (int kt = k0; ok && kt < k1; kt += BN, ++t) {
-          const int s = t % kStages;
-          const uint32_t ph = ((t / kStages) - 1) & 1;
-          if (t >= kStages && !(ok = mbar_wait(&ctl.k_empty[s], ph, p.status, abort))) break;
-          mbar_expect_tx(&ctl.k_full[s], kTileBytes);
+          const int sk = t % kKStages, sv = t % kVStages;
+          if (t >= kKStages && !(ok = mbar_wait(&ctl.k_empty[sk], ((t / kKStages) - 1) & 1, p.status, abort)))
+            break;
+          mbar_expect_tx(&ctl.k_full[sk], kTileBytes);
           for (int b = 0; b < 2; ++b)
-            tma_load_3d(smem + kKOff + s * kTileBytes + b * kBoxBytes, &tmK, &ctl.k_full[s], b * 64, kt, (int)h);
-          last_k[s] = t;
-          if (t >= kStages && !(ok = mbar_wait(&ctl.v_empty[s], ph, p.status, abort))) break;
-          mbar_expect_tx(&ctl.v_full[s], kTileBytes);
+            tma_load_3d(smem + kKOff + sk * kTileBytes + b * kBoxBytes, &tmK, &ctl.k_full[sk], b * 64, kt, (int)h);
+          last_k[sk] = t;
+          if (t >= kVStages && !(ok = mbar_wait(&ctl.v_empty[sv], ((t / kVStages) - 1) & 1, p.status, abort)))
+            break;
+          mbar_expect_tx(&ctl.v_full[sv], kTileBytes);
           for (int b = 0; b < 2; ++b)
-            tma_load_3d(smem + kVOff + s * kTileBytes + b * kBoxBytes, &tmV, &ctl.v_full[s], b * 64, kt, (int)h);
-          last_v[s] = t;
+            tma_load_3d(smem + kVOff + sv * kTileBytes + b * kBoxBytes, &tmV, &ctl.v_full[sv], b * 64, kt, (int)h);
+          last_v[sv] = t;
         }
         ++seg;
       }
       // every issued copy lands before the CTA may exit
       if (last_q >= 0) mbar_wait(&ctl.q_full, last_q & 1, p.status, nullptr);
-      for (int s = 0; s < kStages; ++s) {
-        if (last_k[s] >= 0) mbar_wait(&ctl.k_full[s], (last_k[s] / kStages) & 1, p.status, nullptr);
-        if (last_v[s] >= 0) mbar_wait(&ctl.v_full[s], (last_v[s] / kStages) & 1, p.status, nullptr);
-      }
+      for (int s = 0; s < kKStages; ++s)
+        if (last_k[s] >= 0) mbar_wait(&ctl.k_full[s], (last_k[s] / kKStages) & 1, p.status, nullptr);
+      for (int s = 0; s < kVStages; ++s)
+        if (last_v[s] >= 0) mbar_wait(&ctl.v_full[s], (last_v[s] / kVStages) & 1, p.status, nullptr);
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
@@ -197,7 +202,7 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       const uint64_t dV0 = sdesc_sw128(smem_u32(smem + kVOff), kBoxBytes, 1024);
       const uint64_t dP0 = sdesc_sw128(smem_u32(smem + kPOff), kPBytes, 1024);
       auto issue_S = [&](int t) {
-        const uint32_t ko = (t % kStages) * kTileBytes;
+        const uint32_t ko = (t % kKStages) * kTileBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32, qoff = (k / 4) * kQBox + (k % 4) * 32;
@@ -205,7 +210,7 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
       };
       auto issue_PV = [&](int t, bool acc) {
-        const uint32_t vo = (t % kStages) * kTileBytes, po = (t & 1) * kPBytes;
+        const uint32_t vo = (t % kVStages) * kTileBytes, po = (t & 1) * kPBytes;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
           mma_ss(tmem + kColO, sdesc_add(dV0, vo + k * 2048), sdesc_add(dP0, po + k * 2048), idO,
@@ -218,28 +223,29 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       while (ok && it.next(h, k0, k1)) {
         const int n = (k1 - k0 + BN - 1) / BN;  // tiles in this segment: t .. t + n - 1
         if (!(ok = mbar_wait(&ctl.q_full, seg & 1, p.status, abort))) break;
-        if (!(ok = mbar_wait(&ctl.k_full[t % kStages], (t / kStages) & 1, p.status, abort))) break;
+        if (!(ok = mbar_wait(&ctl.k_full[t % kKStages], (t / kKStages) & 1, p.status, abort))) break;
         tc_fence_after();
         issue_S(t);
-        mma_commit(&ctl.k_empty[t % kStages]);
+        mma_commit(&ctl.k_empty[t % kKStages]);
         mma_commit(&ctl.s_full[t & 1]);
         for (int i = 0; i < n; ++i, ++t) {
           if (i + 1 < n) {  // S of the next tile into the other buffer (read out by tile t-1's softmax)
             if (t >= 1 && !(ok = mbar_wait(&ctl.p_full[(t + 1) & 1], ((t - 1) >> 1) & 1, p.status, abort))) break;
-            if (!(ok = mbar_wait(&ctl.k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1, p.status, abort))) break;
+            if (!(ok = mbar_wait(&ctl.k_full[(t + 1) % kKStages], ((t + 1) / kKStages) & 1, p.status, abort)))
+              break;
             tc_fence_after();
             issue_S(t + 1);
-            mma_commit(&ctl.k_empty[(t + 1) % kStages]);
+            mma_commit(&ctl.k_empty[(t + 1) % kKStages]);
             mma_commit(&ctl.s_full[(t + 1) & 1]);
           } else {
             mma_commit(&ctl.q_empty);  // every S of the segment is issued: Q may be replaced
           }
           if (!(ok = mbar_wait(&ctl.p_full[t & 1], (t >> 1) & 1, p.status, abort))) break;
-          if (!(ok = mbar_wait(&ctl.v_full[t % kStages], (t / kStages) & 1, p.status, abort))) break;
+          if (!(ok = mbar_wait(&ctl.v_full[t % kVStages], (t / kVStages) & 1, p.status, abort))) break;
           if (i == 0 && seg > 0 && !(ok = mbar_wait(&ctl.o_free, (seg - 1) & 1, p.status, abort))) break;
           tc_fence_after();
           issue_PV(t, i > 0);
-          mma_commit(&ctl.v_empty[t % kStages]);
+          mma_commit(&ctl.v_empty[t % kVStages]);
           mma_commit(&ctl.pv_done[t & 1]);
         }
         ++seg;
