@@ -152,45 +152,48 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 
   if (warp == kLoadWarp) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      prefetch_tmap(&tmQ);
+    // Lane 0 streams Q and K, lane 1 streams V: a K slot frees a tile before the V slot of
+    // the same tile, so the two rings advance independently.
+    if (lane < 2) {
+      const bool kq = lane == 0;
+      if (kq) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmQ);
+      } else {
+        prefetch_tmap(&tmV);
+      }
+      constexpr int kMaxStages = kKStages > kVStages ? kKStages : kVStages;
+      const int stages = kq ? kKStages : kVStages;
+      uint64_t* full = kq ? ctl.k_full : ctl.v_full;
+      uint64_t* empty = kq ? ctl.k_empty : ctl.v_empty;
+      const CUtensorMap* map = kq ? &tmK : &tmV;
+      uint8_t* ring = smem + (kq ? kKOff : kVOff);
       SegIter it{g_begin, g_end, p.Nk};
       int64_t h;
-      int k0, k1, seg = 0, t = 0, last_k[kKStages], last_v[kVStages], last_q = -1;
-      for (int s = 0; s < kKStages; ++s) last_k[s] = -1;
-      for (int s = 0; s < kVStages; ++s) last_v[s] = -1;
+      int k0, k1, seg = 0, t = 0, last[kMaxStages], last_q = -1;
+      for (int s = 0; s < kMaxStages; ++s) last[s] = -1;
       bool ok = true;
       while (ok && it.next(h, k0, k1)) {
-        // Q of this head, once the previous segment's S products have read the old one
-        if (seg > 0 && !(ok = mbar_wait(&ctl.q_empty, (seg - 1) & 1, p.status, abort))) break;
-        mbar_expect_tx(&ctl.q_full, kQBytes);
-        for (int b = 0; b < 2; ++b) tma_load_3d(smem + kQOff + b * kQBox, &tmQ, &ctl.q_full, b * 64, 0, (int)h);
-        last_q = seg;
+        if (kq) {  // Q of this head, once the previous segment's S products have read the old one
+          if (seg > 0 && !(ok = mbar_wait(&ctl.q_empty, (seg - 1) & 1, p.status, abort))) break;
+          mbar_expect_tx(&ctl.q_full, kQBytes);
+          for (int b = 0; b < 2; ++b) tma_load_3d(smem + kQOff + b * kQBox, &tmQ, &ctl.q_full, b * 64, 0, (int)h);
+          last_q = seg;
+        }
         for (int kt = k0; ok && kt < k1; kt += BN, ++t) {
-          const int sk = t % kKStages, sv = t % kVStages;
-          if (t >= kKStages && !(ok = mbar_wait(&ctl.k_empty[sk], ((t / kKStages) - 1) & 1, p.status, abort)))
-            break;
-          mbar_expect_tx(&ctl.k_full[sk], kTileBytes);
+          const int s = t % stages;
+          if (t >= stages && !(ok = mbar_wait(&empty[s], ((t / stages) - 1) & 1, p.status, abort))) break;
+          mbar_expect_tx(&full[s], kTileBytes);
           for (int b = 0; b < 2; ++b)
-            tma_load_3d(smem + kKOff + sk * kTileBytes + b * kBoxBytes, &tmK, &ctl.k_full[sk], b * 64, kt, (int)h);
-          last_k[sk] = t;
-          if (t >= kVStages && !(ok = mbar_wait(&ctl.v_empty[sv], ((t / kVStages) - 1) & 1, p.status, abort)))
-            break;
-          mbar_expect_tx(&ctl.v_full[sv], kTileBytes);
-          for (int b = 0; b < 2; ++b)
-            tma_load_3d(smem + kVOff + sv * kTileBytes + b * kBoxBytes, &tmV, &ctl.v_full[sv], b * 64, kt, (int)h);
-          last_v[sv] = t;
+            tma_load_3d(ring + s * kTileBytes + b * kBoxBytes, map, &full[s], b * 64, kt, (int)h);
+          last[s] = t;
         }
         ++seg;
       }
       // every issued copy lands before the CTA may exit
       if (last_q >= 0) mbar_wait(&ctl.q_full, last_q & 1, p.status, nullptr);
-      for (int s = 0; s < kKStages; ++s)
-        if (last_k[s] >= 0) mbar_wait(&ctl.k_full[s], (last_k[s] / kKStages) & 1, p.status, nullptr);
-      for (int s = 0; s < kVStages; ++s)
-        if (last_v[s] >= 0) mbar_wait(&ctl.v_full[s], (last_v[s] / kVStages) & 1, p.status, nullptr);
+      for (int s = 0; s < stages; ++s)
+        if (last[s] >= 0) mbar_wait(&full[s], (last[s] / stages) & 1, p.status, nullptr);
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
