@@ -8,17 +8,26 @@
 //
 // Per 128-key tile (keys on the MMA's M side, queries on N, padded to 64 with zero rows):
 //   S^T = K Q^T           M = 128 keys, N = 64, K = d: one TMEM accumulator [keys x queries]
-//   softmax               4 warps, one thread per key (= TMEM lane): scores in log2 units,
-//                         masked keys -inf; per query a running max m_q, refreshed only when
-//                         some score exceeds it by more than 2^8 (then O^T and the row sums
-//                         are rescaled); p = 2^(s - m_q) <= 256 written as bf16 P^T rows to
-//                         a 128-byte-swizzled shared-memory tile
+//   softmax               one thread per (key = TMEM lane, query group): scores in log2
+//                         units, masked keys -inf; per query a running max m_q, refreshed
+//                         only when some score exceeds it by more than 2^8 (then O^T and the
+//                         row sums are rescaled); p = 2^(s - m_q) <= 256 written as bf16 P^T
+//                         rows to a 128-byte-swizzled shared-memory tile. m_q starts at the
+//                         finite -1e30, so no score needs a test for -inf: the first visible
+//                         score always triggers a refresh, and a masked one gives 2^-inf = 0.
+//                         A tile that no key bound or causal rule touches for the group skips
+//                         the masking altogether.
 //   O^T += V^T P^T        M = 128 (d), N = 64, K = 128 keys: A = the V tile read MN-major,
 //                         B = P^T (MN-major), accumulator O^T [d x queries] in TMEM
 // Row sums stay per thread (64 partial sums) and are reduced once per segment. An N = 64
 // product costs the same issue slot as N = 16, so the padding costs nothing.
 //
-// Roles: warps 0-3 softmax and epilogue, warp 4 TMA producer, warp 5 MMA issuer.
+// Roles: warps 0-7 softmax and epilogue, warp 8 TMA producer (lane 0 Q and K, lane 1 V),
+// warp 9 MMA issuer. The softmax warps form two groups of four; group g owns the query
+// columns g*C .. g*C + C - 1 (C = 8, 16 or 32, the smallest with 2C >= N_q), keeps their
+// running maxima and synchronises on its own named barrier. Warp w reads TMEM lanes
+// 32*(w%4)..+31, so both groups see every key. A group without queries sits out, and the
+// barriers it would arrive on count only the groups that have queries.
 // Rows: K/V through 3-D maps [heads, N_k, d] (rows past the end of a head read as zeros),
 // Q through [heads, N_q, d] with 64-row boxes (rows past N_q read as zeros).
 #include <cuda_bf16.h>
@@ -39,9 +48,11 @@ constexpr int kMinKeys = 256;
 constexpr int BN = 128;  // keys per tile
 constexpr int D = 128;
 constexpr int NQP = 64;  // queries padded to the MMA's N
-constexpr int kThreads = 192;
-constexpr int kLoadWarp = 4, kMmaWarp = 5;
+constexpr int kSoftThreads = 256;  // two groups of four softmax warps
+constexpr int kThreads = kSoftThreads + 64;
+constexpr int kLoadWarp = 8, kMmaWarp = 9;
 constexpr float kThreshold = 8.f;
+constexpr float kNegM0 = 1e30f;  // -m of a query before its first visible score
 
 constexpr int kBoxBytes = BN * 128;           // [128 rows x 64 bf16]
 constexpr int kTileBytes = 2 * kBoxBytes;     // one K or V tile (d = 128)
@@ -54,10 +65,11 @@ constexpr int kVOff = kKOff + kKStages * kTileBytes;
 constexpr int kQOff = kVOff + kVStages * kTileBytes;
 constexpr int kPOff = kQOff + kQBytes;
 constexpr int kCorrOff = kPOff + 2 * kPBytes;       // float[64] rescale factors
-constexpr int kMOff = kCorrOff + 4 * NQP;           // float[64] running max per query (log2 units)
-constexpr int kRedOff = kMOff + 4 * NQP;            // float[4][64] cross-warp scratch
-constexpr int kFlagOff = kRedOff + 4 * 4 * NQP;     // int[2][4] per-warp flags, by tile parity
-constexpr int kSmemBytes = kFlagOff + 32 + 1024;
+constexpr int kNmOff = kCorrOff + 4 * NQP;          // float[64] -m per query (log2 units)
+constexpr int kNmtOff = kNmOff + 4 * NQP;           // float[64] -(m + threshold) per query
+constexpr int kRedOff = kNmtOff + 4 * NQP;          // float[4][64] cross-warp scratch
+constexpr int kFlagOff = kRedOff + 4 * 4 * NQP;     // int[2][8] per-warp flags, by tile parity
+constexpr int kSmemBytes = kFlagOff + 64 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 constexpr uint32_t kColS0 = 0, kColO = 2 * NQP;  // S buffers [0,128), O^T [128,192)
@@ -95,7 +107,41 @@ struct Ctl {
   int abort;
 };
 
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier of softmax group g (barrier 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); }
+
+// kN consecutive fp32 columns of this thread's TMEM lane (kN = 8, 16 or 32); the load and
+// its wait form one statement, so no use of the values is scheduled before they arrive.
+template <int kN>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t ta, float (&v)[kN]) {
+  static_assert(kN == 8 || kN == 16 || kN == 32, "columns");
+  if constexpr (kN == 32) {
+    tmem_ld32(ta, v);
+  } else if constexpr (kN == 16) {
+    tmem_ld16(ta, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+  } else {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(ta)
+        : "memory");
+  }
+}
+
+// Store kN consecutive 32-bit columns of this thread's TMEM lane (no wait).
+template <int kN>
+__device__ __forceinline__ void tmem_st_cols(uint32_t ta, const uint32_t (&w)[kN]) {
+  if constexpr (kN == 8) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(ta), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+  } else {
+#pragma unroll
+    for (int c = 0; c < kN; c += 16) tmem_st16(ta + c, *reinterpret_cast<const uint32_t(*)[16]>(&w[c]));
+  }
+}
 
 // Segment iteration shared by every role: segment (head h, keys [k0, k1)).
 struct SegIter {
@@ -111,6 +157,7 @@ struct SegIter {
   }
 };
 
+template <int kCols>
 __global__ void __launch_bounds__(kThreads, 1)
 splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmQ, const TcParams p) {
@@ -120,6 +167,7 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t g_begin = (int64_t)blockIdx.x * p.L;
   const int64_t g_end = min(p.total, g_begin + p.L);
+  const uint32_t groups = (uint32_t)((p.nq + kCols - 1) / kCols);  // softmax groups with queries: 1 or 2
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
@@ -134,16 +182,22 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     mbar_init(&ctl.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl.s_full[b], 1);
-      mbar_init(&ctl.p_full[b], 4);  // one arrival per softmax warp
+      mbar_init(&ctl.p_full[b], 4 * groups);  // one arrival per softmax warp with queries
     }
     mbar_init(&ctl.pv_done[0], 1);
     mbar_init(&ctl.pv_done[1], 1);
-    mbar_init(&ctl.o_free, 4);
+    mbar_init(&ctl.o_free, 4 * groups);
     mbar_init(&ctl.drain, 1);
     ctl.abort = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&ctl.tmem_base, kTmemCols);
+  if (threadIdx.x < kSoftThreads) {
+    // P^T columns no group writes (queries past 2C) stay zero for every PV product
+    for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += kSoftThreads)
+      reinterpret_cast<uint4*>(smem + kPOff)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -259,144 +313,171 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     }
   } else {
     // ---------------------------------------------------------------- softmax + epilogue
-    const int r = warp * 32 + lane;  // TMEM lane: key of the tile in S^T, head-dim row in O^T
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int g = warp >> 2, wq = warp & 3;  // softmax group, TMEM lane quarter
+    const int r = wq * 32 + lane;            // TMEM lane: key of the tile in S^T, head-dim row in O^T
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const int q0 = g * kCols;                // the group's first query column
     float* corr = reinterpret_cast<float*>(smem + kCorrOff);
-    float* mrow = reinterpret_cast<float*>(smem + kMOff);  // uniform over the threads
+    float* nm = reinterpret_cast<float*>(smem + kNmOff);    // uniform over the group's threads
+    float* nmt = reinterpret_cast<float*>(smem + kNmtOff);
+    const float sl2 = p.sl2;
+    const float2 sl2x2 = make_float2(sl2, sl2);
     float* red = reinterpret_cast<float*>(smem + kRedOff);
     int* flags = reinterpret_cast<int*>(smem + kFlagOff);
     const int nq = p.nq;
-    SegIter it{g_begin, g_end, p.Nk};
-    int64_t h;
-    int k0, k1, t = 0;
-    bool ok = true;
-    // After a failed (timed-out) wait the loops keep their shape, skipping the waits and the
-    // TMEM accesses, so that every softmax warp still reaches every named barrier.
-    while (it.next(h, k0, k1)) {
-      const int n = (k1 - k0 + BN - 1) / BN;
-      if (r < NQP) mrow[r] = -INFINITY;
-      float l[NQP];
-#pragma unroll
-      for (int q = 0; q < NQP; ++q) l[q] = 0.f;
-      softmax_sync();
-      for (int i = 0; i < n; ++i, ++t) {
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full[t & 1], (t >> 1) & 1, p.status, abort));
-        float x[NQP];
-        if (ok) {
-          tc_fence_after();
-          tmem_ld32x2(tmem + lane_off + kColS0 + (t & 1) * NQP, tmem + lane_off + kColS0 + (t & 1) * NQP + 32,
-                      *reinterpret_cast<float(*)[32]>(&x[0]), *reinterpret_cast<float(*)[32]>(&x[32]));
-        } else {
-#pragma unroll
-          for (int q = 0; q < NQP; ++q) x[q] = 0.f;
+    if (q0 < nq) {
+      SegIter it{g_begin, g_end, p.Nk};
+      int64_t h;
+      int k0, k1, t = 0;
+      bool ok = true;
+      // After a failed (timed-out) wait the loops keep their shape, skipping the waits and
+      // the TMEM accesses, so that every warp of the group still reaches every named barrier.
+      while (it.next(h, k0, k1)) {
+        const int n = (k1 - k0 + BN - 1) / BN;
+        if (r < kCols) {
+          nm[q0 + r] = kNegM0;
+          nmt[q0 + r] = kNegM0;  // -(m + threshold) rounds to the same value
         }
-        const int key = k0 + i * BN + r;
-        const bool kin = key < k1;
-        bool grow = false;
+        float l[kCols];
 #pragma unroll
-        for (int q = 0; q < NQP; ++q) {
-          const bool vis = ok && kin && q < nq && !(p.causal && key > q + p.offset);
-          x[q] = vis ? x[q] * p.sl2 : -INFINITY;
-          grow |= x[q] > mrow[q] + kThreshold;
-        }
-        // does any score of the tile exceed its query's reference max by the threshold?
-        grow = __any_sync(0xffffffffu, grow);
-        int* fl = flags + (t & 1) * 4;
-        if (lane == 0) fl[warp] = grow ? 1 : 0;
-        softmax_sync();
-        if ((fl[0] | fl[1] | fl[2] | fl[3]) != 0) {  // uniform over the four warps
-          // exact column maxima of the tile: warp reduction, then across the warps
+        for (int q = 0; q < kCols; ++q) l[q] = 0.f;
+        group_sync(g);
+        for (int i = 0; i < n; ++i, ++t) {
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full[t & 1], (t >> 1) & 1, p.status, abort));
+          float x[kCols];
+          if (ok) {
+            tc_fence_after();
+            tmem_ld_cols<kCols>(tmem + lane_off + kColS0 + (t & 1) * NQP + q0, x);
+          } else {
 #pragma unroll
-          for (int q = 0; q < NQP; ++q) {
-            float v = x[q];
-#pragma unroll
-            for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0) red[warp * NQP + q] = v;
+            for (int q = 0; q < kCols; ++q) x[q] = 0.f;
           }
-          softmax_sync();
-          if (r < NQP) {
-            const float mx = fmaxf(fmaxf(red[r], red[NQP + r]), fmaxf(red[2 * NQP + r], red[3 * NQP + r]));
-            const float mo = mrow[r], mn = fmaxf(mo, mx);
-            corr[r] = mn > mo ? ex2(mo - mn) : 1.f;  // mo = -inf gives 0: nothing accumulated yet
-            mrow[r] = mn;
-          }
-          softmax_sync();
+          // x holds raw scores q.k; masked ones become -inf (scaled: still -inf)
+          const int kb = k0 + i * BN;  // first key of the tile
+          const bool full = ok && kb + BN <= k1 && q0 + kCols <= nq && (!p.causal || kb + BN - 1 <= q0 + p.offset);
+          if (!full) {
+            const int key = kb + r;
+            const bool kin = key < k1;
 #pragma unroll
-          for (int q = 0; q < NQP; ++q) l[q] *= corr[q];
-          if (i > 0 && ok) {
-            // O^T (lane = head-dim row) is rescaled once the previous tile's PV has finished
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&ctl.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, p.status, abort));
-            if (ok) {
-              tc_fence_after();
-              float ov[NQP];
-              tmem_ld32x2(tmem + lane_off + kColO, tmem + lane_off + kColO + 32,
-                          *reinterpret_cast<float(*)[32]>(&ov[0]), *reinterpret_cast<float(*)[32]>(&ov[32]));
-#pragma unroll
-              for (int c = 0; c < NQP; c += 16) {
-                uint32_t w[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) w[u] = __float_as_uint(ov[c + u] * corr[c + u]);
-                tmem_st16(tmem + lane_off + kColO + c, w);
-              }
-              tmem_wait_st();
+            for (int q = 0; q < kCols; ++q) {
+              const int qg = q0 + q;
+              const bool vis = ok && kin && qg < nq && !(p.causal && key > qg + p.offset);
+              x[q] = vis ? x[q] : -INFINITY;
             }
           }
-        }
-        // The P^T buffer of this tile was last read by PV(t - 2).
-        if (t >= 2 && ok)
-          ok = __all_sync(0xffffffffu, mbar_wait(&ctl.pv_done[t & 1], ((t - 2) >> 1) & 1, p.status, abort));
-        // p = 2^(x - m) <= 2^threshold; P^T row r of the tile: 128 bytes, 128-byte swizzle
-        uint8_t* prow = smem + kPOff + (t & 1) * kPBytes + r * 128;
+          // does any score of the tile exceed its query's reference max by the threshold?
+          const float4* nmt4 = reinterpret_cast<const float4*>(nmt + q0);
+          float e = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < NQP / 8; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int q = c * 8 + 2 * u;
-            const float m0 = mrow[q], m1 = mrow[q + 1];
-            const float p0 = ex2(x[q] - (m0 == -INFINITY ? 0.f : m0));
-            const float p1 = ex2(x[q + 1] - (m1 == -INFINITY ? 0.f : m1));
-            l[q] += p0;
-            l[q + 1] += p1;
-            w[u] = pack_bf16(p0, p1);
+          for (int q = 0; q < kCols; q += 4) {
+            const float4 t4 = nmt4[q / 4];
+            const float2 a = ffma2(make_float2(x[q], x[q + 1]), sl2x2, make_float2(t4.x, t4.y));
+            const float2 b = ffma2(make_float2(x[q + 2], x[q + 3]), sl2x2, make_float2(t4.z, t4.w));
+            e = fmax3(e, a.x, a.y);
+            e = fmax3(e, b.x, b.y);
           }
-          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          const bool grow = __any_sync(0xffffffffu, e > 0.f);
+          int* fl = flags + (t & 1) * 8 + 4 * g;
+          if (lane == 0) fl[wq] = grow ? 1 : 0;
+          group_sync(g);
+          if ((fl[0] | fl[1] | fl[2] | fl[3]) != 0) {  // uniform over the group
+            // exact column maxima of the tile: warp reduction, then across the group's warps
+#pragma unroll
+            for (int q = 0; q < kCols; ++q) {
+              float v = x[q] * sl2;
+#pragma unroll
+              for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+              if (lane == 0) red[wq * NQP + q0 + q] = v;
+            }
+            group_sync(g);
+            if (r < kCols) {
+              const int qg = q0 + r;
+              const float mx = fmaxf(fmaxf(red[qg], red[NQP + qg]), fmaxf(red[2 * NQP + qg], red[3 * NQP + qg]));
+              const float mo = -nm[qg], mn = fmaxf(mo, mx);
+              corr[qg] = mn > mo ? ex2(mo - mn) : 1.f;  // mo = -1e30 gives 0: nothing accumulated yet
+              nm[qg] = -mn;
+              nmt[qg] = -(mn + kThreshold);
+            }
+            group_sync(g);
+#pragma unroll
+            for (int q = 0; q < kCols; ++q) l[q] *= corr[q0 + q];
+            if (i > 0 && ok) {
+              // the group's O^T columns (lane = head-dim row) are rescaled once the previous
+              // tile's PV has finished
+              ok = __all_sync(0xffffffffu,
+                              mbar_wait(&ctl.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, p.status, abort));
+              if (ok) {
+                tc_fence_after();
+                float ov[kCols];
+                tmem_ld_cols<kCols>(tmem + lane_off + kColO + q0, ov);
+                uint32_t w[kCols];
+#pragma unroll
+                for (int q = 0; q < kCols; ++q) w[q] = __float_as_uint(ov[q] * corr[q0 + q]);
+                tmem_st_cols<kCols>(tmem + lane_off + kColO + q0, w);
+                tmem_wait_st();
+              }
+            }
+          }
+          // The P^T buffer of this tile was last read by PV(t - 2).
+          if (t >= 2 && ok)
+            ok = __all_sync(0xffffffffu, mbar_wait(&ctl.pv_done[t & 1], ((t - 2) >> 1) & 1, p.status, abort));
+          // p = 2^(s - m) <= 2^threshold; the group's 2C bytes of P^T row r (128-byte swizzle)
+          uint8_t* prow = smem + kPOff + (t & 1) * kPBytes + r * 128;
+          const float4* nm4 = reinterpret_cast<const float4*>(nm + q0);
+#pragma unroll
+          for (int c = 0; c < kCols / 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int q = c * 8 + 2 * u;
+              const float4 m4 = nm4[q / 4];
+              const float2 a = ffma2(make_float2(x[q], x[q + 1]), sl2x2,
+                                     (u & 1) ? make_float2(m4.z, m4.w) : make_float2(m4.x, m4.y));
+              const float p0 = ex2(a.x), p1 = ex2(a.y);
+              const float2 ls = fadd2(make_float2(l[q], l[q + 1]), make_float2(p0, p1));
+              l[q] = ls.x;
+              l[q + 1] = ls.y;
+              w[u] = pack_bf16(p0, p1);
+            }
+            const int chunk = q0 / 8 + c;
+            *reinterpret_cast<uint4*>(prow + ((chunk ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.p_full[t & 1]);
         }
-        fence_proxy_async_smem();
+        // ---- end of segment: reduce the row sums, read O^T, write this CTA's partial state
+        const int tl = t - 1;  // the segment's last tile
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.pv_done[tl & 1], (tl >> 1) & 1, p.status, abort));
+#pragma unroll
+        for (int q = 0; q < kCols; ++q) {
+          float v = l[q];
+#pragma unroll
+          for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) red[wq * NQP + q0 + q] = v;
+        }
+        group_sync(g);
+        const int slot = (int)(blockIdx.x - (h * p.Nk) / p.L);
+        const int64_t base = (h * p.P + slot) * nq;
+        if (r < kCols && q0 + r < nq) {
+          const int qg = q0 + r;
+          const float m = -nm[qg];
+          p.part_ml[(base + qg) * 2] = m <= -0.5f * kNegM0 ? -INFINITY : m;  // no visible key: -inf
+          p.part_ml[(base + qg) * 2 + 1] = red[qg] + red[NQP + qg] + red[2 * NQP + qg] + red[3 * NQP + qg];
+        }
+        if (ok) {
+          tc_fence_after();
+          float ov[kCols];
+          tmem_ld_cols<kCols>(tmem + lane_off + kColO + q0, ov);
+#pragma unroll
+          for (int q = 0; q < kCols; ++q)
+            if (q0 + q < nq) p.part_o[(base + q0 + q) * D + r] = ov[q];
+        }
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.p_full[t & 1]);
+        group_sync(g);  // red[], nm[], nmt[] and the group's O^T columns are free for the next segment
+        if (lane == 0) mbar_arrive(&ctl.o_free);
       }
-      // ---- end of segment: reduce the row sums, read O^T, write this CTA's partial state
-      const int tl = t - 1;  // the segment's last tile
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.pv_done[tl & 1], (tl >> 1) & 1, p.status, abort));
-#pragma unroll
-      for (int q = 0; q < NQP; ++q) {
-        float v = l[q];
-#pragma unroll
-        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) red[warp * NQP + q] = v;
-      }
-      softmax_sync();
-      const int slot = (int)(blockIdx.x - (h * p.Nk) / p.L);
-      const int64_t base = (h * p.P + slot) * nq;
-      if (r < nq) {
-        p.part_ml[(base + r) * 2] = mrow[r];
-        p.part_ml[(base + r) * 2 + 1] = red[r] + red[NQP + r] + red[2 * NQP + r] + red[3 * NQP + r];
-      }
-      if (ok) {
-        tc_fence_after();
-        float ov[NQP];
-        tmem_ld32x2(tmem + lane_off + kColO, tmem + lane_off + kColO + 32, *reinterpret_cast<float(*)[32]>(&ov[0]),
-                    *reinterpret_cast<float(*)[32]>(&ov[32]));
-#pragma unroll
-        for (int q = 0; q < NQP; ++q)
-          if (q < nq) p.part_o[(base + q) * D + r] = ov[q];
-      }
-      tc_fence_before();
-      softmax_sync();  // red[], mrow[] and O^T are free for the next segment
-      if (lane == 0) mbar_arrive(&ctl.o_free);
     }
   }
 
@@ -406,6 +487,16 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+template <int kCols>
+cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mq, const TcParams& p, int ctas,
+                   cudaStream_t st) {
+  static const bool attr = cudaFuncSetAttribute(splitkv_tc_kernel<kCols>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                kSmemBytes) == cudaSuccess;
+  if (!attr) return cudaErrorInvalidConfiguration;
+  splitkv_tc_kernel<kCols><<<ctas, kThreads, kSmemBytes, st>>>(mk, mv, mq, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -427,10 +518,6 @@ cudaError_t splitkv_tc_partial(const void* Q, const void* K, const void* V, int6
   if (!make_map_bf16_3d(&mk, K, heads, Nk, D, BN) || !make_map_bf16_3d(&mv, V, heads, Nk, D, BN) ||
       !make_map_bf16_3d(&mq, Q, heads, Nq, D, NQP))
     return cudaErrorInvalidValue;
-  static const bool attr =
-      cudaFuncSetAttribute(splitkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ==
-      cudaSuccess;
-  if (!attr) return cudaErrorInvalidConfiguration;
   TcParams p;
   p.part_o = workspace;
   p.part_ml = workspace + (size_t)lay.P * heads * Nq * D;
@@ -443,8 +530,9 @@ cudaError_t splitkv_tc_partial(const void* Q, const void* K, const void* V, int6
   p.offset = Nk - Nq;
   p.sl2 = scale * 1.4426950408889634f;
   p.status = status;
-  splitkv_tc_kernel<<<lay.ctas, kThreads, kSmemBytes, st>>>(mk, mv, mq, p);
-  return cudaGetLastError();
+  if (Nq <= 16) return launch<8>(mk, mv, mq, p, lay.ctas, st);
+  if (Nq <= 32) return launch<16>(mk, mv, mq, p, lay.ctas, st);
+  return launch<32>(mk, mv, mq, p, lay.ctas, st);
 }
 
 }  // namespace fa

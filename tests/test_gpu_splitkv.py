@@ -52,6 +52,11 @@ CASES = [  # B, H, Nq, Nk, d, causal, qk_gain
     (4, 8, 8, 600, 128, True, 4.0),      # peaky scores: the running max moves often
     (1, 1, 64, 100000, 128, True, 1.0),  # one head over ~150 CTAs
     (10, 100, 3, 5, 128, True, 1.0),     # dozens of short segments per CTA
+    # query groups of C = 8, 16, 32 columns: one query in the second group, then both full
+    (1, 3, 9, 5000, 128, True, 2.0),
+    (2, 2, 17, 1500, 128, False, 1.0),
+    (1, 2, 33, 2048, 128, True, 4.0),
+    (3, 5, 16, 700, 128, True, 1.0),
 ]
 
 
