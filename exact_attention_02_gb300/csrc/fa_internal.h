@@ -62,14 +62,14 @@ cudaError_t tc_bwd_dropout(const void* Q, const void* K, const void* V, const vo
                            float scale, bool causal, uint64_t seed, uint32_t threshold, int* status,
                            cudaStream_t st);
 
-// ---- split-KV forward for few queries (fa_splitkv.cu): bf16; d = 64 with Nq <= 16, d = 128 with
-// Nq <= 64 (one query on FFMA pipes, more on the tensor cores) ----
+// ---- split-KV forward for few queries (fa_splitkv.cu): bf16; d = 64 with Nq <= 16 on the FFMA
+// pipes, d = 128 with Nq <= 64 on the tensor cores ----
 size_t splitkv_workspace_floats(int64_t heads, int Nq, int Nk, int d);
 cudaError_t splitkv_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t heads,
                         int Nq, int Nk, int d, float scale, bool causal, float* workspace, int* status,
                         cudaStream_t st);
 
-// tcgen05 partial kernel for d = 128 and 2..64 queries (fa_splitkv_tc.cu); writes the same
+// tcgen05 partial kernel for d = 128 and 1..64 queries (fa_splitkv_tc.cu); writes the same
 // partial states as the FFMA partial kernel, merged by the same merge kernel.
 cudaError_t splitkv_tc_partial(const void* Q, const void* K, const void* V, int64_t heads, int Nq, int Nk,
                                float scale, bool causal, float* workspace, int* status, cudaStream_t st);

@@ -1,8 +1,7 @@
 // Split-KV forward: a few queries (e.g. one decoding step) against a long key / value
 // sequence; what it computes is fa_fwd_splitkv in include/fa.h. This file holds the work
-// split, the FFMA partial kernel (one query, or d = 64 with up to 16) and the merge; with
-// d = 128 and 2..64 queries the partial states come from the tensor-core kernel in
-// fa_splitkv_tc.cu instead.
+// split, the FFMA partial kernel (d = 64, up to 16 queries) and the merge; with d = 128 the
+// partial states come from the tensor-core kernel in fa_splitkv_tc.cu instead.
 //
 // The work per head is too small to fill the GPU along the query axis, so the keys are cut
 // into pieces processed by separate CTAs, each keeping the online-softmax state (running
@@ -440,9 +439,6 @@ cudaError_t splitkv_fwd(const void* Q, const void* K, const void* V, void* O, fl
                         int Nq, int Nk, int d, float scale, bool causal, float* workspace, int* status,
                         cudaStream_t st) {
   const Layout lay = layout(heads, Nk);
-  CUtensorMap mk, mv;
-  if (!make_map_bf16_3d(&mk, K, heads, Nk, d, kTileKeys) || !make_map_bf16_3d(&mv, V, heads, Nk, d, kTileKeys))
-    return cudaErrorInvalidValue;
   SplitParams p;
   p.Q = static_cast<const __nv_bfloat16*>(Q);
   p.total = heads * Nk;
@@ -456,10 +452,15 @@ cudaError_t splitkv_fwd(const void* Q, const void* K, const void* V, void* O, fl
   p.status = status;
   p.part_o = workspace;
   p.part_ml = workspace + (size_t)lay.P * heads * Nq * d;
-  // d = 128 with several queries: the tensor-core partial kernel (same partial states)
-  cudaError_t e = d == 128 && Nq >= 2
-                      ? splitkv_tc_partial(Q, K, V, heads, Nq, Nk, scale, causal, workspace, status, st)
-                      : (d == 64 ? launch_d<64>(mk, mv, p, lay.ctas, st) : launch_d<128>(mk, mv, p, lay.ctas, st));
+  cudaError_t e;
+  if (d == 128) {  // the tensor-core partial kernel (same partial states)
+    e = splitkv_tc_partial(Q, K, V, heads, Nq, Nk, scale, causal, workspace, status, st);
+  } else {
+    CUtensorMap mk, mv;
+    if (!make_map_bf16_3d(&mk, K, heads, Nk, d, kTileKeys) || !make_map_bf16_3d(&mv, V, heads, Nk, d, kTileKeys))
+      return cudaErrorInvalidValue;
+    e = launch_d<64>(mk, mv, p, lay.ctas, st);
+  }
   if (e != cudaSuccess) return e;
   const int64_t rows = heads * Nq;
   const unsigned grid = (unsigned)((rows + 3) / 4);

@@ -1,4 +1,4 @@
-// Split-KV forward on the tensor cores, for 2..64 queries against a long key/value
+// Split-KV forward on the tensor cores, for 1..64 queries against a long key/value
 // sequence (d = 128): the same partial states and merge as fa_splitkv.cu, with the two
 // products of each 128-key tile on tcgen05.
 //

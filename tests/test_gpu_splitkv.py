@@ -44,7 +44,7 @@ CASES = [  # B, H, Nq, Nk, d, causal, qk_gain
     # 1000 heads of 5 keys: dozens of short segments per CTA
     (10, 100, 2, 5, 128, True, 1.0),
     (1, 2, 12, 4096, 128, True, 2.0),
-    # d = 128 with 2..64 queries: the tensor-core partial kernel
+    # more d = 128 cases (the tensor-core partial kernel)
     (1, 4, 32, 4096, 128, True, 1.0),
     (2, 2, 64, 3000, 128, False, 1.0),
     (1, 2, 2, 1000, 128, True, 2.0),
