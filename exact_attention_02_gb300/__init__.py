@@ -27,9 +27,7 @@ BF16_KERNEL_BOUND = {"fa_fwd": "tensor", "fa_bwd": "tensor", "fa_bwd_preprocess"
 # cudaMemsetAsync, not a library kernel).
 BF16_KERNELS = {"fa_fwd": ["fa_fwd_tc_kernel"], "fa_bwd_preprocess": ["preprocess_kernel"],
                 "fa_bwd": ["fa_bwd_tc_kernel", "dq_convert_kernel"]}
-# split-KV by head dimension: d = 128 on the tensor cores, d = 64 on the FFMA pipes
-SPLITKV_KERNELS = {128: ["splitkv_tc_kernel", "splitkv_merge_kernel"],
-                   64: ["splitkv_partial_kernel", "splitkv_merge_kernel"]}
+SPLITKV_KERNELS = ["splitkv_tc_kernel", "splitkv_merge_kernel"]
 FP8_KERNELS = ["fa_fwd_tc_kernel"]  # the e4m3 instance of the forward kernel
 FP32_KERNELS = {"fa_fwd": ["simt_fwd_kernel"], "fa_bwd_preprocess": ["preprocess_kernel"],
                 "fa_bwd": ["simt_bwd_dkdv_kernel", "simt_bwd_dq_kernel"]}

@@ -252,7 +252,7 @@ fa_status_t check_splitkv(int B, int H, int Nq, int Nk, int d, float scale, int 
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if ((int64_t)B * H >= (int64_t(1) << 31) || (int64_t)B * H * Nk > (int64_t(1) << 50)) return FA_ERR_INVALID_ARG;
   if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_DTYPE_BF16 || (d != 64 && d != 128) || Nq > (d == 128 ? 64 : 16)) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_DTYPE_BF16 || (d != 64 && d != 128) || Nq > 64) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 }  // namespace

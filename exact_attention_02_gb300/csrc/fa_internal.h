@@ -62,17 +62,18 @@ cudaError_t tc_bwd_dropout(const void* Q, const void* K, const void* V, const vo
                            float scale, bool causal, uint64_t seed, uint32_t threshold, int* status,
                            cudaStream_t st);
 
-// ---- split-KV forward for few queries (fa_splitkv.cu): bf16; d = 64 with Nq <= 16 on the FFMA
-// pipes, d = 128 with Nq <= 64 on the tensor cores ----
+// ---- split-KV forward for few queries (fa_splitkv.cu): bf16, d = 64 or 128, Nq <= 64 ----
 size_t splitkv_workspace_floats(int64_t heads, int Nq, int Nk, int d);
 cudaError_t splitkv_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t heads,
                         int Nq, int Nk, int d, float scale, bool causal, float* workspace, int* status,
                         cudaStream_t st);
 
-// tcgen05 partial kernel for d = 128 and 1..64 queries (fa_splitkv_tc.cu); writes the same
-// partial states as the FFMA partial kernel, merged by the same merge kernel.
-cudaError_t splitkv_tc_partial(const void* Q, const void* K, const void* V, int64_t heads, int Nq, int Nk,
-                               float scale, bool causal, float* workspace, int* status, cudaStream_t st);
+// tcgen05 partial kernel (fa_splitkv_tc.cu): ctas CTA ranges of L keys each over the
+// flattened (head, key) sequence; writes part_o [heads][P][Nq][d] and part_ml
+// [heads][P][Nq][2] = (m in log2 units, l), merged by fa_splitkv.cu.
+cudaError_t splitkv_tc_partial(const void* Q, const void* K, const void* V, int64_t heads, int Nq, int Nk, int d,
+                               float scale, bool causal, int64_t L, int ctas, int P, float* part_o, float* part_ml,
+                               int* status, cudaStream_t st);
 
 // ---- memory-bound helpers (fa_simt.cu) ----
 cudaError_t preprocess_d(const void* O, const void* dO, float* D, const Shape& s, bool bf16,

@@ -1,10 +1,11 @@
 // Split-KV forward on the tensor cores, for 1..64 queries against a long key/value
-// sequence (d = 128): the same partial states and merge as fa_splitkv.cu, with the two
-// products of each 128-key tile on tcgen05.
+// sequence (d = 64 or 128): the same partial states and merge as fa_splitkv.cu, with the
+// two products of each 128-key tile on tcgen05.
 //
-// Work split: as in fa_splitkv.cu, one CTA per SM takes an equal contiguous range of the
-// flattened (head, key) sequence; each piece of a head inside the range is a segment with
-// its own partial state (m, l, O) per query, merged afterwards by splitkv_merge_kernel.
+// Work split (chosen by fa_splitkv.cu): one CTA per SM takes an equal contiguous range of L
+// keys of the flattened (head, key) sequence; each piece of a head inside the range is a
+// segment with its own partial state (m, l, O) per query, stored in slot (head, CTA - first
+// CTA of the head) and merged afterwards by splitkv_merge_kernel.
 //
 // Per 128-key tile (keys on the MMA's M side, queries on N, padded to 64 with zero rows):
 //   S^T = K Q^T           M = 128 keys, N = 64, K = d: one TMEM accumulator [keys x queries]
@@ -30,6 +31,11 @@
 // barriers it would arrive on count only the groups that have queries.
 // Rows: K/V through 3-D maps [heads, N_k, d] (rows past the end of a head read as zeros),
 // Q through [heads, N_q, d] with 64-row boxes (rows past N_q read as zeros).
+// d = 64 loads one 64-column box per tile into 16 KB stages (twice as many as d = 128 has):
+// S^T takes 4 k-steps instead of 8, and O^T += V^T P^T stays an M = 128 product whose
+// second 64-row atom reads the 16 KB that follow the V stage in shared memory. Those rows
+// land in O^T lanes 64..127, which nothing reads (each output row depends only on its own
+// row of V^T).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -43,10 +49,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kCtas = 152;
-constexpr int kMinKeys = 256;
 constexpr int BN = 128;  // keys per tile
-constexpr int D = 128;
 constexpr int NQP = 64;  // queries padded to the MMA's N
 constexpr int kSoftThreads = 256;  // two groups of four softmax warps
 constexpr int kThreads = kSoftThreads + 64;
@@ -55,44 +58,40 @@ constexpr float kThreshold = 8.f;
 constexpr float kNegM0 = 1e30f;  // -m of a query before its first visible score
 
 constexpr int kBoxBytes = BN * 128;           // [128 rows x 64 bf16]
-constexpr int kTileBytes = 2 * kBoxBytes;     // one K or V tile (d = 128)
 constexpr int kQBox = NQP * 128;              // [64 rows x 64 bf16]
-constexpr int kQBytes = 2 * kQBox;
 constexpr int kPBytes = BN * NQP * 2;         // P^T [128 keys x 64 queries] bf16
-constexpr int kKStages = 3, kVStages = 2;  // K is read a tile before V, so it gets the deeper ring
-constexpr int kKOff = 0;
-constexpr int kVOff = kKOff + kKStages * kTileBytes;
-constexpr int kQOff = kVOff + kVStages * kTileBytes;
-constexpr int kPOff = kQOff + kQBytes;
-constexpr int kCorrOff = kPOff + 2 * kPBytes;       // float[64] rescale factors
-constexpr int kNmOff = kCorrOff + 4 * NQP;          // float[64] -m per query (log2 units)
-constexpr int kNmtOff = kNmOff + 4 * NQP;           // float[64] -(m + threshold) per query
-constexpr int kRedOff = kNmtOff + 4 * NQP;          // float[4][64] cross-warp scratch
-constexpr int kFlagOff = kRedOff + 4 * 4 * NQP;     // int[2][8] per-warp flags, by tile parity
-constexpr int kSmemBytes = kFlagOff + 64 + 1024;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+constexpr int kMaxStages = 8;
+
+// Shared-memory layout by head dimension (1024-byte aligned base).
+template <int D>
+struct Cfg {
+  static constexpr int kBoxes = D / 64;               // 64-column boxes per row
+  static constexpr int kTile = kBoxes * kBoxBytes;    // one K or V stage
+  // K is read a tile before V, so it gets the deeper ring
+  static constexpr int kKStages = D == 128 ? 3 : 4;
+  static constexpr int kVStages = D == 128 ? 2 : 4;
+  static constexpr int kQBytes = kBoxes * kQBox;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kKStages * kTile;
+  static constexpr int kQOff = kVOff + kVStages * kTile;
+  static constexpr int kPOff = kQOff + kQBytes;
+  static constexpr int kCorrOff = kPOff + 2 * kPBytes;   // float[64] rescale factors
+  static constexpr int kNmOff = kCorrOff + 4 * NQP;      // float[64] -m per query (log2 units)
+  static constexpr int kNmtOff = kNmOff + 4 * NQP;       // float[64] -(m + threshold) per query
+  static constexpr int kRedOff = kNmtOff + 4 * NQP;      // float[4][64] cross-warp scratch
+  static constexpr int kFlagOff = kRedOff + 4 * 4 * NQP; // int[2][8] per-warp flags, by tile parity
+  static constexpr int kSmemBytes = kFlagOff + 64 + 1024;
+  static_assert(kKStages <= kMaxStages && kVStages <= kMaxStages, "stages");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  // the second 64-row atom of V^T (kBoxBytes past the stage) stays inside the allocation
+  static_assert(kVOff + kVStages * kTile + kBoxBytes <= kSmemBytes - 1024, "V^T atom");
+};
 
 constexpr uint32_t kColS0 = 0, kColO = 2 * NQP;  // S buffers [0,128), O^T [128,192)
 constexpr uint32_t kTmemCols = 256;
 
-struct Layout {
-  int64_t L;
-  int ctas;
-  int P;
-};
-Layout layout(int64_t heads, int Nk) {
-  const int64_t total = heads * Nk;
-  int64_t L = std::max<int64_t>((total + kCtas - 1) / kCtas, kMinKeys);
-  L = (L + 31) / 32 * 32;
-  Layout r;
-  r.L = L;
-  r.ctas = (int)((total + L - 1) / L);
-  r.P = (int)((Nk + L - 1) / L) + 1;
-  return r;
-}
-
 struct TcParams {
-  float* part_o;   // [heads][P][nq][D]
+  float* part_o;   // [heads][P][nq][d]
   float* part_ml;  // [heads][P][nq][2]
   int64_t total, L;
   int nq, Nk, P, causal, offset;
@@ -101,7 +100,7 @@ struct TcParams {
 };
 
 struct Ctl {
-  uint64_t k_full[kKStages], v_full[kVStages], k_empty[kKStages], v_empty[kVStages];
+  uint64_t k_full[kMaxStages], v_full[kMaxStages], k_empty[kMaxStages], v_empty[kMaxStages];
   uint64_t q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_free, drain;
   uint32_t tmem_base;
   int abort;
@@ -157,10 +156,11 @@ struct SegIter {
   }
 };
 
-template <int kCols>
+template <int D, int kCols>
 __global__ void __launch_bounds__(kThreads, 1)
 splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmQ, const TcParams p) {
+  using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Ctl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -170,11 +170,11 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   const uint32_t groups = (uint32_t)((p.nq + kCols - 1) / kCols);  // softmax groups with queries: 1 or 2
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kKStages; ++s) {
+    for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&ctl.k_full[s], 1);
       mbar_init(&ctl.k_empty[s], 1);
     }
-    for (int s = 0; s < kVStages; ++s) {
+    for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(&ctl.v_full[s], 1);
       mbar_init(&ctl.v_empty[s], 1);
     }
@@ -195,7 +195,7 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   if (threadIdx.x < kSoftThreads) {
     // P^T columns no group writes (queries past 2C) stay zero for every PV product
     for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += kSoftThreads)
-      reinterpret_cast<uint4*>(smem + kPOff)[i] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(smem + C::kPOff)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -216,12 +216,11 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       } else {
         prefetch_tmap(&tmV);
       }
-      constexpr int kMaxStages = kKStages > kVStages ? kKStages : kVStages;
-      const int stages = kq ? kKStages : kVStages;
+      const int stages = kq ? C::kKStages : C::kVStages;
       uint64_t* full = kq ? ctl.k_full : ctl.v_full;
       uint64_t* empty = kq ? ctl.k_empty : ctl.v_empty;
       const CUtensorMap* map = kq ? &tmK : &tmV;
-      uint8_t* ring = smem + (kq ? kKOff : kVOff);
+      uint8_t* ring = smem + (kq ? C::kKOff : C::kVOff);
       SegIter it{g_begin, g_end, p.Nk};
       int64_t h;
       int k0, k1, seg = 0, t = 0, last[kMaxStages], last_q = -1;
@@ -230,16 +229,16 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       while (ok && it.next(h, k0, k1)) {
         if (kq) {  // Q of this head, once the previous segment's S products have read the old one
           if (seg > 0 && !(ok = mbar_wait(&ctl.q_empty, (seg - 1) & 1, p.status, abort))) break;
-          mbar_expect_tx(&ctl.q_full, kQBytes);
-          for (int b = 0; b < 2; ++b) tma_load_3d(smem + kQOff + b * kQBox, &tmQ, &ctl.q_full, b * 64, 0, (int)h);
+          mbar_expect_tx(&ctl.q_full, C::kQBytes);
+          for (int b = 0; b < D / 64; ++b) tma_load_3d(smem + C::kQOff + b * kQBox, &tmQ, &ctl.q_full, b * 64, 0, (int)h);
           last_q = seg;
         }
         for (int kt = k0; ok && kt < k1; kt += BN, ++t) {
           const int s = t % stages;
           if (t >= stages && !(ok = mbar_wait(&empty[s], ((t / stages) - 1) & 1, p.status, abort))) break;
-          mbar_expect_tx(&full[s], kTileBytes);
-          for (int b = 0; b < 2; ++b)
-            tma_load_3d(ring + s * kTileBytes + b * kBoxBytes, map, &full[s], b * 64, kt, (int)h);
+          mbar_expect_tx(&full[s], C::kTile);
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_3d(ring + s * C::kTile + b * kBoxBytes, map, &full[s], b * 64, kt, (int)h);
           last[s] = t;
         }
         ++seg;
@@ -253,13 +252,14 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(BN, NQP, false, false);  // S^T: A = K, B = Q, both K-major
-      constexpr uint32_t idO = idesc_bf16(D, NQP, true, true);     // O^T: A = V^T, B = P^T, MN-major
-      const uint64_t dK0 = sdesc_sw128(smem_u32(smem + kKOff), 16, 1024);
-      const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + kQOff), 16, 1024);
-      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + kVOff), kBoxBytes, 1024);
-      const uint64_t dP0 = sdesc_sw128(smem_u32(smem + kPOff), kPBytes, 1024);
+      // O^T: A = V^T (M = 128 rows of d, zero past d = 64), B = P^T, both MN-major
+      constexpr uint32_t idO = idesc_bf16(128, NQP, true, true);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::kVOff), kBoxBytes, 1024);
+      const uint64_t dP0 = sdesc_sw128(smem_u32(smem + C::kPOff), kPBytes, 1024);
       auto issue_S = [&](int t) {
-        const uint32_t ko = (t % kKStages) * kTileBytes;
+        const uint32_t ko = (t % C::kKStages) * C::kTile;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32, qoff = (k / 4) * kQBox + (k % 4) * 32;
@@ -267,7 +267,7 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         }
       };
       auto issue_PV = [&](int t, bool acc) {
-        const uint32_t vo = (t % kVStages) * kTileBytes, po = (t & 1) * kPBytes;
+        const uint32_t vo = (t % C::kVStages) * C::kTile, po = (t & 1) * kPBytes;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
           mma_ss(tmem + kColO, sdesc_add(dV0, vo + k * 2048), sdesc_add(dP0, po + k * 2048), idO,
@@ -280,29 +280,29 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       while (ok && it.next(h, k0, k1)) {
         const int n = (k1 - k0 + BN - 1) / BN;  // tiles in this segment: t .. t + n - 1
         if (!(ok = mbar_wait(&ctl.q_full, seg & 1, p.status, abort))) break;
-        if (!(ok = mbar_wait(&ctl.k_full[t % kKStages], (t / kKStages) & 1, p.status, abort))) break;
+        if (!(ok = mbar_wait(&ctl.k_full[t % C::kKStages], (t / C::kKStages) & 1, p.status, abort))) break;
         tc_fence_after();
         issue_S(t);
-        mma_commit(&ctl.k_empty[t % kKStages]);
+        mma_commit(&ctl.k_empty[t % C::kKStages]);
         mma_commit(&ctl.s_full[t & 1]);
         for (int i = 0; i < n; ++i, ++t) {
           if (i + 1 < n) {  // S of the next tile into the other buffer (read out by tile t-1's softmax)
             if (t >= 1 && !(ok = mbar_wait(&ctl.p_full[(t + 1) & 1], ((t - 1) >> 1) & 1, p.status, abort))) break;
-            if (!(ok = mbar_wait(&ctl.k_full[(t + 1) % kKStages], ((t + 1) / kKStages) & 1, p.status, abort)))
+            if (!(ok = mbar_wait(&ctl.k_full[(t + 1) % C::kKStages], ((t + 1) / C::kKStages) & 1, p.status, abort)))
               break;
             tc_fence_after();
             issue_S(t + 1);
-            mma_commit(&ctl.k_empty[(t + 1) % kKStages]);
+            mma_commit(&ctl.k_empty[(t + 1) % C::kKStages]);
             mma_commit(&ctl.s_full[(t + 1) & 1]);
           } else {
             mma_commit(&ctl.q_empty);  // every S of the segment is issued: Q may be replaced
           }
           if (!(ok = mbar_wait(&ctl.p_full[t & 1], (t >> 1) & 1, p.status, abort))) break;
-          if (!(ok = mbar_wait(&ctl.v_full[t % kVStages], (t / kVStages) & 1, p.status, abort))) break;
+          if (!(ok = mbar_wait(&ctl.v_full[t % C::kVStages], (t / C::kVStages) & 1, p.status, abort))) break;
           if (i == 0 && seg > 0 && !(ok = mbar_wait(&ctl.o_free, (seg - 1) & 1, p.status, abort))) break;
           tc_fence_after();
           issue_PV(t, i > 0);
-          mma_commit(&ctl.v_empty[t % kVStages]);
+          mma_commit(&ctl.v_empty[t % C::kVStages]);
           mma_commit(&ctl.pv_done[t & 1]);
         }
         ++seg;
@@ -317,13 +317,13 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const int r = wq * 32 + lane;            // TMEM lane: key of the tile in S^T, head-dim row in O^T
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const int q0 = g * kCols;                // the group's first query column
-    float* corr = reinterpret_cast<float*>(smem + kCorrOff);
-    float* nm = reinterpret_cast<float*>(smem + kNmOff);    // uniform over the group's threads
-    float* nmt = reinterpret_cast<float*>(smem + kNmtOff);
+    float* corr = reinterpret_cast<float*>(smem + C::kCorrOff);
+    float* nm = reinterpret_cast<float*>(smem + C::kNmOff);    // uniform over the group's threads
+    float* nmt = reinterpret_cast<float*>(smem + C::kNmtOff);
     const float sl2 = p.sl2;
     const float2 sl2x2 = make_float2(sl2, sl2);
-    float* red = reinterpret_cast<float*>(smem + kRedOff);
-    int* flags = reinterpret_cast<int*>(smem + kFlagOff);
+    float* red = reinterpret_cast<float*>(smem + C::kRedOff);
+    int* flags = reinterpret_cast<int*>(smem + C::kFlagOff);
     const int nq = p.nq;
     if (q0 < nq) {
       SegIter it{g_begin, g_end, p.Nk};
@@ -422,7 +422,7 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           if (t >= 2 && ok)
             ok = __all_sync(0xffffffffu, mbar_wait(&ctl.pv_done[t & 1], ((t - 2) >> 1) & 1, p.status, abort));
           // p = 2^(s - m) <= 2^threshold; the group's 2C bytes of P^T row r (128-byte swizzle)
-          uint8_t* prow = smem + kPOff + (t & 1) * kPBytes + r * 128;
+          uint8_t* prow = smem + C::kPOff + (t & 1) * kPBytes + r * 128;
           const float4* nm4 = reinterpret_cast<const float4*>(nm + q0);
 #pragma unroll
           for (int c = 0; c < kCols / 8; ++c) {
@@ -469,10 +469,12 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         if (ok) {
           tc_fence_after();
           float ov[kCols];
-          tmem_ld_cols<kCols>(tmem + lane_off + kColO + q0, ov);
+          tmem_ld_cols<kCols>(tmem + lane_off + kColO + q0, ov);  // warp-collective: every lane loads
+          if (r < D) {  // O^T lanes past d hold V^T's zero rows
 #pragma unroll
-          for (int q = 0; q < kCols; ++q)
-            if (q0 + q < nq) p.part_o[(base + q0 + q) * D + r] = ov[q];
+            for (int q = 0; q < kCols; ++q)
+              if (q0 + q < nq) p.part_o[(base + q0 + q) * D + r] = ov[q];
+          }
         }
         tc_fence_before();
         group_sync(g);  // red[], nm[], nmt[] and the group's O^T columns are free for the next segment
@@ -489,50 +491,47 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   }
 }
 
-template <int kCols>
+template <int D, int kCols>
 cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mq, const TcParams& p, int ctas,
                    cudaStream_t st) {
-  static const bool attr = cudaFuncSetAttribute(splitkv_tc_kernel<kCols>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                kSmemBytes) == cudaSuccess;
+  static const bool attr = cudaFuncSetAttribute(splitkv_tc_kernel<D, kCols>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes) == cudaSuccess;
   if (!attr) return cudaErrorInvalidConfiguration;
-  splitkv_tc_kernel<kCols><<<ctas, kThreads, kSmemBytes, st>>>(mk, mv, mq, p);
+  splitkv_tc_kernel<D, kCols><<<ctas, kThreads, Cfg<D>::kSmemBytes, st>>>(mk, mv, mq, p);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mq, const TcParams& p, int ctas,
+                     cudaStream_t st) {
+  if (p.nq <= 16) return launch<D, 8>(mk, mv, mq, p, ctas, st);
+  if (p.nq <= 32) return launch<D, 16>(mk, mv, mq, p, ctas, st);
+  return launch<D, 32>(mk, mv, mq, p, ctas, st);
 }
 
 }  // namespace
 
-size_t splitkv_tc_workspace_floats(int64_t heads, int Nq, int Nk) {
-  return (size_t)layout(heads, Nk).P * heads * Nq * (D + 2);
-}
-
-int splitkv_tc_partials(int64_t heads, int Nk, int64_t* L) {
-  const Layout lay = layout(heads, Nk);
-  *L = lay.L;
-  return lay.P;
-}
-
-cudaError_t splitkv_tc_partial(const void* Q, const void* K, const void* V, int64_t heads, int Nq, int Nk,
-                               float scale, bool causal, float* workspace, int* status, cudaStream_t st) {
-  const Layout lay = layout(heads, Nk);
+cudaError_t splitkv_tc_partial(const void* Q, const void* K, const void* V, int64_t heads, int Nq, int Nk, int d,
+                               float scale, bool causal, int64_t L, int ctas, int P, float* part_o, float* part_ml,
+                               int* status, cudaStream_t st) {
+  if (d != 64 && d != 128) return cudaErrorInvalidValue;
   CUtensorMap mk, mv, mq;
-  if (!make_map_bf16_3d(&mk, K, heads, Nk, D, BN) || !make_map_bf16_3d(&mv, V, heads, Nk, D, BN) ||
-      !make_map_bf16_3d(&mq, Q, heads, Nq, D, NQP))
+  if (!make_map_bf16_3d(&mk, K, heads, Nk, d, BN) || !make_map_bf16_3d(&mv, V, heads, Nk, d, BN) ||
+      !make_map_bf16_3d(&mq, Q, heads, Nq, d, NQP))
     return cudaErrorInvalidValue;
   TcParams p;
-  p.part_o = workspace;
-  p.part_ml = workspace + (size_t)lay.P * heads * Nq * D;
+  p.part_o = part_o;
+  p.part_ml = part_ml;
   p.total = heads * Nk;
-  p.L = lay.L;
+  p.L = L;
   p.nq = Nq;
   p.Nk = Nk;
-  p.P = lay.P;
+  p.P = P;
   p.causal = causal ? 1 : 0;
   p.offset = Nk - Nq;
   p.sl2 = scale * 1.4426950408889634f;
   p.status = status;
-  if (Nq <= 16) return launch<8>(mk, mv, mq, p, lay.ctas, st);
-  if (Nq <= 32) return launch<16>(mk, mv, mq, p, lay.ctas, st);
-  return launch<32>(mk, mv, mq, p, lay.ctas, st);
+  return d == 64 ? launch_d<64>(mk, mv, mq, p, ctas, st) : launch_d<128>(mk, mv, mq, p, ctas, st);
 }
 
 }  // namespace fa

@@ -138,9 +138,9 @@ FA_API fa_status_t fa_bwd_noalloc(const void* Q, const void* K, const void* V, c
  * In:  Q [B,H,N_q,d], K and V [B,H,N_k,d] bf16.  Out: O [B,H,N_q,d] bf16, LSE [B,H,N_q] fp32.
  * causal: the queries are the last N_q positions (requires N_q <= N_k): query i hides
  *      keys j > i + N_k - N_q. causal = 0: every key is visible.
- * Supported: bf16; d = 128 with 1 <= N_q <= 64, d = 64 with 1 <= N_q <= 16 (else
- *      FA_ERR_UNSUPPORTED); any N_k >= 1. d = 128 runs both products of each 128-key tile on
- *      the tensor cores; d = 64 runs on the FFMA pipes.
+ * Supported: bf16; d = 64 or 128 with 1 <= N_q <= 64 (else
+ *      FA_ERR_UNSUPPORTED); any N_k >= 1. Both products of each 128-key tile run on the
+ *      tensor cores.
  * workspace: device buffer of at least fa_fwd_splitkv_workspace_size(...) bytes (fp32
  *      chunk states); its contents on entry do not matter.
  */

@@ -128,9 +128,10 @@ def test_splitkv_workspace_and_rejects(lib):
     n = fa.lib().fa_fwd_splitkv_workspace_size(1, 2, 1, 1000, 128, 0)
     assert n > 0 and n % 4 == 0
     assert fa.lib().fa_fwd_splitkv_workspace_size(1, 2, 65, 1000, 128, 0) == 0
-    assert fa.lib().fa_fwd_splitkv_workspace_size(1, 2, 17, 1000, 64, 0) == 0
-    assert _splitkv(lib, Nq=65) == 2            # more queries than the split-KV path takes (d = 128)
-    assert _splitkv(lib, Nq=17, d=64) == 2      # d = 64: at most 16
+    assert fa.lib().fa_fwd_splitkv_workspace_size(1, 2, 65, 1000, 64, 0) == 0
+    assert fa.lib().fa_fwd_splitkv_workspace_size(1, 2, 64, 1000, 64, 0) > 0
+    assert _splitkv(lib, Nq=65) == 2            # more queries than the split-KV path takes
+    assert _splitkv(lib, Nq=65, d=64) == 2
     assert _splitkv(lib, d=96) == 2
     assert _splitkv(lib, dtype=1) == 2          # fp32 goes through fa_fwd
     assert _splitkv(lib, Nq=8, Nk=4) == 1       # causal needs N_q <= N_k

@@ -57,6 +57,11 @@ CASES = [  # B, H, Nq, Nk, d, causal, qk_gain
     (2, 2, 17, 1500, 128, False, 1.0),
     (1, 2, 33, 2048, 128, True, 4.0),
     (3, 5, 16, 700, 128, True, 1.0),
+    # d = 64 with more than 16 queries, every query-group width
+    (1, 2, 24, 3000, 64, True, 1.0),
+    (2, 3, 64, 1000, 64, False, 2.0),
+    (1, 1, 40, 100000, 64, True, 1.0),
+    (4, 4, 33, 777, 64, True, 4.0),
 ]
 
 
