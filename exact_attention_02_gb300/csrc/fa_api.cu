@@ -125,15 +125,15 @@ fa_status_t check_mask(const Mask& m, const Shape& s, int dtype) {
 
 struct Drop {
   uint64_t seed;
-  uint32_t t;  // keep iff the 16-bit uniform >= t
+  uint32_t t;  // keep iff the 8-bit uniform >= t
 };
 
-// Dropout probability p in [0, 1) -> 16-bit keep threshold round(p * 65536), at most 65535.
+// Dropout probability p in [0, 1) -> 8-bit keep threshold round(p * 256), at most 255.
 fa_status_t drop_threshold(float p, int dtype, uint32_t* t) {
   if (!(isfinite(p) && p >= 0.f && p < 1.f)) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
-  const double r = floor((double)p * 65536.0 + 0.5);
-  *t = (uint32_t)(r > 65535.0 ? 65535.0 : r);
+  const double r = floor((double)p * 256.0 + 0.5);
+  *t = (uint32_t)(r > 255.0 ? 255.0 : r);
   return FA_OK;
 }
 

@@ -113,9 +113,24 @@ struct BwdParams {
   int64_t mask_sb, mask_sh, mask_srow;
   int H;
   // dropout (kVar == 2): Philox key, keep threshold and the scale of a kept weight
-  uint32_t seed_lo, seed_hi, drop_t;
+  uint32_t seed_lo, seed_hi, drop_tt;  // drop_tt: the keep threshold in all four bytes
   float drop_scale;
 };
+
+// Transpose of a 32 x 32 bit matrix held one row per lane: on return lane T holds bit c =
+// bit T of lane c's row. Five butterfly stages; the stage of width s swaps, between lanes
+// l and l ^ s, the s-bit groups whose position differs from the lane in bit s.
+__device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
+  constexpr uint32_t kLow[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const int s = 16 >> k;
+    const uint32_t m = kLow[k];  // bit positions p with (p & s) == 0
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, s);
+    x = (lane & s) ? ((x & ~m) | ((y & ~m) >> s)) : ((x & m) | ((y & m) << s));
+  }
+  return x;
+}
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -420,22 +435,16 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           }
         }
         // kDrop: keep bits of this thread's key against the chunk's 32 queries. Lane L draws
-        // the bits of query (chunk start + L) against the warp's 32 keys (4 Philox blocks of
-        // 8 keys); 32 ballots transpose that 32 x 32 bit block, so lane T ends up with bit c
-        // = keep(query c, key T).
+        // the bits of query (chunk start + L) against the warp's 32 keys (2 Philox blocks of
+        // 16 keys); transposing that 32 x 32 bit block leaves lane T with bit c =
+        // keep(query c, key T).
         uint32_t kbits = 0;
         if constexpr (kDrop) {
           const uint32_t i = (uint32_t)(q0 + c0 + lane);
-          const uint32_t blk0 = (uint32_t)((kt * BN + (warp & 3) * 32) >> 3);
-          uint32_t row = 0;
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb)
-            row |= rng::keep8(blk0 + bb, i, (uint32_t)head, p.seed_lo, p.seed_hi, p.drop_t) << (8 * bb);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const uint32_t col = __ballot_sync(0xffffffffu, (row >> e) & 1u);
-            if (lane == e) kbits = col;
-          }
+          const uint32_t blk0 = (uint32_t)((kt * BN + (warp & 3) * 32) >> 4);
+          const uint32_t row = rng::keep16(blk0, i, (uint32_t)head, p.seed_lo, p.seed_hi, p.drop_tt) |
+                               (rng::keep16(blk0 + 1, i, (uint32_t)head, p.seed_lo, p.seed_hi, p.drop_tt) << 16);
+          kbits = transpose32(row, lane);
         }
         float sv[32], dp[32];
         tmem_ld32x2(tmem + lane_off + C::colS(b) + c0, tmem + lane_off + C::colDP(b) + c0, sv, dp);
@@ -657,8 +666,8 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
   p.H = s.H;
   p.seed_lo = (uint32_t)(drop.seed & 0xFFFFFFFFu);
   p.seed_hi = (uint32_t)(drop.seed >> 32);
-  p.drop_t = drop.t;
-  p.drop_scale = (float)(65536.0 / (65536.0 - (double)drop.t));
+  p.drop_tt = drop.t * 0x01010101u;
+  p.drop_scale = (float)(256.0 / (256.0 - (double)drop.t));
   const int64_t grid = (int64_t)p.kvtiles * p.heads;
   if (s.N % 128 != 0)
     fa_bwd_tc_kernel<D, true, kVar><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);

@@ -41,8 +41,8 @@
 //
 // Dropout instance (kVar == 2): the same section of "知识点13" fuses dropout into the
 // softmax step. Each softmax thread draws the keep bits of its row for the next K tile
-// (16 Philox calls, see philox.cuh) while the tile's S is being computed, stores p only
-// for kept keys (row sums l still take every p) and scales O by 65536 / (65536 - t).
+// (8 Philox calls of 16 keys, see philox.cuh) while the tile's S is being computed, stores
+// p only for kept keys (row sums l still take every p) and scales O by 256 / (256 - t).
 //
 // Causal: tile t sees K tiles 0..qtile_t; the diagonal tile masks key > query.
 // Any N: Q/K/V are read through [heads, N, d] tensor maps, so rows past the end of a head
@@ -112,7 +112,7 @@ struct FwdParams {
   int H;
   float inv_scale;  // 1 / scale: M joins the raw scores as M / scale
   // dropout (kVar == 2): Philox key, keep threshold and the scale of a kept weight
-  uint32_t seed_lo, seed_hi, drop_t;
+  uint32_t seed_lo, seed_hi, drop_tt;  // drop_tt: the keep threshold in all four bytes
   float drop_scale;
 };
 
@@ -326,10 +326,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int w = 0; w < BN / 32; ++w) keep[w] = 0;
 #pragma unroll
-        for (int c8 = 0; c8 < BN / 8; ++c8)
-          keep[c8 / 4] |= rng::keep8((uint32_t)(j * (BN / 8) + c8), (uint32_t)qrow, (uint32_t)head, p.seed_lo,
-                                     p.seed_hi, p.drop_t)
-                          << (8 * (c8 % 4));
+        for (int c16 = 0; c16 < BN / 16; ++c16)
+          keep[c16 / 2] |= rng::keep16((uint32_t)(j * (BN / 16) + c16), (uint32_t)qrow, (uint32_t)head, p.seed_lo,
+                                       p.seed_hi, p.drop_tt)
+                           << (16 * (c16 % 2));
       }
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full[t], j & 1, p.status, abort));
       if (!ok) break;
@@ -540,8 +540,8 @@ cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.inv_scale = 1.f / scale;
   p.seed_lo = (uint32_t)(drop.seed & 0xFFFFFFFFu);
   p.seed_hi = (uint32_t)(drop.seed >> 32);
-  p.drop_t = drop.t;
-  p.drop_scale = (float)(65536.0 / (65536.0 - (double)drop.t));
+  p.drop_tt = drop.t * 0x01010101u;
+  p.drop_scale = (float)(256.0 / (256.0 - (double)drop.t));
   const int64_t grid = (int64_t)p.pairs * p.heads;
   fa_fwd_tc_kernel<D, F8, kVar><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p);
   return cudaGetLastError();

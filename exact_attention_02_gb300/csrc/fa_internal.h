@@ -36,8 +36,8 @@ cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* 
 cudaError_t tc_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                           float scale, bool causal, const void* mask, int64_t mask_sb, int64_t mask_sh,
                           int64_t mask_srow, int* status, cudaStream_t st);
-// bf16 forward with dropout: Philox-4x32-10 keep bits keyed by `seed`, kept iff the 16-bit
-// uniform is >= threshold; kept weights scaled by 65536 / (65536 - threshold).
+// bf16 forward with dropout: Philox-4x32-10 keep bits keyed by `seed`, kept iff the 8-bit
+// uniform is >= threshold; kept weights scaled by 256 / (256 - threshold).
 cudaError_t tc_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                            float scale, bool causal, uint64_t seed, uint32_t threshold, int* status,
                            cudaStream_t st);

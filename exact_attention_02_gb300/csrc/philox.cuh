@@ -7,10 +7,10 @@
 // M0 = 0xD2511F53, M1 = 0xCD9E8D57; the key is bumped by (0x9E3779B9, 0xBB67AE85)
 // between rounds; 10 rounds.
 //
-// Dropout layout: element (query i, key j) of head h takes the 16-bit half j % 2 of word
-// (j % 8) / 2 of Philox(counter = (j / 8, i, h, 0), key = (seed low, seed high)); the key
-// is kept iff that value is >= the threshold t = round(p * 65536), and a kept weight is
-// scaled by 65536 / (65536 - t).
+// Dropout layout: element (query i, key j) of head h takes byte j % 4 of word (j % 16) / 4
+// of Philox(counter = (j / 16, i, h, 0), key = (seed low, seed high)), so one generator
+// call serves 16 keys; the key is kept iff that byte is >= the threshold
+// t = min(255, round(p * 256)), and a kept weight is scaled by 256 / (256 - t).
 #pragma once
 
 #include <stdint.h>
@@ -32,15 +32,23 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Keep bits of the 8 keys 8*blk .. 8*blk + 7 for query i of head h: bit e = key 8*blk + e.
-__device__ __forceinline__ uint32_t keep8(uint32_t blk, uint32_t i, uint32_t h, uint32_t k0, uint32_t k1,
-                                          uint32_t t) {
+// Bit b (b < 4) is set iff byte b of a is >= byte b of tt (unsigned), for all four bytes at
+// once. With H the byte sign bits: (a | H) - (tt & ~H) never borrows across bytes, and its
+// sign bit says a' >= t' for the low 7 bits; a >= t then holds iff a's top bit is set and
+// t's is not, or the top bits agree and a' >= t'.
+__device__ __forceinline__ uint32_t bytes_ge(uint32_t a, uint32_t tt) {
+  constexpr uint32_t H = 0x80808080u;
+  const uint32_t d = (a | H) - (tt & ~H);
+  const uint32_t r = ((a & ~tt) | (~(a ^ tt) & d)) & H;
+  return ((r >> 7) & 1u) | ((r >> 14) & 2u) | ((r >> 21) & 4u) | ((r >> 28) & 8u);
+}
+
+// Keep bits of the 16 keys 16*blk .. 16*blk + 15 for query i of head h: bit e = key
+// 16*blk + e. tt is the threshold t repeated in all four bytes (t * 0x01010101).
+__device__ __forceinline__ uint32_t keep16(uint32_t blk, uint32_t i, uint32_t h, uint32_t k0, uint32_t k1,
+                                           uint32_t tt) {
   const uint4 w = philox4x32_10(make_uint4(blk, i, h, 0u), k0, k1);
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-  uint32_t bits = 0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) bits |= (((ws[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) >= t ? 1u : 0u) << e;
-  return bits;
+  return bytes_ge(w.x, tt) | (bytes_ge(w.y, tt) << 4) | (bytes_ge(w.z, tt) << 8) | (bytes_ge(w.w, tt) << 12);
 }
 
 }  // namespace rng

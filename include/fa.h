@@ -184,11 +184,11 @@ FA_API fa_status_t fa_bwd_masked(const void* Q, const void* K, const void* V, co
  * LSE is the undropped softmax's. The backward is the exact gradient of that O for the
  *      same K: pass the same p_drop and seed to both calls (and D from the dropped O).
  * Keep bits: Philox-4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3",
- *      SC 2011). Element (query i, key j) of head h = b*H + head takes the 16-bit half
- *      j % 2 of word (j % 8) / 2 of Philox(counter (j / 8, i, h, 0), key (seed & 0xffffffff,
- *      seed >> 32)); the key is kept iff that value >= t = min(65535, round(p_drop * 65536)),
- *      and c = 65536 / (65536 - t): the probability is quantised to a multiple of 2^-16
- *      and every weight keeps its expected value exactly.
+ *      SC 2011). Element (query i, key j) of head h = b*H + head takes byte j % 4 of word
+ *      (j % 16) / 4 of Philox(counter (j / 16, i, h, 0), key (seed & 0xffffffff,
+ *      seed >> 32)); the key is kept iff that byte >= t = min(255, round(p_drop * 256)),
+ *      and c = 256 / (256 - t): the probability is quantised to a multiple of 2^-8 and
+ *      every weight keeps its expected value exactly.
  * p_drop: finite, 0 <= p_drop < 1 (else FA_ERR_INVALID_ARG); dtype must be FA_DTYPE_BF16
  *      (else FA_ERR_UNSUPPORTED). The remaining arguments are those of fa_fwd / fa_bwd.
  */

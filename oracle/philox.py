@@ -12,12 +12,12 @@ key is bumped by (0x9E3779B9, 0xBB67AE85) between rounds; 10 rounds.
 
 Dropout layout (the reading this project takes; the pages only name dropout as one of the
 steps fused into the softmax, "知识点13 FlashAttention深度攻略" section 7):
-  * element (i, j) of head h (h = b * H + head within batch b) takes the 16-bit uniform
-    u = bits 16*(j % 2)..+15 of word (j % 8) / 2 of Philox(counter = (j // 8, i, h, 0),
-    key = (seed & 0xffffffff, seed >> 32));
-  * the key is kept iff u >= t, where t = min(65535, round(p * 65536)) for the dropout
-    probability p; kept weights are scaled by 65536 / (65536 - t), so every weight keeps
-    its expected value exactly for the quantised probability t / 65536.
+  * element (i, j) of head h (h = b * H + head within batch b) takes the 8-bit uniform
+    u = bits 8*(j % 4)..+7 of word (j % 16) / 4 of Philox(counter = (j // 16, i, h, 0),
+    key = (seed & 0xffffffff, seed >> 32)): one generator call serves 16 keys;
+  * the key is kept iff u >= t, where t = min(255, round(p * 256)) for the dropout
+    probability p; kept weights are scaled by 256 / (256 - t), so every weight keeps its
+    expected value exactly for the quantised probability t / 256.
 """
 from __future__ import annotations
 
@@ -46,27 +46,27 @@ def philox4x32_10(ctr, key) -> np.ndarray:
 
 
 def threshold(p: float) -> int:
-    """The 16-bit keep threshold of dropout probability p in [0, 1)."""
-    return int(min(65535, int(np.floor(float(p) * 65536.0 + 0.5))))
+    """The 8-bit keep threshold of dropout probability p in [0, 1)."""
+    return int(min(255, int(np.floor(float(p) * 256.0 + 0.5))))
 
 
 def keep_scale(t: int) -> float:
-    """Scale of a kept weight: 65536 / (65536 - t)."""
-    return 65536.0 / (65536.0 - t)
+    """Scale of a kept weight: 256 / (256 - t)."""
+    return 256.0 / (256.0 - t)
 
 
 def uniforms(seed: int, head: int, rows, ncols: int) -> np.ndarray:
-    """The 16-bit uniforms u of the query rows ``rows`` against keys 0..ncols-1 of one head."""
+    """The 8-bit uniforms u of the query rows ``rows`` against keys 0..ncols-1 of one head."""
     rows = np.asarray(rows, dtype=np.uint64)
-    nblk = (ncols + 7) // 8
+    nblk = (ncols + 15) // 16
     ctr = np.zeros((rows.size, nblk, 4), dtype=np.uint64)
     ctr[..., 0] = np.arange(nblk, dtype=np.uint64)[None, :]
     ctr[..., 1] = rows[:, None]
     ctr[..., 2] = np.uint64(head)
     key = np.array([seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF], dtype=np.uint64)
-    words = philox4x32_10(ctr, key).astype(np.uint32)          # [rows, nblk, 4]
-    halves = np.stack([words & 0xFFFF, words >> 16], axis=-1)  # [rows, nblk, 4, 2]
-    return halves.reshape(rows.size, nblk * 8)[:, :ncols].astype(np.uint32)
+    words = philox4x32_10(ctr, key).astype(np.uint32)                  # [rows, nblk, 4]
+    octets = np.stack([(words >> (8 * b)) & 0xFF for b in range(4)], axis=-1)  # [rows, nblk, 4, 4]
+    return octets.reshape(rows.size, nblk * 16)[:, :ncols].astype(np.uint32)
 
 
 def keep_matrix(seed: int, head: int, n_rows: int, n_cols: int, p: float) -> np.ndarray:

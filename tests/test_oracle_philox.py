@@ -3,10 +3,10 @@
 - Philox-4x32-10 against the generator's published known-answer vectors (the Random123
   library's known-answer tests for philox4x32 with 10 rounds, distributed with the paper
   "Parallel random numbers: as easy as 1, 2, 3", SC 2011).
-- The keep layout: element (i, j) takes 16-bit half j % 2 of word (j % 8) / 2 of the block
-  (j // 8, i, head, 0), checked against direct calls of the generator.
+- The keep layout: element (i, j) takes byte j % 4 of word (j % 16) / 4 of the block
+  (j // 16, i, head, 0), checked against direct calls of the generator.
 - The keep decision's closed forms (p = 0 keeps everything; the threshold of p = 1/2) and
-  its statistics (binomial bounds on the kept fraction).
+  its statistics (binomial bounds on the kept fraction, the mean of a uniform byte).
 - Planted mistakes in copies of the module, each caught.
 """
 import math
@@ -35,26 +35,27 @@ def pin_known_answers(mod):
 
 def pin_layout(mod):
     seed, head = 0x1234_5678_9ABC_DEF0, 5
-    u = mod.uniforms(seed, head, [0, 3, 77], 21)
+    u = mod.uniforms(seed, head, [0, 3, 77], 37)
     key = np.array([seed & 0xFFFFFFFF, seed >> 32], np.uint64)
     for a, i in enumerate((0, 3, 77)):
-        for j in range(21):
-            w = mod.philox4x32_10(np.array([j // 8, i, head, 0], np.uint64), key)
-            half = (int(w[(j % 8) // 2]) >> (16 * (j % 2))) & 0xFFFF
-            assert u[a, j] == half, (i, j)
+        for j in range(37):
+            w = mod.philox4x32_10(np.array([j // 16, i, head, 0], np.uint64), key)
+            octet = (int(w[(j % 16) // 4]) >> (8 * (j % 4))) & 0xFF
+            assert u[a, j] == octet, (i, j)
 
 
 def pin_keep_rule(mod):
-    assert mod.threshold(0.0) == 0 and mod.threshold(0.5) == 32768 and mod.threshold(0.9999999) == 65535
-    assert mod.keep_scale(0) == 1.0 and mod.keep_scale(32768) == 2.0
+    assert mod.threshold(0.0) == 0 and mod.threshold(0.5) == 128 and mod.threshold(0.9999999) == 255
+    assert mod.threshold(0.1) == 26   # round(25.6)
+    assert mod.keep_scale(0) == 1.0 and mod.keep_scale(128) == 2.0 and mod.keep_scale(192) == 4.0
     assert mod.keep_matrix(7, 0, 16, 40, 0.0).all()
     n_rows, n_cols, p = 256, 2048, 0.25
     K = mod.keep_matrix(99, 3, n_rows, n_cols, p)
     n = K.size
-    keep_p = 1 - mod.threshold(p) / 65536
+    keep_p = 1 - mod.threshold(p) / 256
     assert abs(K.mean() - keep_p) < 5 * math.sqrt(keep_p * (1 - keep_p) / n)
     u = mod.uniforms(99, 3, np.arange(64), 512).astype(np.float64)
-    assert abs(u.mean() - 32767.5) < 5 * 18918.6 / math.sqrt(u.size)   # uniform on 0..65535
+    assert u.max() <= 255 and abs(u.mean() - 127.5) < 5 * 73.9 / math.sqrt(u.size)   # uniform on 0..255
     assert not np.array_equal(K, mod.keep_matrix(99, 4, n_rows, n_cols, p))   # another head
     assert not np.array_equal(K, mod.keep_matrix(100, 3, n_rows, n_cols, p))  # another seed
 
@@ -73,8 +74,10 @@ MUTATIONS = [
     ("hi and lo swapped",
      "c0, c1, c2, c3 = (p1 >> np.uint64(32)) ^ c1 ^ k0, p1 & _MASK, (p0 >> np.uint64(32)) ^ c3 ^ k1, p0 & _MASK",
      "c0, c1, c2, c3 = (p1 & _MASK) ^ c1 ^ k0, p1 >> np.uint64(32), (p0 >> np.uint64(32)) ^ c3 ^ k1, p0 & _MASK"),
-    ("halves in the wrong order", "np.stack([words & 0xFFFF, words >> 16], axis=-1)",
-     "np.stack([words >> 16, words & 0xFFFF], axis=-1)"),
+    ("bytes in the wrong order", "np.stack([(words >> (8 * b)) & 0xFF for b in range(4)], axis=-1)",
+     "np.stack([(words >> (8 * b)) & 0xFF for b in range(3, -1, -1)], axis=-1)"),
+    ("row and head swapped in the counter", "ctr[..., 1] = rows[:, None]\n    ctr[..., 2] = np.uint64(head)",
+     "ctr[..., 2] = rows[:, None]\n    ctr[..., 1] = np.uint64(head)"),
 ]
 
 
