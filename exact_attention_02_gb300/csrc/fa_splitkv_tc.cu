@@ -483,6 +483,9 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     }
   }
 
+  // The producer and MMA roles run on single lanes: they rejoin the rest of their warps
+  // first, so that the barrier below (which counts whole warps) holds until every role is done.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
