@@ -15,19 +15,17 @@
 //   dS^T = P^T * (dP^T - D_i)                     softmax warps, one thread per key
 //   dV_j += P^T dO_i          TMEM accumulator    A = P^T from TMEM
 //   dK_j += dS^T Q_i          TMEM accumulator    A = dS^T from TMEM
-//   d = 128: dQ_i^T = K_j^T dS^T   (lanes = head dim)   A = K_j (MN-major), B = dS^T (smem, MN-major)
-//   d =  64: dQ_i   = dS K_j       (lanes = queries)    A = dS^T (smem, MN-major), B = K_j (MN-major)
+//   dQ_i^T = K_j^T dS^T            (lanes = head dim)   A = K_j (MN-major), B = dS^T (smem, MN-major)
 // and the dQ partials are added into an fp32 accumulator in global memory (red.add); a
-// last pass scales it by `scale` and rounds to bf16.
+// last pass scales it by `scale` and rounds to bf16. dQ^T is always an M = 128 product:
+// at d = 64 its second 64-row atom of K^T reads the V tile that follows K in shared
+// memory, and those rows land in TMEM lanes 64..127, which the dQ warps do not read.
 //
-// TMEM (512 columns): dV | dK | NB buffers of (S^T | dP^T). Each softmax warpgroup
+// TMEM (512 columns): dV | dK | 2 buffers of (S^T | dP^T). Each softmax warpgroup
 // writes its bf16 P^T over the S^T columns it has just read and its bf16 dS^T over the
 // dP^T columns it has just read; the dQ partial of a tile then reuses its S^T columns
-// once dV has consumed P^T. Query tiles are BQ = 64 rows for d = 128, which leaves room
-// for NB = 2 buffers, so the softmax of tile i+1 overlaps the MMAs of tile i; for d = 64
-// they are BQ = 128 rows with one buffer (wider MMAs, fewer operand bytes per FLOP).
-// Per tile the tensor core runs dV, dK, dQ of tile i, then dP of tile i+NB while the dQ
-// warpgroup drains the partial, then S of tile i+NB.
+// once dV has consumed P^T. Query tiles are BQ = 64 rows, which leaves room for two
+// buffers, so the softmax of tile i+1 overlaps the MMAs of tile i.
 //
 // CTA = 14 warps: 0-7 softmax (two warpgroups splitting the query columns), 8-11 dQ
 // reduction + dK/dV epilogue, 12 TMA producer, 13 MMA issuer.
@@ -63,10 +61,9 @@ struct BwdCtl {
 
 template <int D>
 struct BwdCfg {
-  static constexpr int BQ = D == 128 ? 64 : 128;     // queries per tile
-  static constexpr int NB = D == 128 ? 2 : 1;        // S^T/dP^T buffers in TMEM
+  static constexpr int BQ = 64;                      // queries per tile
+  static constexpr int NB = 2;                       // S^T/dP^T buffers in TMEM
   static constexpr int kCols = BQ / 2;               // query columns per softmax warpgroup
-  static constexpr bool kDqT = D == 128;             // dQ^T (lanes = head dim) or dQ (lanes = queries)
   static constexpr int kBoxes = D / 64;              // 64-column boxes per row
   static constexpr int kKVBytes = BN * D * 2;        // K_j or V_j
   static constexpr int kQBox = BQ * 128;             // one [BQ x 64] box of Q_i / dO_i
@@ -90,7 +87,9 @@ struct BwdCfg {
   __device__ static constexpr uint32_t colDP(int b) { return 2 * D + b * 2 * BQ + BQ; }
   static constexpr uint32_t kTmemCols = 512;
   static_assert(2 * D + NB * 2 * BQ <= 512, "TMEM budget");
-  static_assert((kDqT ? BQ : D) <= BQ, "dQ partial must fit in the S^T columns");
+  // the dQ^T partial (BQ columns) reuses a buffer's S^T columns; at d = 64 the M = 128
+  // dQ^T product reads its second atom of K^T from the V tile right after K
+  static_assert(kVOff == kKOff + kKVBytes || D == 128, "V follows K");
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
 };
 
@@ -269,7 +268,7 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (lane == 0) {
       constexpr uint32_t idSP = idesc_bf16(BN, BQ, false, false);   // S^T, dP^T
       constexpr uint32_t idKV = idesc_bf16(BN, D, false, true);     // dV, dK
-      constexpr uint32_t idQ = C::kDqT ? idesc_bf16(D, BQ, true, true) : idesc_bf16(BQ, D, true, true);
+      constexpr uint32_t idQ = idesc_bf16(128, BQ, true, true);    // dQ^T: M = 128 rows of the head dim
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
       const uint32_t aStage = smem_u32(smem + C::kStageOff);
       const uint32_t aDs = smem_u32(smem + C::kDsOff);
@@ -310,85 +309,49 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         // issue order).
         const uint64_t dsd = sdesc_sw128(aDs + dsbuf * C::kDsBytes, BN * 128, 1024);
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          if constexpr (C::kDqT)
-            mma_ss(tmem + C::colS(b), sdesc_add(dK_mn, k * 2048), sdesc_add(dsd, k * 2048), idQ, k > 0);
-          else
-            mma_ss(tmem + C::colS(b), sdesc_add(dsd, k * 2048), sdesc_add(dK_mn, k * 2048), idQ, k > 0);
-        }
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ss(tmem + C::colS(b), sdesc_add(dK_mn, k * 2048), sdesc_add(dsd, k * 2048), idQ, k > 0);
       };
       bool ok = mbar_wait(&ctl.kv_full, 0, p.status, abort);
-      if constexpr (C::NB == 2) {
-        // Issue order per tile i (buffer b = i % 2):
-        //   dV(i), S(i+1), dK(i), dQ(i), dP(i+2)
-        // S(i+1) lands in the columns that held the partial dQ(i-1); placing dP(i+1) and
-        // dV(i) ahead of it gives the dQ warpgroup time to read that partial out, and the
-        // softmax of tile i+1 runs while dK(i), dQ(i) and dP(i+2) execute.
-        if (ok && nq > 0 && (ok = mbar_wait(&ctl.stage_full[0], 0, p.status, abort))) {
-          tc_fence_after();
-          issue_S(0, 0);
-          issue_dP(0, 0);
-          mma_commit(&ctl.s_full[0]);
+      // Issue order per tile i (buffer b = i % 2):
+      //   dV(i), S(i+1), dK(i), dQ(i), dP(i+2)
+      // S(i+1) lands in the columns that held the partial dQ(i-1); placing dP(i+1) and
+      // dV(i) ahead of it gives the dQ warpgroup time to read that partial out, and the
+      // softmax of tile i+1 runs while dK(i), dQ(i) and dP(i+2) execute.
+      if (ok && nq > 0 && (ok = mbar_wait(&ctl.stage_full[0], 0, p.status, abort))) {
+        tc_fence_after();
+        issue_S(0, 0);
+        issue_dP(0, 0);
+        mma_commit(&ctl.s_full[0]);
+      }
+      if (ok && nq > 1 && (ok = mbar_wait(&ctl.stage_full[1], 0, p.status, abort))) {
+        tc_fence_after();
+        issue_dP(1, 1);
+      }
+      for (int it = 0; ok && it < nq; ++it) {
+        const int s = it % C::kStages;
+        const int b = it & 1;
+        if (!(ok = mbar_wait(&ctl.sm_done[b], (it / 2) & 1, p.status, abort))) break;
+        tc_fence_after();
+        issue_dV_dK(it, b, s, false);
+        // The previous partial dQ(i-1) sits in buffer b^1's S^T columns; it must have been
+        // read out before S(i+1) overwrites them (and before dQ(i) is handed off, so the
+        // two hand-off barriers stay one phase apart).
+        if (it > 0 && !(ok = mbar_wait(&ctl.dq_empty, (it - 1) & 1, p.status, abort))) break;
+        tc_fence_after();
+        if (it + 1 < nq) {
+          issue_S((it + 1) % C::kStages, b ^ 1);  // stage it+1 was waited for with dP(i+1)
+          mma_commit(&ctl.s_full[b ^ 1]);
         }
-        if (ok && nq > 1 && (ok = mbar_wait(&ctl.stage_full[1], 0, p.status, abort))) {
+        issue_dV_dK(it, b, s, true);
+        issue_dQ(b, it & 1);
+        mma_commit(&ctl.dq_full);
+        mma_commit(&ctl.stage_empty[s]);
+        if (it + 2 < nq) {
+          const int s2 = (it + 2) % C::kStages;
+          if (!(ok = mbar_wait(&ctl.stage_full[s2], ((it + 2) / C::kStages) & 1, p.status, abort))) break;
           tc_fence_after();
-          issue_dP(1, 1);
-        }
-        for (int it = 0; ok && it < nq; ++it) {
-          const int s = it % C::kStages;
-          const int b = it & 1;
-          if (!(ok = mbar_wait(&ctl.sm_done[b], (it / 2) & 1, p.status, abort))) break;
-          tc_fence_after();
-          issue_dV_dK(it, b, s, false);
-          // The previous partial dQ(i-1) sits in buffer b^1's S^T columns; it must have been
-          // read out before S(i+1) overwrites them (and before dQ(i) is handed off, so the
-          // two hand-off barriers stay one phase apart).
-          if (it > 0 && !(ok = mbar_wait(&ctl.dq_empty, (it - 1) & 1, p.status, abort))) break;
-          tc_fence_after();
-          if (it + 1 < nq) {
-            issue_S((it + 1) % C::kStages, b ^ 1);  // stage it+1 was waited for with dP(i+1)
-            mma_commit(&ctl.s_full[b ^ 1]);
-          }
-          issue_dV_dK(it, b, s, true);
-          issue_dQ(b, it & 1);
-          mma_commit(&ctl.dq_full);
-          mma_commit(&ctl.stage_empty[s]);
-          if (it + 2 < nq) {
-            const int s2 = (it + 2) % C::kStages;
-            if (!(ok = mbar_wait(&ctl.stage_full[s2], ((it + 2) / C::kStages) & 1, p.status, abort))) break;
-            tc_fence_after();
-            issue_dP(s2, b);  // dP^T columns of buffer b: dS^T was read by dK above (issue order)
-          }
-        }
-      } else {
-        // One buffer: dV(i), dK(i), dQ(i) into the S^T columns, then dP(i+1), then S(i+1)
-        // once the partial has been read out.
-        if (ok && nq > 0 && (ok = mbar_wait(&ctl.stage_full[0], 0, p.status, abort))) {
-          tc_fence_after();
-          issue_S(0, 0);
-          issue_dP(0, 0);
-          mma_commit(&ctl.s_full[0]);
-        }
-        for (int it = 0; ok && it < nq; ++it) {
-          const int s = it % C::kStages;
-          if (!(ok = mbar_wait(&ctl.sm_done[0], it & 1, p.status, abort))) break;
-          tc_fence_after();
-          issue_dV_dK(it, 0, s, false);
-          issue_dV_dK(it, 0, s, true);
-          if (it > 0 && !(ok = mbar_wait(&ctl.dq_empty, (it - 1) & 1, p.status, abort))) break;
-          issue_dQ(0, it & 1);
-          mma_commit(&ctl.dq_full);
-          mma_commit(&ctl.stage_empty[s]);
-          if (it + 1 < nq) {
-            const int s2 = (it + 1) % C::kStages;
-            if (!(ok = mbar_wait(&ctl.stage_full[s2], ((it + 1) / C::kStages) & 1, p.status, abort))) break;
-            tc_fence_after();
-            issue_dP(s2, 0);  // dP^T columns: dS^T was read by dK above (issue order)
-            if (!(ok = mbar_wait(&ctl.dq_empty, it & 1, p.status, abort))) break;
-            tc_fence_after();
-            issue_S(s2, 0);   // S^T columns: the dQ partial has been read out
-            mma_commit(&ctl.s_full[0]);
-          }
+          issue_dP(s2, b);  // dP^T columns of buffer b: dS^T was read by dK above (issue order)
         }
       }
       mma_commit(&ctl.kv_done);
@@ -519,44 +482,27 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const int q0 = row_base + (q_first + it) * BQ;
       const int nvalid = p.N - (q_first + it) * BQ;  // queries of the tile inside the head
       const uint32_t colQ = C::colS(it % C::NB);
-      if constexpr (C::kDqT) {
-        // lane = head-dim index r; columns = the BQ queries of the tile, drained in two
-        // halves of 64 (the columns are released after the second load)
+      // lane = head-dim index r; columns = the BQ queries of the tile, released as soon as
+      // they are in registers
+      static_assert(BQ == 64, "one 64-column drain per tile");
+      float v[BQ];
+      tmem_ld32x2(tmem + lane_off + colQ, tmem + lane_off + colQ + 32, *reinterpret_cast<float(*)[32]>(&v[0]),
+                  *reinterpret_cast<float(*)[32]>(&v[32]));
+      tc_fence_before();
+      mbar_arrive(&ctl.dq_empty);
+      // At d = 64, TMEM lanes 64..127 (the warps with warp % 4 >= 2) hold no head-dim row:
+      // those warps skip the reductions, a branch that is uniform over each warp.
+      if (D == 128 || r < D) {
         float* dst = p.dQacc + (size_t)q0 * D + r;
-#pragma unroll 1
-        for (int h = 0; h < BQ; h += 64) {
-          float v[64];
-          tmem_ld32x2(tmem + lane_off + colQ + h, tmem + lane_off + colQ + h + 32,
-                      *reinterpret_cast<float(*)[32]>(&v[0]), *reinterpret_cast<float(*)[32]>(&v[32]));
-          if (h + 64 == BQ) {
-            tc_fence_before();
-            mbar_arrive(&ctl.dq_empty);
-          }
-          // Keep the bound test out of the reduction loop: a predicate inside it makes the
-          // compiler serialise the reductions (measured 1.7x slower backward).
-          if (!kTail || h + 64 <= nvalid) {
+        // Keep the bound test out of the reduction loop: a predicate inside it makes the
+        // compiler serialise the reductions (measured 1.7x slower backward).
+        if (!kTail || BQ <= nvalid) {
 #pragma unroll 16
-            for (int c = 0; c < 64; ++c) atomicAdd(dst + (size_t)(h + c) * D, v[c]);
-          } else {  // the last, partial tile of a head
+          for (int c = 0; c < BQ; ++c) atomicAdd(dst + (size_t)c * D, v[c]);
+        } else {  // the last, partial tile of a head
 #pragma unroll 16
-            for (int c = 0; c < 64; ++c)
-              if (h + c < nvalid) atomicAdd(dst + (size_t)(h + c) * D, v[c]);
-          }
-        }
-      } else {
-        // lane = query row r of the tile; columns = head dim
-        float v[D];
-#pragma unroll
-        for (int c = 0; c < D; c += 64)
-          tmem_ld32x2(tmem + lane_off + colQ + c, tmem + lane_off + colQ + c + 32,
-                      *reinterpret_cast<float(*)[32]>(&v[c]), *reinterpret_cast<float(*)[32]>(&v[c + 32]));
-        tc_fence_before();
-        mbar_arrive(&ctl.dq_empty);
-        float4* dst = reinterpret_cast<float4*>(p.dQacc + (size_t)(q0 + r) * D);
-        if (!kTail || r < nvalid) {
-#pragma unroll
-          for (int c = 0; c < D / 4; ++c)
-            atomicAdd(dst + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+          for (int c = 0; c < BQ; ++c)
+            if (c < nvalid) atomicAdd(dst + (size_t)c * D, v[c]);
         }
       }
     }
