@@ -3,7 +3,7 @@
 The keep bits are Philox-4x32-10 on both sides (oracle/philox.py and the kernels'
 philox.cuh, written separately from the same published definition), so the dropped
 attention is the same function of the inputs, and the tolerances are those of every bf16
-test with one derived change: kept weights are multiplied by c = 65536 / (65536 - t), which
+test with one derived change: kept weights are multiplied by c = 256 / (256 - t), which
 scales O and every rounding error in it (the bf16 weights, the bf16 output) by c, so O's
 max-abs bound is 2e-2 * c. LSE 1e-3 and dQ/dK/dV relative Frobenius 2e-2 are unchanged
 (LSE is the undropped softmax's; the relative norms do not see the scale). Two tests read the keep
