@@ -1,8 +1,8 @@
 // fa_fwd_bwd_host: forward + backward of host-resident tensors, with the host<->device
 // copies overlapped with the kernels.
 //
-// The heads are independent, so the call cuts the B*H heads into `chunks` contiguous
-// groups and runs each group through three stages on three internal streams:
+// The heads are independent, so the call cuts the B*H heads into contiguous groups and runs
+// each group through three stages on three internal streams:
 //   copy-in  : Q, K, V, dO of the group, host -> device slot
 //   compute  : fa_fwd, fa_bwd_preprocess, fa_bwd on the slot (the group as B = 1, H = heads)
 //   copy-out : O, LSE, dQ, dK, dV of the group, device slot -> host
@@ -13,6 +13,9 @@
 // copy-out has read it. The call forks from the caller's stream (the internal
 // streams wait on an event recorded there) and joins back into it (the caller's stream
 // waits on the last copy-out), so it enqueues work and returns without synchronising.
+//
+// Only the first group's copy-in and the last group's copy-out overlap no kernel, so the
+// default schedule makes those two groups half the size of the others (1:2:2:2:1).
 #include <algorithm>
 #include <mutex>
 
@@ -83,9 +86,32 @@ DeviceQueues* queues_for_current_device() {
   return &q;
 }
 
-int chunk_count(int64_t heads, int chunks) {
-  const int c = chunks <= 0 ? 4 : chunks;
-  return (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)c, heads, (int64_t)kMaxChunks}));
+// Group g holds heads start[g] .. start[g+1] - 1.
+struct Groups {
+  int n = 0;
+  int64_t start[kMaxChunks + 1] = {};
+  int64_t largest = 0;
+};
+
+// chunks > 0: that many equal groups (at most B*H and 16; the last may be smaller).
+// chunks == 0: with at least 8 heads, five groups in the ratio 1:2:2:2:1; else up to 4
+// equal groups.
+Groups make_groups(int64_t heads, int chunks) {
+  Groups g;
+  if (chunks <= 0 && heads >= 8) {
+    const int64_t q = heads / 8, rem = heads - 2 * q;
+    const int64_t size[5] = {q, rem / 3 + (rem % 3 > 0), rem / 3 + (rem % 3 > 1), rem / 3, q};
+    g.n = 5;
+    for (int i = 0; i < 5; ++i) g.start[i + 1] = g.start[i] + size[i];
+  } else {
+    const int c = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)(chunks <= 0 ? 4 : chunks), heads,
+                                                               (int64_t)kMaxChunks}));
+    const int64_t hc = (heads + c - 1) / c;
+    g.n = (int)((heads + hc - 1) / hc);
+    for (int i = 0; i < g.n; ++i) g.start[i + 1] = std::min<int64_t>(heads, g.start[i] + hc);
+  }
+  for (int i = 0; i < g.n; ++i) g.largest = std::max(g.largest, g.start[i + 1] - g.start[i]);
+  return g;
 }
 
 }  // namespace
@@ -93,10 +119,8 @@ int chunk_count(int64_t heads, int chunks) {
 
 extern "C" size_t fa_fwd_bwd_host_workspace_size(int B, int H, int N, int d, int dtype, int chunks) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || dtype != FA_DTYPE_BF16) return 0;
-  const int64_t heads = (int64_t)B * H;
-  const int c = fa::chunk_count(heads, chunks);
-  const int64_t hc = (heads + c - 1) / c;
-  return 2 * fa::slot_layout(hc, N, d).bytes;
+  const fa::Groups g = fa::make_groups((int64_t)B * H, chunks);
+  return 2 * fa::slot_layout(g.largest, N, d).bytes;
 }
 
 extern "C" fa_status_t fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const void* dO, void* O,
@@ -116,11 +140,9 @@ extern "C" fa_status_t fa_fwd_bwd_host(const void* Q, const void* K, const void*
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
 
-  const int64_t heads = (int64_t)B * H;
-  const int nc = fa::chunk_count(heads, chunks);
-  const int64_t hc = (heads + nc - 1) / nc;
-  const int ng = (int)((heads + hc - 1) / hc);  // groups actually formed (<= nc)
-  const fa::SlotLayout L = fa::slot_layout(hc, N, d);
+  const fa::Groups G = fa::make_groups((int64_t)B * H, chunks);
+  const int ng = G.n;
+  const fa::SlotLayout L = fa::slot_layout(G.largest, N, d);
   const size_t head_el = (size_t)N * d * 2, head_rows = (size_t)N * 4;
 
   std::lock_guard<std::mutex> lock(fa::g_mu);
@@ -143,7 +165,7 @@ extern "C" fa_status_t fa_fwd_bwd_host(const void* Q, const void* K, const void*
 
   cudaEvent_t out_done[fa::kMaxChunks] = {};
   for (int g = 0; g < ng; ++g) {
-    const int64_t h0 = g * hc, nh = std::min<int64_t>(hc, heads - h0);
+    const int64_t h0 = G.start[g], nh = G.start[g + 1] - h0;
     char* slot = static_cast<char*>(workspace) + (size_t)(g & 1) * L.bytes;
     const size_t el = (size_t)nh * head_el, rows = (size_t)nh * head_rows;
     const size_t off = (size_t)h0 * head_el, roff = (size_t)h0 * head_rows;

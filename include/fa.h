@@ -224,7 +224,10 @@ FA_API fa_status_t fa_fwd_fp8(const void* Q, const void* K, const void* V, void*
 /*
  * fa_fwd_bwd_host — forward and backward of tensors that live in host memory: the
  * copies to and from the device overlap the kernels. The heads (independent of one
- * another) are cut into `chunks` contiguous groups (0 = 4; at most 16 and at most B*H);
+ * another) are cut into contiguous groups: `chunks` equal ones (at most 16 and at most
+ * B*H), or with chunks = 0 five groups in the ratio 1:2:2:2:1 when B*H >= 8 (the first
+ * group's copy-in and the last one's copy-out overlap no kernel, so they are the small
+ * ones) and up to 4 equal groups otherwise;
  * each group is copied in (Q, K, V, dO), run through fa_fwd, fa_bwd_preprocess and fa_bwd,
  * and copied out (O, LSE, dQ, dK, dV) on three internal streams, with two device slots
  * in `workspace` alternating, so one group's copies run while another's kernels do.
