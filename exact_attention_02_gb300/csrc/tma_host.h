@@ -21,21 +21,6 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A [rows x cols] row-major bf16 matrix, loaded as boxes of 64 columns x box_rows rows
-// with the 128-byte swizzle (one box = box_rows x 128 bytes in shared memory).
-inline bool make_map_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
-                             int box_rows) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // [heads x N x cols] bf16 (contiguous), loaded as boxes of 64 columns x box_rows rows of
 // one head with the 128-byte swizzle. Rows past N inside a head read as zeros, so a tile
 // that straddles the end of a head never picks up the next head's rows.
