@@ -49,7 +49,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BN = 128;  // keys per tile
+constexpr int BN = 128;  // keys per S^T product (the MMA's M)
 constexpr int NQP = 64;  // queries padded to the MMA's N
 constexpr int kSoftThreads = 256;  // two groups of four softmax warps
 constexpr int kThreads = kSoftThreads + 64;
@@ -59,23 +59,33 @@ constexpr float kNegM0 = 1e30f;  // -m of a query before its first visible score
 
 constexpr int kBoxBytes = BN * 128;           // [128 rows x 64 bf16]
 constexpr int kQBox = NQP * 128;              // [64 rows x 64 bf16]
-constexpr int kPBytes = BN * NQP * 2;         // P^T [128 keys x 64 queries] bf16
 constexpr int kMaxStages = 8;
 
 // Shared-memory layout by head dimension (1024-byte aligned base).
 template <int D>
 struct Cfg {
-  static constexpr int kBoxes = D / 64;               // 64-column boxes per row
-  static constexpr int kTile = kBoxes * kBoxBytes;    // one K or V stage
-  // K is read a tile before V, so it gets the deeper ring
-  static constexpr int kKStages = D == 128 ? 3 : 4;
-  static constexpr int kVStages = D == 128 ? 2 : 4;
+  static constexpr int kBoxes = D / 64;                // 64-column boxes per row
+  // A tile is 32 KB of K (or V): 128 keys at d = 128, 256 keys at d = 64, where S^T takes
+  // two M = 128 products (keys 0..127 and 128..255) and each softmax thread two keys.
+  static constexpr int kHalves = D == 64 ? 2 : 1;
+  static constexpr int kTileKeys = BN * kHalves;
+  static constexpr int kBoxBytesT = kTileKeys * 128;   // one 64-column box of a tile
+  static constexpr int kTile = kBoxes * kBoxBytesT;    // one K or V stage
+  static constexpr int kPTile = kTileKeys * NQP * 2;   // P^T [tile keys x 64 queries] bf16
+  static constexpr int kPBufs = 2;                     // P^T buffers
+  // K is read a tile before V, so it gets the deeper ring where shared memory allows (at
+  // d = 64 the two P^T tiles of 32 KB leave room for two stages of each)
+  static constexpr int kKStages = D == 64 ? 2 : 3;
+  static constexpr int kVStages = 2;
+  static constexpr int kSCols = kHalves * NQP;         // TMEM columns of one S^T buffer
+  static constexpr uint32_t kColO = 2 * kSCols;        // O^T after the two S^T buffers
+  static constexpr uint32_t kTmemCols = kColO + NQP <= 256 ? 256 : 512;
   static constexpr int kQBytes = kBoxes * kQBox;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kKStages * kTile;
   static constexpr int kQOff = kVOff + kVStages * kTile;
   static constexpr int kPOff = kQOff + kQBytes;
-  static constexpr int kCorrOff = kPOff + 2 * kPBytes;   // float[64] rescale factors
+  static constexpr int kCorrOff = kPOff + kPBufs * kPTile;  // float[64] rescale factors
   static constexpr int kNmOff = kCorrOff + 4 * NQP;      // float[64] -m per query (log2 units)
   static constexpr int kNmtOff = kNmOff + 4 * NQP;       // float[64] -(m + threshold) per query
   static constexpr int kRedOff = kNmtOff + 4 * NQP;      // float[4][64] cross-warp scratch
@@ -83,12 +93,12 @@ struct Cfg {
   static constexpr int kSmemBytes = kFlagOff + 64 + 1024;
   static_assert(kKStages <= kMaxStages && kVStages <= kMaxStages, "stages");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-  // the second 64-row atom of V^T (kBoxBytes past the stage) stays inside the allocation
-  static_assert(kVOff + kVStages * kTile + kBoxBytes <= kSmemBytes - 1024, "V^T atom");
+  // the second 64-row atom of V^T (kBoxBytes past each k-step's rows) stays inside the
+  // allocation, also for the last k-step of the last V stage
+  static_assert(kVOff + (kVStages - 1) * kTile + kBoxBytes + kBoxBytesT <= kSmemBytes - 1024, "V^T atom");
 };
 
-constexpr uint32_t kColS0 = 0, kColO = 2 * NQP;  // S buffers [0,128), O^T [128,192)
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS0 = 0;  // S^T buffers, then O^T (Cfg::kColO)
 
 struct TcParams {
   float* part_o;   // [heads][P][nq][d]
@@ -191,10 +201,10 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     ctl.abort = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) tmem_alloc(&ctl.tmem_base, kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&ctl.tmem_base, C::kTmemCols);
   if (threadIdx.x < kSoftThreads) {
     // P^T columns no group writes (queries past 2C) stay zero for every PV product
-    for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += kSoftThreads)
+    for (int i = threadIdx.x; i < C::kPBufs * C::kPTile / 16; i += kSoftThreads)
       reinterpret_cast<uint4*>(smem + C::kPOff)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
@@ -233,12 +243,12 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
           for (int b = 0; b < D / 64; ++b) tma_load_3d(smem + C::kQOff + b * kQBox, &tmQ, &ctl.q_full, b * 64, 0, (int)h);
           last_q = seg;
         }
-        for (int kt = k0; ok && kt < k1; kt += BN, ++t) {
+        for (int kt = k0; ok && kt < k1; kt += C::kTileKeys, ++t) {
           const int s = t % stages;
           if (t >= stages && !(ok = mbar_wait(&empty[s], ((t / stages) - 1) & 1, p.status, abort))) break;
           mbar_expect_tx(&full[s], C::kTile);
           for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(ring + s * C::kTile + b * kBoxBytes, map, &full[s], b * 64, kt, (int)h);
+            tma_load_3d(ring + s * C::kTile + b * C::kBoxBytesT, map, &full[s], b * 64, kt, (int)h);
           last[s] = t;
         }
         ++seg;
@@ -257,20 +267,24 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
       const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::kVOff), kBoxBytes, 1024);
-      const uint64_t dP0 = sdesc_sw128(smem_u32(smem + C::kPOff), kPBytes, 1024);
+      const uint64_t dP0 = sdesc_sw128(smem_u32(smem + C::kPOff), C::kPTile, 1024);
       auto issue_S = [&](int t) {
         const uint32_t ko = (t % C::kKStages) * C::kTile;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * kBoxBytes + (k % 4) * 32, qoff = (k / 4) * kQBox + (k % 4) * 32;
-          mma_ss(tmem + kColS0 + (t & 1) * NQP, sdesc_add(dK0, ko + off), sdesc_add(dQ0, qoff), idS, k > 0);
-        }
+        for (int hb = 0; hb < C::kHalves; ++hb)  // keys 128*hb .. +127 of the tile
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k / 4) * C::kBoxBytesT + hb * (BN * 128) + (k % 4) * 32,
+                           qoff = (k / 4) * kQBox + (k % 4) * 32;
+            mma_ss(tmem + kColS0 + (t & 1) * C::kSCols + hb * NQP, sdesc_add(dK0, ko + off), sdesc_add(dQ0, qoff),
+                   idS, k > 0);
+          }
       };
       auto issue_PV = [&](int t, bool acc) {
-        const uint32_t vo = (t % C::kVStages) * C::kTile, po = (t & 1) * kPBytes;
+        const uint32_t vo = (t % C::kVStages) * C::kTile, po = (t % C::kPBufs) * C::kPTile;
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          mma_ss(tmem + kColO, sdesc_add(dV0, vo + k * 2048), sdesc_add(dP0, po + k * 2048), idO,
+        for (int k = 0; k < C::kTileKeys / 16; ++k)
+          mma_ss(tmem + C::kColO, sdesc_add(dV0, vo + k * 2048), sdesc_add(dP0, po + k * 2048), idO,
                  (acc || k > 0) ? 1u : 0u);
       };
       SegIter it{g_begin, g_end, p.Nk};
@@ -278,7 +292,7 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       int k0, k1, seg = 0, t = 0;
       bool ok = true;
       while (ok && it.next(h, k0, k1)) {
-        const int n = (k1 - k0 + BN - 1) / BN;  // tiles in this segment: t .. t + n - 1
+        const int n = (k1 - k0 + C::kTileKeys - 1) / C::kTileKeys;  // tiles in this segment: t .. t + n - 1
         if (!(ok = mbar_wait(&ctl.q_full, seg & 1, p.status, abort))) break;
         if (!(ok = mbar_wait(&ctl.k_full[t % C::kKStages], (t / C::kKStages) & 1, p.status, abort))) break;
         tc_fence_after();
@@ -333,7 +347,7 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       // After a failed (timed-out) wait the loops keep their shape, skipping the waits and
       // the TMEM accesses, so that every warp of the group still reaches every named barrier.
       while (it.next(h, k0, k1)) {
-        const int n = (k1 - k0 + BN - 1) / BN;
+        const int n = (k1 - k0 + C::kTileKeys - 1) / C::kTileKeys;
         if (r < kCols) {
           nm[q0 + r] = kNegM0;
           nmt[q0 + r] = kNegM0;  // -(m + threshold) rounds to the same value
@@ -344,38 +358,48 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         group_sync(g);
         for (int i = 0; i < n; ++i, ++t) {
           if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full[t & 1], (t >> 1) & 1, p.status, abort));
-          float x[kCols];
-          if (ok) {
-            tc_fence_after();
-            tmem_ld_cols<kCols>(tmem + lane_off + kColS0 + (t & 1) * NQP + q0, x);
-          } else {
+          // x[hb] holds the raw scores q.k of key 128*hb + r of the tile; masked ones become
+          // -inf (scaled: still -inf)
+          float x[C::kHalves][kCols];
 #pragma unroll
-            for (int q = 0; q < kCols; ++q) x[q] = 0.f;
+          for (int hb = 0; hb < C::kHalves; ++hb) {
+            if (ok) {
+              tc_fence_after();
+              tmem_ld_cols<kCols>(tmem + lane_off + kColS0 + (t & 1) * C::kSCols + hb * NQP + q0, x[hb]);
+            } else {
+#pragma unroll
+              for (int q = 0; q < kCols; ++q) x[hb][q] = 0.f;
+            }
           }
-          // x holds raw scores q.k; masked ones become -inf (scaled: still -inf)
-          const int kb = k0 + i * BN;  // first key of the tile
-          const bool full = ok && kb + BN <= k1 && q0 + kCols <= nq && (!p.causal || kb + BN - 1 <= q0 + p.offset);
+          const int kb = k0 + i * C::kTileKeys;  // first key of the tile
+          const bool full = ok && kb + C::kTileKeys <= k1 && q0 + kCols <= nq &&
+                            (!p.causal || kb + C::kTileKeys - 1 <= q0 + p.offset);
           if (!full) {
-            const int key = kb + r;
-            const bool kin = key < k1;
 #pragma unroll
-            for (int q = 0; q < kCols; ++q) {
-              const int qg = q0 + q;
-              const bool vis = ok && kin && qg < nq && !(p.causal && key > qg + p.offset);
-              x[q] = vis ? x[q] : -INFINITY;
+            for (int hb = 0; hb < C::kHalves; ++hb) {
+              const int key = kb + hb * BN + r;
+              const bool kin = key < k1;
+#pragma unroll
+              for (int q = 0; q < kCols; ++q) {
+                const int qg = q0 + q;
+                const bool vis = ok && kin && qg < nq && !(p.causal && key > qg + p.offset);
+                x[hb][q] = vis ? x[hb][q] : -INFINITY;
+              }
             }
           }
           // does any score of the tile exceed its query's reference max by the threshold?
           const float4* nmt4 = reinterpret_cast<const float4*>(nmt + q0);
           float e = -INFINITY;
 #pragma unroll
-          for (int q = 0; q < kCols; q += 4) {
-            const float4 t4 = nmt4[q / 4];
-            const float2 a = ffma2(make_float2(x[q], x[q + 1]), sl2x2, make_float2(t4.x, t4.y));
-            const float2 b = ffma2(make_float2(x[q + 2], x[q + 3]), sl2x2, make_float2(t4.z, t4.w));
-            e = fmax3(e, a.x, a.y);
-            e = fmax3(e, b.x, b.y);
-          }
+          for (int hb = 0; hb < C::kHalves; ++hb)
+#pragma unroll
+            for (int q = 0; q < kCols; q += 4) {
+              const float4 t4 = nmt4[q / 4];
+              const float2 a = ffma2(make_float2(x[hb][q], x[hb][q + 1]), sl2x2, make_float2(t4.x, t4.y));
+              const float2 b = ffma2(make_float2(x[hb][q + 2], x[hb][q + 3]), sl2x2, make_float2(t4.z, t4.w));
+              e = fmax3(e, a.x, a.y);
+              e = fmax3(e, b.x, b.y);
+            }
           const bool grow = __any_sync(0xffffffffu, e > 0.f);
           int* fl = flags + (t & 1) * 8 + 4 * g;
           if (lane == 0) fl[wq] = grow ? 1 : 0;
@@ -384,7 +408,10 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             // exact column maxima of the tile: warp reduction, then across the group's warps
 #pragma unroll
             for (int q = 0; q < kCols; ++q) {
-              float v = x[q] * sl2;
+              float v = x[0][q];
+#pragma unroll
+              for (int hb = 1; hb < C::kHalves; ++hb) v = fmaxf(v, x[hb][q]);
+              v *= sl2;
 #pragma unroll
               for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
               if (lane == 0) red[wq * NQP + q0 + q] = v;
@@ -409,38 +436,43 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
               if (ok) {
                 tc_fence_after();
                 float ov[kCols];
-                tmem_ld_cols<kCols>(tmem + lane_off + kColO + q0, ov);
+                tmem_ld_cols<kCols>(tmem + lane_off + C::kColO + q0, ov);
                 uint32_t w[kCols];
 #pragma unroll
                 for (int q = 0; q < kCols; ++q) w[q] = __float_as_uint(ov[q] * corr[q0 + q]);
-                tmem_st_cols<kCols>(tmem + lane_off + kColO + q0, w);
+                tmem_st_cols<kCols>(tmem + lane_off + C::kColO + q0, w);
                 tmem_wait_st();
               }
             }
           }
-          // The P^T buffer of this tile was last read by PV(t - 2).
-          if (t >= 2 && ok)
-            ok = __all_sync(0xffffffffu, mbar_wait(&ctl.pv_done[t & 1], ((t - 2) >> 1) & 1, p.status, abort));
-          // p = 2^(s - m) <= 2^threshold; the group's 2C bytes of P^T row r (128-byte swizzle)
-          uint8_t* prow = smem + C::kPOff + (t & 1) * kPBytes + r * 128;
+          // The P^T buffer of this tile was last read by PV(t - kPBufs).
+          if (t >= C::kPBufs && ok)
+            ok = __all_sync(0xffffffffu, mbar_wait(&ctl.pv_done[(t - C::kPBufs) & 1], ((t - C::kPBufs) >> 1) & 1,
+                                                   p.status, abort));
+          // p = 2^(s - m) <= 2^threshold; the group's 2C bytes of P^T rows 128*hb + r
+          // (128-byte swizzle; those rows share r's position in their group of 8)
           const float4* nm4 = reinterpret_cast<const float4*>(nm + q0);
 #pragma unroll
-          for (int c = 0; c < kCols / 8; ++c) {
-            uint32_t w[4];
+          for (int hb = 0; hb < C::kHalves; ++hb) {
+            uint8_t* prow = smem + C::kPOff + (t % C::kPBufs) * C::kPTile + (hb * BN + r) * 128;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int q = c * 8 + 2 * u;
-              const float4 m4 = nm4[q / 4];
-              const float2 a = ffma2(make_float2(x[q], x[q + 1]), sl2x2,
-                                     (u & 1) ? make_float2(m4.z, m4.w) : make_float2(m4.x, m4.y));
-              const float p0 = ex2(a.x), p1 = ex2(a.y);
-              const float2 ls = fadd2(make_float2(l[q], l[q + 1]), make_float2(p0, p1));
-              l[q] = ls.x;
-              l[q + 1] = ls.y;
-              w[u] = pack_bf16(p0, p1);
+            for (int c = 0; c < kCols / 8; ++c) {
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int q = c * 8 + 2 * u;
+                const float4 m4 = nm4[q / 4];
+                const float2 a = ffma2(make_float2(x[hb][q], x[hb][q + 1]), sl2x2,
+                                       (u & 1) ? make_float2(m4.z, m4.w) : make_float2(m4.x, m4.y));
+                const float p0 = ex2(a.x), p1 = ex2(a.y);
+                const float2 ls = fadd2(make_float2(l[q], l[q + 1]), make_float2(p0, p1));
+                l[q] = ls.x;
+                l[q + 1] = ls.y;
+                w[u] = pack_bf16(p0, p1);
+              }
+              const int chunk = q0 / 8 + c;
+              *reinterpret_cast<uint4*>(prow + ((chunk ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            const int chunk = q0 / 8 + c;
-            *reinterpret_cast<uint4*>(prow + ((chunk ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
           fence_proxy_async_smem();
           tc_fence_before();
@@ -469,7 +501,7 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         if (ok) {
           tc_fence_after();
           float ov[kCols];
-          tmem_ld_cols<kCols>(tmem + lane_off + kColO + q0, ov);  // warp-collective: every lane loads
+          tmem_ld_cols<kCols>(tmem + lane_off + C::kColO + q0, ov);  // warp-collective: every lane loads
           if (r < D) {  // O^T lanes past d hold V^T's zero rows
 #pragma unroll
             for (int q = 0; q < kCols; ++q)
@@ -490,7 +522,7 @@ splitkv_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -519,7 +551,8 @@ cudaError_t splitkv_tc_partial(const void* Q, const void* K, const void* V, int6
                                int* status, cudaStream_t st) {
   if (d != 64 && d != 128) return cudaErrorInvalidValue;
   CUtensorMap mk, mv, mq;
-  if (!make_map_bf16_3d(&mk, K, heads, Nk, d, BN) || !make_map_bf16_3d(&mv, V, heads, Nk, d, BN) ||
+  const int tile_keys = d == 64 ? Cfg<64>::kTileKeys : Cfg<128>::kTileKeys;
+  if (!make_map_bf16_3d(&mk, K, heads, Nk, d, tile_keys) || !make_map_bf16_3d(&mv, V, heads, Nk, d, tile_keys) ||
       !make_map_bf16_3d(&mq, Q, heads, Nq, d, NQP))
     return cudaErrorInvalidValue;
   TcParams p;
