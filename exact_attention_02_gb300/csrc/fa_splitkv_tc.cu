@@ -1,13 +1,13 @@
 // Split-KV forward on the tensor cores, for 1..64 queries against a long key/value
 // sequence (d = 64 or 128): the same partial states and merge as fa_splitkv.cu, with the
-// two products of each 128-key tile on tcgen05.
+// two products of each key tile on tcgen05.
 //
 // Work split (chosen by fa_splitkv.cu): one CTA per SM takes an equal contiguous range of L
 // keys of the flattened (head, key) sequence; each piece of a head inside the range is a
 // segment with its own partial state (m, l, O) per query, stored in slot (head, CTA - first
 // CTA of the head) and merged afterwards by splitkv_merge_kernel.
 //
-// Per 128-key tile (keys on the MMA's M side, queries on N, padded to 64 with zero rows):
+// Per 128 keys of a tile (keys on the MMA's M side, queries on N, padded to 64 with zero rows):
 //   S^T = K Q^T           M = 128 keys, N = 64, K = d: one TMEM accumulator [keys x queries]
 //   softmax               one thread per (key = TMEM lane, query group): scores in log2
 //                         units, masked keys -inf; per query a running max m_q, refreshed
@@ -31,11 +31,12 @@
 // barriers it would arrive on count only the groups that have queries.
 // Rows: K/V through 3-D maps [heads, N_k, d] (rows past the end of a head read as zeros),
 // Q through [heads, N_q, d] with 64-row boxes (rows past N_q read as zeros).
-// d = 64 loads one 64-column box per tile into 16 KB stages (twice as many as d = 128 has):
-// S^T takes 4 k-steps instead of 8, and O^T += V^T P^T stays an M = 128 product whose
-// second 64-row atom reads the 16 KB that follow the V stage in shared memory. Those rows
-// land in O^T lanes 64..127, which nothing reads (each output row depends only on its own
-// row of V^T).
+// A tile is 32 KB of K (or V): 128 keys at d = 128; 256 keys at d = 64, as one 64-column
+// box, where S^T is two M = 128 products (4 k-steps each) and each softmax thread owns
+// keys r and 128 + r, so a d = 64 tile carries as many bytes per synchronisation as a
+// d = 128 one. At d = 64, O^T += V^T P^T stays an M = 128 product whose second 64-row
+// atom reads 16 KB further into shared memory; those rows land in O^T lanes 64..127,
+// which nothing reads (each output row depends only on its own row of V^T).
 #include <cuda_bf16.h>
 
 #include <algorithm>
