@@ -15,6 +15,7 @@ Multi-GPU (torchrun): each rank runs its own copy of the workload (attention hea
 independent; no collective on the data path); value = all ranks' FLOPs / max time.
 """
 import os
+import platform
 
 os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
 
@@ -108,6 +109,24 @@ def oracle_head_step(w, x, b, h):
     ora.head_backward(*args, w.scale, w.causal)
 
 
+def cpu_model():
+    """The host CPU's model name as lscpu reports it (/proc/cpuinfo as a fallback)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline(w, x, budget_s=12.0, max_heads=8):
     """The oracle, as it stands, on whole heads of the workload until ~budget_s."""
     flop_head = (w.fwd_flop() + w.bwd_flop()) / (w.B * w.H)
@@ -118,7 +137,8 @@ def cpu_baseline(w, x, budget_s=12.0, max_heads=8):
         n += 1
     dt = time.perf_counter() - t0
     return {"value": flop_head * n / dt / 1e12, "unit": "TFLOP/s",
-            "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1)), "kind": "oracle",
+            "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1)), "cpu": cpu_model(),
+            "kind": "oracle",
             "sample": f"{n} whole head(s) of the workload (fwd+bwd, fp64 numpy), {dt:.1f} s; "
                       f"FLOPs counted by the same convention as the GPU line"}
 
@@ -144,7 +164,7 @@ def run_reference(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "step": "one whole head (fwd+bwd) of the workload per step, fp64 numpy oracle on the host"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "cpu": cpu_model(), "kind": "oracle",
                          "sample": "one head of the workload per step"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
