@@ -67,6 +67,10 @@ def _load():
     L.fa_fwd_masked.restype = i
     L.fa_bwd_masked.argtypes = [vp] * 11 + [ll, ll, ll, vp, sz, i, i, i, i, f, i, i, vp]
     L.fa_bwd_masked.restype = i
+    L.fa_fwd_bitmask.argtypes = [vp] * 6 + [ll, ll, ll, i, i, i, i, f, i, i, vp]
+    L.fa_fwd_bitmask.restype = i
+    L.fa_bwd_bitmask.argtypes = [vp] * 11 + [ll, ll, ll, vp, sz, i, i, i, i, f, i, i, vp]
+    L.fa_bwd_bitmask.restype = i
     ull = ctypes.c_ulonglong
     L.fa_fwd_dropout.argtypes = [vp] * 5 + [i, i, i, i, f, i, f, ull, i, vp]
     L.fa_fwd_dropout.restype = i
@@ -163,19 +167,57 @@ def _mask_args(mask, q):
     return _p(mask), sb, sh, srow
 
 
+def pack_mask_bits(visible):
+    """The int32 words ``fa_fwd_bitmask`` reads for a boolean [B|1, H|1, N, N] tensor
+    (True: the key is visible): bit j % 32 of word j / 32 of each row, each row padded to
+    4 words per 128 keys. Returns [B|1, H|1, N, 4 * ceil(N / 128)] on visible's device."""
+    import torch
+    n = int(visible.shape[-1])
+    words = (n + 127) // 128 * 4
+    lead = tuple(visible.shape[:-1])
+    v = torch.zeros(lead + (words * 32,), dtype=torch.int64, device=visible.device)
+    v[..., :n] = visible.to(torch.int64)
+    w = (v.view(lead + (words, 32)) << torch.arange(32, dtype=torch.int64, device=visible.device)).sum(-1)
+    return torch.where(w >= 2 ** 31, w - 2 ** 32, w).to(torch.int32)
+
+
+def _bits_args(bits, q):
+    """Pointer and word strides (batch, head, row) of packed mask bits for q's shape."""
+    import torch
+    B, H, N, _ = _shape(q)
+    if bits.dim() != 4 or bits.dtype != torch.int32 or bits.device != q.device:
+        raise ValueError("mask_bits must be an int32 [B or 1, H or 1, N, words] tensor on q's device")
+    mb, mh, mn, mw = (int(x) for x in bits.shape)
+    if mb not in (1, B) or mh not in (1, H) or mn != N or mw < (N + 127) // 128 * 4 or bits.stride(3) != 1:
+        raise ValueError("mask_bits must be [B or 1, H or 1, N, >= 4 * ceil(N / 128)] with contiguous rows: "
+                         "use pack_mask_bits(visible)")
+    srow = int(bits.stride(2))
+    sb = 0 if mb == 1 else int(bits.stride(0))
+    sh = 0 if mh == 1 else int(bits.stride(1))
+    if srow % 4 or sb % 4 or sh % 4:
+        raise ValueError("mask_bits strides must be multiples of 4 words")
+    return _p(bits), sb, sh, srow
+
+
 def fa_fwd(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None, stream=None, mask=None,
-           dropout: tuple[float, int] | None = None):
+           dropout: tuple[float, int] | None = None, mask_bits=None):
     """O, LSE = attention forward of [B, H, N, d] CUDA tensors (see ``fa_fwd`` in fa.h).
     With ``mask`` (bf16 [B|1, H|1, N, N], added to the scaled scores) it calls
-    ``fa_fwd_masked``; with ``dropout = (p, seed)`` it calls ``fa_fwd_dropout``."""
+    ``fa_fwd_masked``; with ``mask_bits`` (a boolean mask packed by ``pack_mask_bits``)
+    ``fa_fwd_bitmask``; with ``dropout = (p, seed)`` it calls ``fa_fwd_dropout``."""
     import torch
     B, H, N, d = _shape(q)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _same(q, k, v, o)
-    if mask is not None and dropout is not None:
-        raise ValueError("a mask and dropout in one call are not supported")
+    if sum(x is not None for x in (mask, mask_bits, dropout)) > 1:
+        raise ValueError("only one of mask, mask_bits and dropout per call is supported")
+    if mask_bits is not None:
+        bp, sb, sh, srow = _bits_args(mask_bits, q)
+        _check(_load().fa_fwd_bitmask(_p(q), _p(k), _p(v), _p(o), _p(lse), bp, sb, sh, srow, B, H, N, d, scale,
+                                      int(bool(causal)), _dtype_code(q), _stream_ptr(stream)), "fa_fwd_bitmask")
+        return o, lse
     if dropout is not None:
         pd, seed = float(dropout[0]), int(dropout[1]) & 0xFFFFFFFFFFFFFFFF
         _check(_load().fa_fwd_dropout(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, N, d, scale, int(bool(causal)), pd,
@@ -210,9 +252,10 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int, dtype) -> int:
 
 def fa_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None, D=None,
            dq=None, dk=None, dv=None, workspace=None, stream=None, mask=None,
-           dropout: tuple[float, int] | None = None):
+           dropout: tuple[float, int] | None = None, mask_bits=None):
     """dQ, dK, dV of attention from the forward's O and LSE (see ``fa_bwd`` in fa.h);
     with ``mask`` (the forward's additive mask) it calls ``fa_bwd_masked``, with
+    ``mask_bits`` (the forward's packed boolean mask) ``fa_bwd_bitmask``, with
     ``dropout`` (the forward's (p, seed)) ``fa_bwd_dropout``."""
     import torch
     B, H, N, d = _shape(q)
@@ -225,8 +268,14 @@ def fa_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None, D=None
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    if mask is not None and dropout is not None:
-        raise ValueError("a mask and dropout in one call are not supported")
+    if sum(x is not None for x in (mask, mask_bits, dropout)) > 1:
+        raise ValueError("only one of mask, mask_bits and dropout per call is supported")
+    if mask_bits is not None:
+        bp, sb, sh, srow = _bits_args(mask_bits, q)
+        _check(_load().fa_bwd_bitmask(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(D), _p(dq), _p(dk), _p(dv),
+                                      bp, sb, sh, srow, _p(workspace), wbytes, B, H, N, d, scale, int(bool(causal)),
+                                      _dtype_code(q), _stream_ptr(stream)), "fa_bwd_bitmask")
+        return dq, dk, dv
     if dropout is not None:
         pd, seed = float(dropout[0]), int(dropout[1]) & 0xFFFFFFFFFFFFFFFF
         _check(_load().fa_bwd_dropout(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(D), _p(dq), _p(dk), _p(dv),

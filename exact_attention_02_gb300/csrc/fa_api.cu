@@ -123,6 +123,17 @@ fa_status_t check_mask(const Mask& m, const Shape& s, int dtype) {
   return FA_OK;
 }
 
+// Packed visibility bits: each 128-key tile of a row is read as one 16-byte piece, so the
+// base must be 16-byte aligned, every stride a non-negative multiple of 4 words, and each
+// row must hold 4 words per 128-key tile of the head.
+fa_status_t check_bits(const Mask& m, const Shape& s, int dtype) {
+  if (!m.ptr || !aligned16(m.ptr)) return FA_ERR_INVALID_ARG;
+  if (m.sb < 0 || m.sh < 0 || m.sb % 4 || m.sh % 4 || m.srow % 4) return FA_ERR_INVALID_ARG;
+  if (m.srow < ((int64_t)s.N + 127) / 128 * 4) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
 struct Drop {
   uint64_t seed;
   uint32_t t;  // keep iff the 8-bit uniform >= t
@@ -140,7 +151,7 @@ fa_status_t drop_threshold(float p, int dtype, uint32_t* t) {
 fa_status_t bwd_common(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                        const float* LSE, const float* D, void* dQ, void* dK, void* dV, void* workspace,
                        size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal, int dtype,
-                       const Mask* mask, const Drop* drop, void* stream) {
+                       const Mask* mask, const Drop* drop, void* stream, const Mask* bits = nullptr) {
   const Shape s{B, H, N, d};
   fa_status_t r = check_shape(s, dtype, &scale);
   if (r != FA_OK) return r;
@@ -148,6 +159,7 @@ fa_status_t bwd_common(const void* Q, const void* K, const void* V, const void* 
   if (D && !aligned16(D)) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (mask && (r = check_mask(*mask, s, dtype)) != FA_OK) return r;
+  if (bits && (r = check_bits(*bits, s, dtype)) != FA_OK) return r;
   const size_t need = fa_bwd_workspace_size(B, H, N, d, dtype);
   const size_t need_d = D ? 0 : (size_t)s.rows() * sizeof(float);
   if (need + need_d > 0) {
@@ -168,6 +180,10 @@ fa_status_t bwd_common(const void* Q, const void* K, const void* V, const void* 
     if (mask)
       return from_cuda(tc_bwd_masked(Q, K, V, dO, LSE, D, dQ, dK, dV, acc, s, scale, causal == 1, mask->ptr,
                                      mask->sb, mask->sh, mask->srow, status, st));
+    if (bits)
+      return from_cuda(tc_bwd_bitmask(Q, K, V, dO, LSE, D, dQ, dK, dV, acc, s, scale, causal == 1,
+                                      static_cast<const uint32_t*>(bits->ptr), bits->sb, bits->sh, bits->srow,
+                                      status, st));
     if (drop)
       return from_cuda(tc_bwd_dropout(Q, K, V, dO, LSE, D, dQ, dK, dV, acc, s, scale, causal == 1, drop->seed,
                                       drop->t, status, st));
@@ -214,6 +230,34 @@ extern "C" fa_status_t fa_bwd_masked(const void* Q, const void* K, const void* V
   const fa::Mask m{mask, mask_stride_b, mask_stride_h, mask_stride_row};
   return fa::bwd_common(Q, K, V, O, dO, LSE, D, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, scale, causal,
                         dtype, &m, nullptr, stream);
+}
+
+extern "C" fa_status_t fa_fwd_bitmask(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                      const void* bits, long long bits_stride_b, long long bits_stride_h,
+                                      long long bits_stride_row, int B, int H, int N, int d, float scale,
+                                      int causal, int dtype, void* stream) {
+  const Shape s{B, H, N, d};
+  fa_status_t r = fa::check_shape(s, dtype, &scale);
+  if (r != FA_OK) return r;
+  if ((r = fa::check_ptrs({Q, K, V, O, LSE})) != FA_OK) return r;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  const fa::Mask m{bits, bits_stride_b, bits_stride_h, bits_stride_row};
+  if ((r = fa::check_bits(m, s, dtype)) != FA_OK) return r;
+  int* status = fa::device_status_ptr();
+  if (!status) return FA_ERR_CUDA;
+  return fa::from_cuda(fa::tc_fwd_bitmask(Q, K, V, O, LSE, s, scale, causal == 1, static_cast<const uint32_t*>(bits),
+                                          m.sb, m.sh, m.srow, status, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" fa_status_t fa_bwd_bitmask(const void* Q, const void* K, const void* V, const void* O,
+                                      const void* dO, const float* LSE, const float* D, void* dQ, void* dK,
+                                      void* dV, const void* bits, long long bits_stride_b,
+                                      long long bits_stride_h, long long bits_stride_row, void* workspace,
+                                      size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                                      int dtype, void* stream) {
+  const fa::Mask m{bits, bits_stride_b, bits_stride_h, bits_stride_row};
+  return fa::bwd_common(Q, K, V, O, dO, LSE, D, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, scale, causal,
+                        dtype, nullptr, nullptr, stream, &m);
 }
 
 extern "C" fa_status_t fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,

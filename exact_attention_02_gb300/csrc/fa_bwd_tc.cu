@@ -3,7 +3,7 @@
 //
 // Method ("flash-attention-backpropagation", 反向总览 / Softmax梯度 / QKV梯度): the
 // outer loop runs over key/value tiles (one 128-key tile per CTA), the inner loop over
-// 128-row query tiles; P is rebuilt from the forward's LSE, and one recompute of each
+// 64-row query tiles; P is rebuilt from the forward's LSE, and one recompute of each
 // (i, j) tile yields dV, dK and dQ together (the single-recompute loop the Ascend page
 // "FlashAttention 反向传播" recommends over one pass per gradient). All accumulators are
 // fp32 and are rounded to bf16 once, on write-back.
@@ -29,6 +29,10 @@
 //
 // CTA = 14 warps: 0-7 softmax (two warpgroups splitting the query columns), 8-11 dQ
 // reduction + dK/dV epilogue, 12 TMA producer, 13 MMA issuer.
+//
+// Masks and dropout (kVar): the additive mask adds M log2(e) to each exponent; the
+// boolean mask (packed bits, as the forward reads them) and dropout zero P for hidden or
+// dropped keys, so their dS is 0 as well; kept dropout weights are scaled by 256 / (256 - t).
 //
 // Any N: Q/K/V/dO are read through [heads, N, d] tensor maps (rows past the end of a head
 // arrive as zeros), queries past the end get LSE = +inf (P = 0), and dQ/dK/dV rows past
@@ -109,6 +113,9 @@ struct BwdParams {
   float sl2;  // scale * log2(e)
   // additive mask (kMask): element (b, h, i, j) at mask[b*mask_sb + h*mask_sh + i*mask_srow + j]
   const __nv_bfloat16* mask;
+  // boolean mask (kVar == 3): visibility bits, word (b, h, i, j / 32) at
+  // bits[b*mask_sb + h*mask_sh + i*mask_srow + j / 32] (the same strides, in 32-bit words)
+  const uint32_t* bits;
   int64_t mask_sb, mask_sh, mask_srow;
   int H;
   // dropout (kVar == 2): Philox key, keep threshold and the scale of a kept weight
@@ -149,7 +156,7 @@ __device__ __forceinline__ uint32_t packed_col(uint32_t base, int k) {
 
 // kTail: N is not a multiple of the tiles, so the partial-tile guards are compiled in; the
 // instance for whole tiles carries none of them.
-// kVar: 0 plain, 1 additive mask, 2 dropout.
+// kVar: 0 plain, 1 additive mask, 2 dropout, 3 boolean mask (packed bits).
 template <int D, bool kTail, int kVar>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -158,6 +165,7 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   using C = BwdCfg<D>;
   constexpr bool kMask = kVar == 1;
   constexpr bool kDrop = kVar == 2;
+  constexpr bool kBits = kVar == 3;
   constexpr int BQ = C::BQ;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -368,10 +376,24 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const float2 sl2 = make_float2(p.sl2, p.sl2);
     const float2 neg_log2e = make_float2(-kLog2e, -kLog2e);
     const float2 minus1 = make_float2(-1.f, -1.f);
+    // kBits: the warp's 32 keys are one word of each query's row. Lane L reads the word of
+    // query (tile start + this warpgroup's first column + L), one tile ahead, so that the
+    // load's latency hides behind the current tile.
+    static_assert(!kBits || kCols == 32, "one 32-query chunk per tile");
+    const int kword = (kt * BN + (warp & 3) * 32) >> 5;
+    const uint32_t* bcol =
+        kBits ? p.bits + (int64_t)(head / p.H) * p.mask_sb + (int64_t)(head % p.H) * p.mask_sh + kword : nullptr;
+    auto bits_word = [&](int it) -> uint32_t {
+      const int q = (q_first + it) * BQ + wg * kCols + lane;
+      return (it < nq && (!kTail || (q < p.N && kword * 32 < p.N))) ? bcol[(int64_t)q * p.mask_srow] : 0u;
+    };
+    uint32_t bword = kBits ? bits_word(0) : 0u;
     bool ok = true;
     for (int it = 0; ok && it < nq; ++it) {
       const int s = it % C::kStages;
       const int b = it % C::NB;
+      const uint32_t bcur = bword;
+      if constexpr (kBits) bword = bits_word(it + 1);
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full[b], (it / C::NB) & 1, p.status, abort));
       if (!ok) break;
       tc_fence_after();
@@ -409,6 +431,9 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                                (rng::keep16(blk0 + 1, i, (uint32_t)head, p.seed_lo, p.seed_hi, p.drop_tt) << 16);
           kbits = transpose32(row, lane);
         }
+        // kBits: transposing the 32 lanes' words (prefetched above) leaves lane T with
+        // bit c = visible(query c of the chunk, key T).
+        const uint32_t vbits = kBits ? transpose32(bcur, lane) : 0u;
         float sv[32], dp[32];
         tmem_ld32x2(tmem + lane_off + C::colS(b) + c0, tmem + lane_off + C::colDP(b) + c0, sv, dp);
         // -LSE*log2(e) and D for the 32 columns, loaded as 16-byte vectors up front
@@ -419,7 +444,7 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           const float4 b = *reinterpret_cast<const float4*>(vec + BQ + c0 + 4 * u);
           nl[2 * u] = fmul2(make_float2(a.x, a.y), neg_log2e);
           nl[2 * u + 1] = fmul2(make_float2(a.z, a.w), neg_log2e);
-          if constexpr (kMask) {  // a query with no visible key (LSE = -inf) has P = 0
+          if constexpr (kMask || kBits) {  // a query with no visible key (LSE = -inf) has P = 0
             if (a.x == -INFINITY) nl[2 * u].x = -INFINITY;
             if (a.y == -INFINITY) nl[2 * u].y = -INFINITY;
             if (a.z == -INFINITY) nl[2 * u + 1].x = -INFINITY;
@@ -435,6 +460,10 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, nl[u]);
           if constexpr (kMask) x = fadd2(x, make_float2(mk[2 * u], mk[2 * u + 1]));
           float2 pr = make_float2(ex2(x.x), ex2(x.y));
+          if constexpr (kBits) {  // a hidden key has P = 0, and so dS = 0
+            if (!((vbits >> (2 * u)) & 1u)) pr.x = 0.f;
+            if (!((vbits >> (2 * u + 1)) & 1u)) pr.y = 0.f;
+          }
           if (diag) {
             if (key > q0 + c) pr.x = 0.f;
             if (key > q0 + c + 1) pr.y = 0.f;
@@ -615,6 +644,7 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
   p.scale = scale;
   p.sl2 = scale * kLog2e;
   p.mask = static_cast<const __nv_bfloat16*>(mask.ptr);
+  p.bits = static_cast<const uint32_t*>(mask.ptr);
   p.mask_sb = mask.sb;
   p.mask_sh = mask.sh;
   p.mask_srow = mask.srow;
@@ -660,6 +690,21 @@ cudaError_t tc_bwd_masked(const void* Q, const void* K, const void* V, const voi
   return s.d == 64
              ? launch<64, 1>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, m, nodrop, status, st)
              : launch<128, 1>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, m, nodrop, status, st);
+}
+
+cudaError_t tc_bwd_bitmask(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                           const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
+                           float scale, bool causal, const uint32_t* bits, int64_t bits_sb, int64_t bits_sh,
+                           int64_t bits_srow, int* status, cudaStream_t st) {
+  MaskArg m;
+  m.ptr = bits;
+  m.sb = bits_sb;
+  m.sh = bits_sh;
+  m.srow = bits_srow;
+  const DropArg nodrop;
+  return s.d == 64
+             ? launch<64, 3>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, m, nodrop, status, st)
+             : launch<128, 3>(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, m, nodrop, status, st);
 }
 
 cudaError_t tc_bwd_dropout(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,

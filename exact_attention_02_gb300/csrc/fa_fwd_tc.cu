@@ -39,6 +39,12 @@
 // Rows with no visible key so far keep m = -inf and exponentiate against 0; a row with
 // no visible key at all stores O = 0 and LSE = -inf.
 //
+// Boolean mask instance (kVar == 3): the same mask restricted to 0 (visible) and -inf
+// (hidden), packed one bit per key: bit j % 32 of word j / 32 of a query's row. A softmax
+// thread prefetches its row's 128 bits for the next K tile (one 16-byte load, against 256
+// bytes of bf16 mask) and sets the scores of hidden keys to -inf before the row max, as
+// the causal diagonal does; rows without a visible key behave as with the additive mask.
+//
 // Dropout instance (kVar == 2): the same section of "知识点13" fuses dropout into the
 // softmax step. Each softmax thread draws the keep bits of its row for the next K tile
 // (8 Philox calls of 16 keys, see philox.cuh) while the tile's S is being computed, stores
@@ -108,6 +114,9 @@ struct FwdParams {
   float o_scale;  // V's factor for e4m3, else 1
   // additive mask (kMask): element (b, h, i, j) at mask[b*mask_sb + h*mask_sh + i*mask_srow + j]
   const __nv_bfloat16* mask;
+  // boolean mask (kVar == 3): visibility bits, word (b, h, i, j / 32) at
+  // bits[b*mask_sb + h*mask_sh + i*mask_srow + j / 32] (the same strides, in 32-bit words)
+  const uint32_t* bits;
   int64_t mask_sb, mask_sh, mask_srow;
   int H;
   float inv_scale;  // 1 / scale: M joins the raw scores as M / scale
@@ -125,7 +134,7 @@ struct FwdCtl {
   int abort;
 };
 
-// kVar: 0 plain, 1 additive mask, 2 dropout.
+// kVar: 0 plain, 1 additive mask, 2 dropout, 3 boolean mask (packed bits).
 template <int D, bool F8, int kVar>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -133,6 +142,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   using C = FwdCfg<D, F8>;
   constexpr bool kMask = kVar == 1;
   constexpr bool kDrop = kVar == 2;
+  constexpr bool kBits = kVar == 3;
+  constexpr bool kHides = kMask || kBits;  // a row may have no visible key
   static_assert(!(F8 && kVar), "the e4m3 instance has no mask or dropout");
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdCtl ctl;
@@ -316,6 +327,16 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       for (int c8 = 0; c8 < BN / 8; ++c8)
         mreg[c8] = (mrow && 8 * c8 < p.N && nk > 0) ? ld_global_v4_ordered(mrow + 8 * c8) : make_uint4(0, 0, 0, 0);
     }
+    // kBits: this row's visibility bits for the K tile about to be processed (words
+    // 4j .. 4j+3 of the row; rows hold at least 4 words per K tile of the head).
+    uint4 breg = make_uint4(0, 0, 0, 0);
+    const uint32_t* brow = nullptr;
+    if constexpr (kBits) {
+      if (qrow < p.N)
+        brow = p.bits + (int64_t)(head / p.H) * p.mask_sb + (int64_t)(head % p.H) * p.mask_sh +
+               (int64_t)qrow * p.mask_srow;
+      if (brow && nk > 0) breg = ld_global_v4_ordered(brow);
+    }
     // tcgen05.ld/st are warp-collective (.sync.aligned): every branch that guards one
     // is made uniform across the warp, including the outcome of each bounded wait.
     for (int j = 0; ok && j < nk; ++j) {
@@ -358,9 +379,17 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           }
         }
       }
+      // kBits: keys whose bit is clear are hidden. (Skipping this for tiles whose bits are
+      // all set measured 17% slower: the branch costs registers the loop needs.)
+      if constexpr (kBits) {
+        const uint32_t bw[4] = {breg.x, breg.y, breg.z, breg.w};
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (!((bw[c / 32] >> (c % 32)) & 1u)) sv[c] = -INFINITY;
+      }
       // Hidden keys: key > query on the diagonal tile (causal), and keys past the end of
-      // the head in its last, partial tile (their rows were read as zeros). Every row keeps
-      // at least key 0 of the tile visible.
+      // the head in its last, partial tile (their rows were read as zeros). Without a mask
+      // every row keeps at least key 0 of the tile visible.
       const bool diag = p.causal && j == qt0 + t;
       const int valid = p.N - j * BN;
       if (diag || valid < BN) {
@@ -406,7 +435,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const float2 sl2v = make_float2(sl2, sl2);
       // a row with no visible key so far (only possible with a mask) exponentiates
       // against 0: its scores are all -inf, so every p is 0
-      const float m_use = (kMask && m == -INFINITY) ? 0.f : m;
+      const float m_use = (kHides && m == -INFINITY) ? 0.f : m;
       const float2 neg_m = make_float2(C::kPShift - m_use, C::kPShift - m_use);
       float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
       if constexpr (!F8) {
@@ -449,6 +478,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
       l += (rs0.x + rs0.y) + (rs1.x + rs1.y);
+      if constexpr (kBits)  // the next tile's bits land while its S is computed
+        breg = (brow && j + 1 < nk) ? ld_global_v4_ordered(brow + 4 * (j + 1)) : make_uint4(0, 0, 0, 0);
       if constexpr (kMask) {  // the next tile's mask lands while its S is computed
 #pragma unroll
         for (int c8 = 0; c8 < BN / 8; ++c8) {
@@ -463,7 +494,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.o_full[t], 0, p.status, abort));
     if (ok) {
       tc_fence_after();
-      const float inv_l = (!kMask || l > 0.f) ? (kDrop ? p.drop_scale : p.o_scale) / l : 0.f;  // no visible key: O = 0
+      const float inv_l = (!kHides || l > 0.f) ? (kDrop ? p.drop_scale : p.o_scale) / l : 0.f;  // no visible key: O = 0
       __nv_bfloat16* orow = p.O + (size_t)(row_base + qrow) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -536,6 +567,7 @@ cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.sl2 = sl2;
   p.o_scale = o_scale;
   p.mask = static_cast<const __nv_bfloat16*>(mask.ptr);
+  p.bits = static_cast<const uint32_t*>(mask.ptr);
   p.mask_sb = mask.sb;
   p.mask_sh = mask.sh;
   p.mask_srow = mask.srow;
@@ -575,6 +607,20 @@ cudaError_t tc_fwd_masked(const void* Q, const void* K, const void* V, void* O, 
   return s.d == 64
              ? launch<64, false, 1>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, m, nodrop, status, st)
              : launch<128, false, 1>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, m, nodrop, status, st);
+}
+
+cudaError_t tc_fwd_bitmask(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                           float scale, bool causal, const uint32_t* bits, int64_t bits_sb, int64_t bits_sh,
+                           int64_t bits_srow, int* status, cudaStream_t st) {
+  MaskArg m;
+  m.ptr = bits;
+  m.sb = bits_sb;
+  m.sh = bits_sh;
+  m.srow = bits_srow;
+  const DropArg nodrop;
+  return s.d == 64
+             ? launch<64, false, 3>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, m, nodrop, status, st)
+             : launch<128, false, 3>(Q, K, V, O, LSE, s, scale, scale * kLog2e, 1.f, causal, m, nodrop, status, st);
 }
 
 cudaError_t tc_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,

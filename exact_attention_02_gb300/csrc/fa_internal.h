@@ -36,6 +36,12 @@ cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* 
 cudaError_t tc_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
                           float scale, bool causal, const void* mask, int64_t mask_sb, int64_t mask_sh,
                           int64_t mask_srow, int* status, cudaStream_t st);
+// bf16 forward with a boolean mask packed one bit per key: query i sees key j iff bit j % 32
+// of word bits[b*bits_sb + h*bits_sh + i*bits_srow + j / 32] is set (strides in 32-bit words,
+// multiples of 4; rows hold at least 4 words per 128-key tile).
+cudaError_t tc_fwd_bitmask(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                           float scale, bool causal, const uint32_t* bits, int64_t bits_sb, int64_t bits_sh,
+                           int64_t bits_srow, int* status, cudaStream_t st);
 // bf16 forward with dropout: Philox-4x32-10 keep bits keyed by `seed`, kept iff the 8-bit
 // uniform is >= threshold; kept weights scaled by 256 / (256 - threshold).
 cudaError_t tc_fwd_dropout(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
@@ -55,6 +61,12 @@ cudaError_t tc_bwd_masked(const void* Q, const void* K, const void* V, const voi
                           const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
                           float scale, bool causal, const void* mask, int64_t mask_sb, int64_t mask_sh,
                           int64_t mask_srow, int* status, cudaStream_t st);
+
+// The backward with the boolean mask of tc_fwd_bitmask.
+cudaError_t tc_bwd_bitmask(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                           const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
+                           float scale, bool causal, const uint32_t* bits, int64_t bits_sb, int64_t bits_sh,
+                           int64_t bits_srow, int* status, cudaStream_t st);
 
 // The backward with the dropout of tc_fwd_dropout (same seed and threshold).
 cudaError_t tc_bwd_dropout(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,

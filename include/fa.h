@@ -178,6 +178,33 @@ FA_API fa_status_t fa_bwd_masked(const void* Q, const void* K, const void* V, co
                                  int causal, int dtype, void* stream);
 
 /*
+ * fa_fwd_bitmask / fa_bwd_bitmask — fa_fwd_masked / fa_bwd_masked for a boolean mask, whose
+ * entries are 0 (the key is visible) or -inf (hidden), stored one bit per key: the same
+ * result as the additive mask with those entries, at 1/16 of its bytes.
+ * bits: 32-bit words (dtype must be FA_DTYPE_BF16, else FA_ERR_UNSUPPORTED), device
+ *      pointer, 16-byte aligned. Query i of head (b, h) sees key j iff bit (j % 32) of word
+ *      bits[b * bits_stride_b + h * bits_stride_h + i * bits_stride_row + j / 32]
+ *      is 1 (and, when causal, j <= i). Strides are in words, 0 broadcasts over batch or
+ *      heads; every stride must be a non-negative multiple of 4, and bits_stride_row at
+ *      least 4 * ceil(N / 128): each 128-key tile of a row is read as one 16-byte piece.
+ *      Bits of keys j >= N are never used. The caller owns the words; both calls read
+ *      them and never write them; pass the same words, scale and causal flag to both.
+ * A query with no visible key gets O = 0 and LSE = -inf, as with fa_fwd_masked.
+ * The remaining arguments, layouts, workspace and errors are those of fa_fwd_masked and
+ *      fa_bwd_masked.
+ */
+FA_API fa_status_t fa_fwd_bitmask(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                  const void* bits, long long bits_stride_b, long long bits_stride_h,
+                                  long long bits_stride_row, int B, int H, int N, int d, float scale,
+                                  int causal, int dtype, void* stream);
+FA_API fa_status_t fa_bwd_bitmask(const void* Q, const void* K, const void* V, const void* O,
+                                  const void* dO, const float* LSE, const float* D, void* dQ, void* dK,
+                                  void* dV, const void* bits, long long bits_stride_b,
+                                  long long bits_stride_h, long long bits_stride_row, void* workspace,
+                                  size_t workspace_bytes, int B, int H, int N, int d, float scale,
+                                  int causal, int dtype, void* stream);
+
+/*
  * fa_fwd_dropout / fa_bwd_dropout — fa_fwd / fa_bwd with dropout on the attention weights
  * ("知识点13 FlashAttention深度攻略" §7 算子融合优化: dropout is fused into the softmax step):
  *      O = (P o K c) V,  P = softmax of the scores, K the 0/1 keep matrix, c its scale.

@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
     assert set(_declared()) >= {"fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_bwd_workspace_size",
                                 "fa_get_error_string", "fa_get_last_device_status", "fa_fwd_splitkv",
                                 "fa_fwd_splitkv_workspace_size", "fa_fwd_fp8", "fa_fwd_masked", "fa_bwd_masked",
-                                "fa_fwd_dropout", "fa_bwd_dropout"}
+                                "fa_fwd_dropout", "fa_bwd_dropout", "fa_fwd_bitmask", "fa_bwd_bitmask"}
 
 
 def test_exports_every_declared_symbol(lib):
@@ -179,6 +179,41 @@ def test_masked_rejects_before_launch(lib):
     assert call(sh=4) == fa.FA_ERR_INVALID_ARG
     assert call(dtype=1) == fa.FA_ERR_UNSUPPORTED           # the fp32 path has no mask
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_bitmask_rejects_before_launch(lib):
+    """Host-side checks of the packed mask arguments (dummy pointers; nothing is launched)."""
+    import exact_attention_02_gb300 as fa
+    vp, f, ll = ctypes.c_void_p, ctypes.c_float, ctypes.c_longlong
+    L = fa.lib()
+
+    def call(bits=P, sb=0, sh=0, srow=4, N=128, dtype=0, d=64):
+        return L.fa_fwd_bitmask(vp(P), vp(P), vp(P), vp(P), vp(P), vp(bits), ll(sb), ll(sh), ll(srow), 1, 1, N, d,
+                                f(0.125), 0, dtype, None)
+    assert call(bits=0) == fa.FA_ERR_INVALID_ARG            # no words
+    assert call(bits=P + 4) == fa.FA_ERR_INVALID_ARG        # misaligned
+    assert call(N=129, srow=4) == fa.FA_ERR_INVALID_ARG     # 2 key tiles need 8 words per row
+    assert call(srow=6) == fa.FA_ERR_INVALID_ARG            # not a multiple of 4 words
+    assert call(sb=-4) == fa.FA_ERR_INVALID_ARG
+    assert call(sh=2) == fa.FA_ERR_INVALID_ARG
+    assert call(dtype=1) == fa.FA_ERR_UNSUPPORTED           # the fp32 path has no mask
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_pack_mask_bits_layout():
+    """pack_mask_bits puts key j of a row at bit j % 32 of word j / 32, rows padded to 4
+    words per 128 keys, written out here bit by bit with numpy."""
+    import numpy as np
+    torch = pytest.importorskip("torch")
+    import exact_attention_02_gb300 as fa
+    rng = np.random.default_rng(5)
+    vis = rng.random((2, 3, 200, 200)) < 0.4
+    got = fa.pack_mask_bits(torch.from_numpy(vis)).numpy().astype(np.int64) & 0xFFFFFFFF
+    assert got.shape == (2, 3, 200, 8)
+    want = np.zeros((2, 3, 200, 8), np.int64)
+    for j in range(200):
+        want[..., j // 32] |= vis[..., j].astype(np.int64) << (j % 32)
+    assert np.array_equal(got, want)
 
 
 def test_dropout_rejects_before_launch(lib):
