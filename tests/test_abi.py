@@ -216,6 +216,29 @@ def test_pack_mask_bits_layout():
     assert np.array_equal(got, want)
 
 
+def test_binding_checks_mask_bits_before_calling(lib):
+    """The binding refuses packed bits of the wrong dtype, shape or row length before it
+    calls into the library (CPU tensors: nothing reaches a device)."""
+    torch = pytest.importorskip("torch")
+    import exact_attention_02_gb300 as fa
+    q = torch.zeros(2, 3, 200, 64, dtype=torch.bfloat16)
+    good = fa.pack_mask_bits(torch.ones(1, 1, 200, 200, dtype=torch.bool))
+    bad = [good.to(torch.int64),                              # not int32
+           good[..., :4].contiguous(),                       # 4 words cannot hold 200 keys' tiles
+           torch.zeros(1, 2, 200, 8, dtype=torch.int32),     # 2 heads for H = 3
+           torch.zeros(1, 1, 199, 8, dtype=torch.int32),     # rows for the wrong N
+           torch.zeros(1, 1, 200, 10, dtype=torch.int32)[..., :8],  # row stride not a multiple of 4
+           good[0]]                                          # not 4-D
+    for bits in bad:
+        with pytest.raises(ValueError):
+            fa.fa_fwd(q, q, q, False, mask_bits=bits)
+        with pytest.raises(ValueError):
+            fa.fa_bwd(q, q, q, q, q, torch.zeros(2, 3, 200), False, mask_bits=bits,
+                      workspace=torch.zeros(16, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q, False, mask_bits=good, dropout=(0.1, 1))
+
+
 def test_dropout_rejects_before_launch(lib):
     """Host-side checks of the dropout rate (dummy pointers; nothing is launched)."""
     import exact_attention_02_gb300 as fa
