@@ -6,11 +6,13 @@
 //   copy-in  : Q, K, V, dO of the group, host -> device slot
 //   compute  : fa_fwd, fa_bwd_preprocess, fa_bwd on the slot (the group as B = 1, H = heads)
 //   copy-out : O, LSE, dQ, dK, dV of the group, device slot -> host
-// Two device slots alternate, so group g's copy-in overlaps group g-1's kernels and group
-// g-2's copy-out. Events order the stages at the granularity the kernels need: the forward
-// starts once Q, K and V have landed (dO is still on its way), and O and LSE go back to
-// the host while the backward runs; a slot is refilled only after its previous group's
-// copy-out has read it. The call forks from the caller's stream (the internal
+// Three device slots rotate, so group g's copy-in overlaps group g-1's kernels and the
+// copy-outs of groups g-1 and g-2; with two slots, the copy-in of a group had to wait for
+// the copy-out of the group two before it, which left the kernels idle between groups.
+// Events order the stages at the granularity the kernels need: the forward starts once
+// Q, K and V have landed (dO is still on its way), and O and LSE go back to the host while
+// the backward runs; a slot is refilled only after its previous group's copy-out has
+// read it. The call forks from the caller's stream (the internal
 // streams wait on an event recorded there) and joins back into it (the caller's stream
 // waits on the last copy-out), so it enqueues work and returns without synchronising.
 //
@@ -25,6 +27,7 @@ namespace fa {
 namespace {
 
 constexpr int kMaxChunks = 16;
+constexpr int kSlots = 3;
 constexpr int kEventsPerChunk = 5;
 constexpr int kRing = kMaxChunks * kEventsPerChunk + 2;
 
@@ -120,7 +123,7 @@ Groups make_groups(int64_t heads, int chunks) {
 extern "C" size_t fa_fwd_bwd_host_workspace_size(int B, int H, int N, int d, int dtype, int chunks) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || dtype != FA_DTYPE_BF16) return 0;
   const fa::Groups g = fa::make_groups((int64_t)B * H, chunks);
-  return 2 * fa::slot_layout(g.largest, N, d).bytes;
+  return fa::kSlots * fa::slot_layout(g.largest, N, d).bytes;
 }
 
 extern "C" fa_status_t fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const void* dO, void* O,
@@ -166,11 +169,11 @@ extern "C" fa_status_t fa_fwd_bwd_host(const void* Q, const void* K, const void*
   cudaEvent_t out_done[fa::kMaxChunks] = {};
   for (int g = 0; g < ng; ++g) {
     const int64_t h0 = G.start[g], nh = G.start[g + 1] - h0;
-    char* slot = static_cast<char*>(workspace) + (size_t)(g & 1) * L.bytes;
+    char* slot = static_cast<char*>(workspace) + (size_t)(g % fa::kSlots) * L.bytes;
     const size_t el = (size_t)nh * head_el, rows = (size_t)nh * head_rows;
     const size_t off = (size_t)h0 * head_el, roff = (size_t)h0 * head_rows;
     // copy-in, once the slot's previous group has been copied out
-    if (g >= 2) FA_TRY(cudaStreamWaitEvent(qs->in, out_done[g - 2], 0));
+    if (g >= fa::kSlots) FA_TRY(cudaStreamWaitEvent(qs->in, out_done[g - fa::kSlots], 0));
     FA_TRY(cudaMemcpyAsync(slot + L.q, static_cast<const char*>(Q) + off, el, cudaMemcpyHostToDevice, qs->in));
     FA_TRY(cudaMemcpyAsync(slot + L.k, static_cast<const char*>(K) + off, el, cudaMemcpyHostToDevice, qs->in));
     FA_TRY(cudaMemcpyAsync(slot + L.v, static_cast<const char*>(V) + off, el, cudaMemcpyHostToDevice, qs->in));

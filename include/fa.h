@@ -256,8 +256,8 @@ FA_API fa_status_t fa_fwd_fp8(const void* Q, const void* K, const void* V, void*
  * group's copy-in and the last one's copy-out overlap no kernel, so they are the small
  * ones) and up to 4 equal groups otherwise;
  * each group is copied in (Q, K, V, dO), run through fa_fwd, fa_bwd_preprocess and fa_bwd,
- * and copied out (O, LSE, dQ, dK, dV) on three internal streams, with two device slots
- * in `workspace` alternating, so one group's copies run while another's kernels do.
+ * and copied out (O, LSE, dQ, dK, dV) on three internal streams, with three device slots
+ * in `workspace` in rotation, so one group's copies run while another's kernels do.
  * In:  Q, K, V, dO host [B,H,N,d] bf16 (page-locked memory, e.g. cudaHostAlloc, lets
  *      the copies run asynchronously; pageable memory works but serialises them).
  * Out: O host [B,H,N,d] bf16, LSE host [B,H,N] fp32, dQ, dK, dV host [B,H,N,d] bf16.
