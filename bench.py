@@ -332,7 +332,8 @@ def run_ours(args, w):
 
         if w.dtype == "bf16":
             # the library's host-tensor entry point: copies of one head group overlap the
-            # kernels of another (fa_fwd_bwd_host, default 4 groups)
+            # kernels of another (fa_fwd_bwd_host, default schedule: five head groups in
+            # the ratio 1:2:2:2:1)
             e2e_path = "fa_fwd_bwd_host (C ABI on pinned host tensors; copies overlapped with kernels)"
             hws = torch.empty(fa.fa_fwd_bwd_host_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8,
                               device=dev)
