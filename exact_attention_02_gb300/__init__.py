@@ -175,10 +175,13 @@ def pack_mask_bits(visible):
     n = int(visible.shape[-1])
     words = (n + 127) // 128 * 4
     lead = tuple(visible.shape[:-1])
-    v = torch.zeros(lead + (words * 32,), dtype=torch.int64, device=visible.device)
-    v[..., :n] = visible.to(torch.int64)
-    w = (v.view(lead + (words, 32)) << torch.arange(32, dtype=torch.int64, device=visible.device)).sum(-1)
-    return torch.where(w >= 2 ** 31, w - 2 ** 32, w).to(torch.int32)
+    v = torch.zeros(lead + (words * 32,), dtype=torch.uint8, device=visible.device)
+    v[..., :n] = visible.to(torch.uint8)
+    # one byte per 8 keys (bit k = key 8i + k); read as little-endian words, byte i of a
+    # word holds keys 8i .. 8i+7 of its 32, so bit j % 32 of word j / 32 is key j
+    shifts = torch.arange(8, dtype=torch.uint8, device=visible.device)
+    b = (v.view(lead + (words * 4, 8)) << shifts).sum(-1, dtype=torch.uint8)
+    return b.view(torch.int32)
 
 
 def _bits_args(bits, q):
