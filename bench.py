@@ -106,7 +106,7 @@ def oracle_head_step(w, x, b, h):
     from oracle import attention as ora
     import numpy as np
     args = [x[n][b, h].astype(np.float64) for n in ("q", "k", "v", "do")]
-    ora.head_backward(*args, w.scale, w.causal)
+    return ora.head_backward(*args, w.scale, w.causal)
 
 
 def cpu_model():
@@ -127,13 +127,17 @@ def cpu_model():
     return platform.machine() or "unknown"
 
 
-def cpu_baseline(w, x, budget_s=12.0, max_heads=8):
-    """The oracle, as it stands, on whole heads of the workload until ~budget_s."""
+def cpu_baseline(w, x, budget_s=12.0, max_heads=8, keep=None):
+    """The oracle, as it stands, on whole heads of the workload until ~budget_s. With
+    ``keep`` (a list), each head's oracle outputs are appended to it as ((b, h), outputs)."""
     flop_head = (w.fwd_flop() + w.bwd_flop()) / (w.B * w.H)
     t0 = time.perf_counter()
     n = 0
     while n < max_heads and (time.perf_counter() - t0) < budget_s:
-        oracle_head_step(w, x, n // w.H % w.B, n % w.H)
+        b, h = n // w.H % w.B, n % w.H
+        r = oracle_head_step(w, x, b, h)
+        if keep is not None:
+            keep.append(((b, h), r))
         n += 1
     dt = time.perf_counter() - t0
     return {"value": flop_head * n / dt / 1e12, "unit": "TFLOP/s",
@@ -141,6 +145,28 @@ def cpu_baseline(w, x, budget_s=12.0, max_heads=8):
             "kind": "oracle",
             "sample": f"{n} whole head(s) of the workload (fwd+bwd, fp64 numpy), {dt:.1f} s; "
                       f"FLOPs counted by the same convention as the GPU line"}
+
+
+def oracle_parity(w, ref_heads, got):
+    """Errors of the timed run's outputs against the oracle, on the heads the CPU baseline
+    computed, in the metrics and bounds of the parity tests: bf16 O and LSE max-abs (2e-2,
+    1e-3) and dQ, dK, dV relative Frobenius (2e-2); fp32 max-abs 1e-4 on all five."""
+    import numpy as np
+    bf16 = w.dtype == "bf16"
+    err = {"o": 0.0, "lse": 0.0, "dq": 0.0, "dk": 0.0, "dv": 0.0}
+    for (b, h), r in ref_heads:
+        for n in err:
+            g = got[n][b, h].float().cpu().numpy().astype(np.float64)
+            if bf16 and n in ("dq", "dk", "dv"):
+                e = float(np.linalg.norm(g - r[n]) / max(float(np.linalg.norm(r[n])), 1e-300))
+            else:
+                e = float(np.abs(g - r[n]).max())
+            err[n] = max(err[n], e)
+    bound = ({"o": 2e-2, "lse": 1e-3, "dq": 2e-2, "dk": 2e-2, "dv": 2e-2} if bf16
+             else dict.fromkeys(err, 1e-4))
+    kind = {n: ("rel_fro" if bf16 and n in ("dq", "dk", "dv") else "max_abs") for n in err}
+    return {"heads": [list(bh) for bh, _ in ref_heads], "error": err, "metric": kind, "bound": bound,
+            "pass": bool(ref_heads) and all(err[n] <= bound[n] for n in err)}
 
 
 def run_reference(args, w):
@@ -418,7 +444,12 @@ def run_ours(args, w):
     line["bwd"]["frac_tensor_peak"] = line["bwd"]["tflops"] / tpeak if w.dtype == "bf16" else None
     line["frac_tensor_peak"] = value / world / tpeak if w.dtype == "bf16" else None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, x)
+        ref_heads = []
+        line["cpu_baseline"] = cpu_baseline(w, x, keep=ref_heads)
+        try:  # the oracle's heads double as a full-size parity check of the timed outputs
+            line["oracle_parity"] = oracle_parity(w, ref_heads, dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv))
+        except Exception as e:  # a failed check is reported, never fatal to the bench line
+            line["oracle_parity"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
