@@ -451,6 +451,30 @@ def pin_mask_torch_sdpa(m):
     assert np.allclose(m.forward(*arrs[:3], 0.3, False, mask=M1)[0], o1.numpy(), rtol=0, atol=1e-12)
 
 
+def pin_boolean_mask_is_key_removal(m):
+    """A mask of 0 (visible) and -inf (hidden) entries, the boolean mask the packed-bit
+    kernels take: each query's output and LSE equal attention over its visible keys alone,
+    and a key's dK and dV collect only the queries that see it."""
+    N, d, scale = 8, 3, 0.7
+    q, k, v, do = (_rand((N, d), 780 + s) for s in range(4))
+    vis = np.random.default_rng(784).random((N, N)) < 0.6
+    vis[np.arange(N), (np.arange(N) * 3) % N] = True  # every query sees at least one key
+    M = np.where(vis, 0.0, -np.inf)
+    r = m.head_backward(q, k, v, do, scale, False, mask=M)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for i in range(N):
+        keys = np.flatnonzero(vis[i])
+        ri = m.head_backward(q[i:i + 1], k[keys], v[keys], do[i:i + 1], scale, False)
+        assert np.allclose(r["o"][i], ri["o"][0], rtol=0, atol=1e-13), i
+        assert abs(r["lse"][i] - ri["lse"][0]) < 1e-13, i
+        assert np.allclose(r["dq"][i], ri["dq"][0], rtol=0, atol=1e-13), i
+        dk[keys] += ri["dk"]
+        dv[keys] += ri["dv"]
+    assert np.allclose(r["dk"], dk, rtol=0, atol=1e-13)
+    assert np.allclose(r["dv"], dv, rtol=0, atol=1e-13)
+
+
 def pin_mask_hidden_row(m):
     """A row with every key hidden: O = 0, LSE = -inf, no gradient through it, and the
     other rows as without that row's queries."""
