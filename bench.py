@@ -350,6 +350,7 @@ def run_ours(args, w):
 
     # end to end: pinned host inputs in, results (O, LSE, dQ, dK, dV) back to pinned host memory
     e2e = None
+    e2e_out = None
     if not args.no_e2e:
         out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                     for n, t in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items()}
@@ -392,6 +393,7 @@ def run_ours(args, w):
         e2e_ms = max_over_ranks([e2e_ms], device=dev)[0]
         e2e = {"value": world * flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "path": e2e_path}
+        e2e_out = out_host
 
     esz = 2 if w.dtype == "bf16" else 4
     rows = w.B * w.H * w.N
@@ -401,8 +403,11 @@ def run_ours(args, w):
     bound = fa.BF16_KERNEL_BOUND[dominant] if w.dtype == "bf16" else ("hbm" if dominant == "fa_bwd_preprocess" else "alu")
     dom_flop = {"fa_fwd": w.fwd_flop(), "fa_bwd": w.bwd_flop()}.get(dominant)
     if bound == "tensor":
-        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-        peak_desc = f"bf16 dense, sustained ({peak_src})"
+        # The burst figure: the kernel runs in a timed region of well under a second at the
+        # maximum SM clock, while the sustained figure was taken over seconds under the
+        # power cap at a lower clock. The sustained fraction is reported beside it.
+        peak = peaks["bf16_tflops"]
+        peak_desc = f"bf16 dense, burst ({peak_src})"
         unit = "TFLOP/s"
         achieved = dom_flop / (kern[dominant] * 1e-3) / 1e12
     elif bound == "alu":
@@ -419,6 +424,10 @@ def run_ours(args, w):
                 "frac": achieved / peak, "peak_source": peak_desc, "traffic": traffic,
                 "traffic_note": "DRAM bytes per launch from profiles/traffic.json (ncu, scaled by heads)"
                 if traffic else "no capture recorded for this kernel build and workload"}
+    if bound == "tensor":
+        sus = peaks.get("bf16_tflops_sustained")
+        roofline["frac_burst"] = achieved / peaks["bf16_tflops"]
+        roofline["frac_sustained"] = achieved / sus if sus else None
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -439,10 +448,15 @@ def run_ours(args, w):
         "clocks": dict(clk, window=f"{args.soak_s:.1f} s of untimed steps, then the timed region"),
         "e2e": e2e,
     }
-    tpeak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    line["fwd"]["frac_tensor_peak"] = line["fwd"]["tflops"] / tpeak if w.dtype == "bf16" else None
-    line["bwd"]["frac_tensor_peak"] = line["bwd"]["tflops"] / tpeak if w.dtype == "bf16" else None
+    # fractions of the dense bf16 tensor peak: burst (the headline) and sustained
+    tpeak, spk = peaks["bf16_tflops"], peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    for key, tf in (("fwd", line["fwd"]["tflops"]), ("bwd", line["bwd"]["tflops"])):
+        line[key]["frac_tensor_peak"] = tf / tpeak if w.dtype == "bf16" else None
+        line[key]["frac_tensor_peak_sustained"] = tf / spk if w.dtype == "bf16" else None
     line["frac_tensor_peak"] = value / world / tpeak if w.dtype == "bf16" else None
+    line["frac_tensor_peak_sustained"] = value / world / spk if w.dtype == "bf16" else None
+    line["tensor_peak"] = {"burst": tpeak, "sustained": spk, "source": peak_src,
+                           "headline": "burst: the timed region lasts well under a second"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ref_heads = []
         line["cpu_baseline"] = cpu_baseline(w, x, keep=ref_heads)
@@ -450,6 +464,11 @@ def run_ours(args, w):
             line["oracle_parity"] = oracle_parity(w, ref_heads, dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv))
         except Exception as e:  # a failed check is reported, never fatal to the bench line
             line["oracle_parity"] = {"error": f"{type(e).__name__}: {e}"}
+        if e2e_out is not None:  # and of what the end-to-end leg copied back to the host
+            try:
+                line["e2e"]["oracle_parity"] = oracle_parity(w, ref_heads, e2e_out)
+            except Exception as e:
+                line["e2e"]["oracle_parity"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -520,8 +539,8 @@ def run_fp8(args):
     """Forward on e4m3 inputs (fa_fwd_fp8) for a B,H,N,d,causal shape (d = 128).
 
     Tensor-bound like the bf16 forward and counted with the same FLOP convention; the
-    peak is the measured dense bf16 rate times 2, the nominal fp8/bf16 ratio of the part
-    (4.5 / 2.25 PFLOP/s), taken sustained because the forward runs in a long loop."""
+    peak is the measured dense bf16 burst rate times 2, the nominal fp8/bf16 ratio of the
+    part (4.5 / 2.25 PFLOP/s); the fraction of 2 x the sustained rate is reported beside it."""
     import torch
 
     import exact_attention_02_gb300 as fa
@@ -552,7 +571,8 @@ def run_fp8(args):
     peaks, src = load_peaks()
     flop = 4.0 * B * H * N * N * d / (2 if c else 1)
     tf = flop / (ms * 1e-3) / 1e12
-    peak = 2 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    peak = 2 * peaks["bf16_tflops"]
+    peak_sus = 2 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     in_bytes = 3 * B * H * N * d
     workload = f"fp8_b{B}h{H}_n{N}_d{d}" + ("_causal" if c else "")
     print(json.dumps({
@@ -563,8 +583,8 @@ def run_fp8(args):
                    "d": d, "causal": bool(c),
                    "l2": "no flush: inputs and output exceed the 129 MB L2" if in_bytes * 3 > 129e6 else "fits L2"},
         "roofline": {"kernel": "fa_fwd_tc_kernel<128, e4m3>", "bound": "tensor", "achieved": tf, "peak": peak,
-                     "unit": "TFLOP/s", "frac": tf / peak,
-                     "peak_source": f"2 x dense bf16 sustained ({src}); nominal fp8/bf16 ratio",
+                     "unit": "TFLOP/s", "frac": tf / peak, "frac_sustained": tf / peak_sus,
+                     "peak_source": f"2 x dense bf16 burst ({src}); nominal fp8/bf16 ratio",
                      "traffic": recorded_traffic("fa_fwd_fp8", _Named(workload))},
         "gpu_launches": args.steps, "kernels_per_step": fa.FP8_KERNELS,
     }), flush=True)

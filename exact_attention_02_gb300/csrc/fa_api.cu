@@ -8,18 +8,51 @@ namespace fa {
 
 __device__ int g_device_status;  // 0 or FA_ERR_DEVICE_TIMEOUT, per device
 
-int* device_status_ptr() {
-  static std::mutex mu;
-  static int* cache[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static const GetCurrent get_current = [] {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<int*>(p);
-  }
-  return cache[dev];
+    cudaDriverEntryPointQueryResult q{};
+    return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+                   q == cudaDriverEntryPointSuccess
+               ? reinterpret_cast<GetCurrent>(p)
+               : nullptr;
+  }();
+  static const GetId get_id = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    return cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+                   q == cudaDriverEntryPointSuccess
+               ? reinterpret_cast<GetId>(p)
+               : nullptr;
+  }();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+void* symbol_address_cached(const void* symbol, DeviceAddressCache& cache) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= DeviceAddressCache::kDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(cache.mu);
+  DeviceAddressCache::Entry& e = cache.entry[dev];
+  const unsigned long long ctx = current_context_id();
+  if (e.ptr && ctx != 0 && ctx == e.ctx) return e.ptr;
+  // First use on this device, or a new context (e.g. after cudaDeviceReset): look it up.
+  // The lookup makes the device's primary context current if none was.
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) return nullptr;
+  e.ptr = p;
+  e.ctx = current_context_id();
+  return p;
+}
+
+int* device_status_ptr() {
+  static DeviceAddressCache cache;
+  return static_cast<int*>(symbol_address_cached(&g_device_status, cache));
 }
 
 namespace {
@@ -68,7 +101,7 @@ extern "C" fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void*
     if (!status) return FA_ERR_CUDA;
     return fa::from_cuda(fa::tc_fwd(Q, K, V, O, LSE, s, scale, causal == 1, status, st));
   }
-  return fa::from_cuda(fa::simt_fwd(Q, K, V, O, LSE, s, scale, causal == 1, false, st));
+  return fa::from_cuda(fa::simt_fwd(Q, K, V, O, LSE, s, scale, causal == 1, st));
 }
 
 extern "C" fa_status_t fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE,
@@ -189,7 +222,7 @@ fa_status_t bwd_common(const void* Q, const void* K, const void* V, const void* 
                                       drop->t, status, st));
     return from_cuda(tc_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, acc, s, scale, causal == 1, status, st));
   }
-  return from_cuda(simt_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal == 1, false, st));
+  return from_cuda(simt_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, s, scale, causal == 1, st));
 }
 
 }  // namespace

@@ -1,8 +1,11 @@
 // Internal declarations shared by the library's translation units (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "../../include/fa.h"
 
@@ -18,15 +21,37 @@ struct Shape {
 
 // Device status word: bounded waits that give up write FA_ERR_DEVICE_TIMEOUT here.
 // Defined in fa_api.cu; kernels in other units reach it through this pointer, which
-// fa_api.cu resolves once per device.
+// fa_api.cu resolves once per device context.
 int* device_status_ptr();
 
-// ---- exact FFMA path (fa_simt.cu): fp32 and bf16 element types ----
+// Unique ID of the calling thread's current CUDA context (0 if there is none or the
+// query fails).
+unsigned long long current_context_id();
+
+// Device addresses of a __device__ variable, one per device, each valid for the context it
+// was looked up in: a lookup is repeated when the device's current context has changed
+// (after cudaDeviceReset, symbols move with the new context).
+struct DeviceAddressCache {
+  static constexpr int kDevices = 64;
+  struct Entry {
+    void* ptr = nullptr;
+    unsigned long long ctx = 0;
+  };
+  std::mutex mu;
+  Entry entry[kDevices];
+};
+
+// The current device's address of `symbol` (a __device__ variable of the calling
+// translation unit, passed as its host-side stand-in), from `cache` when its context is
+// unchanged; nullptr on failure.
+void* symbol_address_cached(const void* symbol, DeviceAddressCache& cache);
+
+// ---- exact FFMA path (fa_simt.cu): float32 inputs only (bf16 runs on the tensor cores) ----
 cudaError_t simt_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                     const Shape& s, float scale, bool causal, bool bf16, cudaStream_t st);
+                     const Shape& s, float scale, bool causal, cudaStream_t st);
 cudaError_t simt_bwd(const void* Q, const void* K, const void* V, const void* dO,
                      const float* LSE, const float* D, void* dQ, void* dK, void* dV,
-                     const Shape& s, float scale, bool causal, bool bf16, cudaStream_t st);
+                     const Shape& s, float scale, bool causal, cudaStream_t st);
 
 // ---- tcgen05 tensor-core path (bf16, d in {64, 128}, N % 128 == 0) ----
 cudaError_t tc_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,

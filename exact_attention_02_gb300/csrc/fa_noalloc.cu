@@ -11,11 +11,10 @@
 // The array lives in every GPU context that loads this library, from load until exit.
 // Host code cannot use its name as a device address (it is a host-side stand-in), so the
 // first call on each device looks the address up with cudaGetSymbolAddress while that
-// device is current, and caches it. All calls share the array: the dQ accumulator is
+// device is current, and caches it for that device's context (a call in a new context,
+// e.g. after cudaDeviceReset, looks it up again). All calls share the array: the dQ accumulator is
 // cleared by every call before use, and calls that overlap on the GPU (other streams,
 // other threads) race on it.
-#include <mutex>
-
 #include "fa_internal.h"
 
 namespace fa {
@@ -29,19 +28,11 @@ constexpr size_t kScratchBytes = (kAccFloats + kDFloats) * sizeof(float);
 
 static __device__ __align__(256) float g_bwd_scratch[kAccFloats + kDFloats];
 
-// Device address of g_bwd_scratch on the current device (nullptr on failure).
+// Device address of g_bwd_scratch on the current device (nullptr on failure), looked up
+// once per device context: a new context (after cudaDeviceReset) places the array anew.
 void* scratch_address() {
-  static std::mutex mu;
-  static void* cache[64] = {};
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess) return nullptr;
-    cache[dev] = p;
-  }
-  return cache[dev];
+  static DeviceAddressCache cache;
+  return symbol_address_cached(g_bwd_scratch, cache);
 }
 
 }  // namespace

@@ -29,7 +29,8 @@ namespace {
 constexpr int kMaxChunks = 16;
 constexpr int kSlots = 3;
 constexpr int kEventsPerChunk = 5;
-constexpr int kRing = kMaxChunks * kEventsPerChunk + 2;
+constexpr int kRing = kMaxChunks * kEventsPerChunk + 1;  // + the fork event
+constexpr int kJoinEvents = 3;                            // error join: one per internal stream
 
 size_t round_up(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -65,6 +66,7 @@ SlotLayout slot_layout(int64_t hc, int N, int d) {
 struct DeviceQueues {
   cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
   cudaEvent_t ring[kRing] = {};
+  cudaEvent_t join[kJoinEvents] = {};
   bool ok = false;
 };
 
@@ -83,6 +85,8 @@ DeviceQueues* queues_for_current_device() {
               cudaStreamCreateWithFlags(&q.comp, cudaStreamNonBlocking) == cudaSuccess &&
               cudaStreamCreateWithFlags(&q.out, cudaStreamNonBlocking) == cudaSuccess;
     for (int i = 0; ok && i < kRing; ++i) ok = cudaEventCreateWithFlags(&q.ring[i], cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kJoinEvents; ++i)
+      ok = cudaEventCreateWithFlags(&q.join[i], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) return nullptr;
     q.ok = true;
   }
@@ -126,54 +130,32 @@ extern "C" size_t fa_fwd_bwd_host_workspace_size(int B, int H, int N, int d, int
   return fa::kSlots * fa::slot_layout(g.largest, N, d).bytes;
 }
 
-extern "C" fa_status_t fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const void* dO, void* O,
-                                       float* LSE, void* dQ, void* dK, void* dV, void* workspace,
-                                       size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
-                                       int dtype, int chunks, void* stream) {
-  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
-  if (!(scale > 0.f && scale < INFINITY)) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  for (const void* p : {Q, K, V, dO, (const void*)O, (const void*)LSE, (const void*)dQ, (const void*)dK,
-                        (const void*)dV})
-    if (!p) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_DTYPE_BF16 || (d != 64 && d != 128)) return FA_ERR_UNSUPPORTED;
-  if ((int64_t)B * H * N > INT32_MAX) return FA_ERR_UNSUPPORTED;
-  const size_t need = fa_fwd_bwd_host_workspace_size(B, H, N, d, dtype, chunks);
-  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
+namespace fa {
+namespace {
 
-  const fa::Groups G = fa::make_groups((int64_t)B * H, chunks);
-  const int ng = G.n;
-  const fa::SlotLayout L = fa::slot_layout(G.largest, N, d);
-  const size_t head_el = (size_t)N * d * 2, head_rows = (size_t)N * 4;
-
-  std::lock_guard<std::mutex> lock(fa::g_mu);
-  fa::DeviceQueues* qs = fa::queues_for_current_device();
-  if (!qs) return FA_ERR_CUDA;
-  cudaStream_t caller = static_cast<cudaStream_t>(stream);
-  int ev = 0;
+// Enqueues every group's copy-in, kernels and copy-out on the internal streams (which have
+// already forked from the caller's stream) and joins the caller's stream to the last
+// copy-out. Returns at the first failure, with some work possibly enqueued.
+fa_status_t enqueue_groups(const void* Q, const void* K, const void* V, const void* dO, void* O, float* LSE,
+                           void* dQ, void* dK, void* dV, void* workspace, int N, int d, float scale, int causal,
+                           int dtype, const Groups& G, const SlotLayout& L, DeviceQueues* qs, int& ev,
+                           cudaStream_t caller) {
   auto next_event = [&]() { return qs->ring[ev++]; };
+  const int ng = G.n;
+  const size_t head_el = (size_t)N * d * 2, head_rows = (size_t)N * 4;
 #define FA_TRY(x)                                   \
   do {                                              \
     const cudaError_t e_ = (x);                     \
     if (e_ != cudaSuccess) return FA_ERR_CUDA;      \
   } while (0)
-  // fork: every internal stream starts after the work already queued on the caller's stream
-  cudaEvent_t start = next_event();
-  FA_TRY(cudaEventRecord(start, caller));
-  FA_TRY(cudaStreamWaitEvent(qs->in, start, 0));
-  FA_TRY(cudaStreamWaitEvent(qs->comp, start, 0));
-  FA_TRY(cudaStreamWaitEvent(qs->out, start, 0));
-
-  cudaEvent_t out_done[fa::kMaxChunks] = {};
+  cudaEvent_t out_done[kMaxChunks] = {};
   for (int g = 0; g < ng; ++g) {
     const int64_t h0 = G.start[g], nh = G.start[g + 1] - h0;
-    char* slot = static_cast<char*>(workspace) + (size_t)(g % fa::kSlots) * L.bytes;
+    char* slot = static_cast<char*>(workspace) + (size_t)(g % kSlots) * L.bytes;
     const size_t el = (size_t)nh * head_el, rows = (size_t)nh * head_rows;
     const size_t off = (size_t)h0 * head_el, roff = (size_t)h0 * head_rows;
     // copy-in, once the slot's previous group has been copied out
-    if (g >= fa::kSlots) FA_TRY(cudaStreamWaitEvent(qs->in, out_done[g - fa::kSlots], 0));
+    if (g >= kSlots) FA_TRY(cudaStreamWaitEvent(qs->in, out_done[g - kSlots], 0));
     FA_TRY(cudaMemcpyAsync(slot + L.q, static_cast<const char*>(Q) + off, el, cudaMemcpyHostToDevice, qs->in));
     FA_TRY(cudaMemcpyAsync(slot + L.k, static_cast<const char*>(K) + off, el, cudaMemcpyHostToDevice, qs->in));
     FA_TRY(cudaMemcpyAsync(slot + L.v, static_cast<const char*>(V) + off, el, cudaMemcpyHostToDevice, qs->in));
@@ -218,3 +200,53 @@ extern "C" fa_status_t fa_fwd_bwd_host(const void* Q, const void* K, const void*
 #undef FA_TRY
   return FA_OK;
 }
+
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status_t fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const void* dO, void* O,
+                                       float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                                       size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                                       int dtype, int chunks, void* stream) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f && scale < INFINITY)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  for (const void* p : {Q, K, V, dO, (const void*)O, (const void*)LSE, (const void*)dQ, (const void*)dK,
+                        (const void*)dV})
+    if (!p) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 || (d != 64 && d != 128)) return FA_ERR_UNSUPPORTED;
+  if ((int64_t)B * H * N > INT32_MAX) return FA_ERR_UNSUPPORTED;
+  const size_t need = fa_fwd_bwd_host_workspace_size(B, H, N, d, dtype, chunks);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
+
+  const fa::Groups G = fa::make_groups((int64_t)B * H, chunks);
+  const fa::SlotLayout L = fa::slot_layout(G.largest, N, d);
+
+  std::lock_guard<std::mutex> lock(fa::g_mu);
+  fa::DeviceQueues* qs = fa::queues_for_current_device();
+  if (!qs) return FA_ERR_CUDA;
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  int ev = 0;
+  // fork: every internal stream starts after the work already queued on the caller's stream
+  cudaEvent_t start = qs->ring[ev++];
+  if (cudaEventRecord(start, caller) != cudaSuccess) return FA_ERR_CUDA;
+  fa_status_t r = FA_OK;
+  if (cudaStreamWaitEvent(qs->in, start, 0) != cudaSuccess || cudaStreamWaitEvent(qs->comp, start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(qs->out, start, 0) != cudaSuccess)
+    r = FA_ERR_CUDA;
+  if (r == FA_OK)
+    r = fa::enqueue_groups(Q, K, V, dO, O, LSE, dQ, dK, dV, workspace, N, d, scale, causal, dtype, G, L, qs, ev,
+                           caller);
+  if (r != FA_OK) {
+    // Work already enqueued on the internal streams keeps running after a failure: the
+    // caller's stream waits for all of it, so that synchronising that stream before freeing
+    // or reusing the buffers is safe even after an error.
+    const cudaStream_t internal[fa::kJoinEvents] = {qs->in, qs->comp, qs->out};
+    for (int i = 0; i < fa::kJoinEvents; ++i)
+      if (cudaEventRecord(qs->join[i], internal[i]) == cudaSuccess) cudaStreamWaitEvent(caller, qs->join[i], 0);
+  }
+  return r;
+}
+

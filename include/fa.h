@@ -116,7 +116,9 @@ FA_API fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const voi
  * Arguments and results are those of fa_bwd (without workspace / workspace_bytes).
  * Limits: B*H*N*d <= FA_NOALLOC_MAX_ELEMS, else FA_ERR_WORKSPACE and nothing runs.
  * First call on a device: looks up the array's device address (cudaGetSymbolAddress) with
- * that device current and caches it; make that first call before any stream capture.
+ * that device current and caches it for the device's current context (a first call in a
+ * new context, e.g. after cudaDeviceReset, looks it up again); make that first call before
+ * any stream capture.
  * Sharing: all calls use the same array. Each call clears the accumulator before use, so
  * leftovers of earlier calls do not leak into results, but calls that overlap on the GPU
  * (concurrent streams or threads) race on the array and must be serialised by the caller.
@@ -267,8 +269,9 @@ FA_API fa_status_t fa_fwd_fp8(const void* Q, const void* K, const void* V, void*
  *      for all of it: the outputs are in host memory once `stream` has been synchronised.
  *      The call itself does not block.
  * Supported: bf16, d in {64, 128}, causal 0/1, B*H*N < 2^31 (else FA_ERR_UNSUPPORTED).
- * Errors: as for fa_fwd / fa_bwd; a failure returned after some work was enqueued leaves
- *      that work running: synchronise the device before reusing the buffers.
+ * Errors: as for fa_fwd / fa_bwd. A failure returned after some work was enqueued leaves
+ *      that work running, but `stream` still waits for all of it: synchronise `stream`
+ *      before freeing or reusing the buffers.
  */
 FA_API size_t fa_fwd_bwd_host_workspace_size(int B, int H, int N, int d, int dtype, int chunks);
 FA_API fa_status_t fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const void* dO, void* O,

@@ -67,7 +67,9 @@ def test_dropout_matches_oracle(case):
             K = philox.keep_matrix(seed, b * H + h, N, N, p)
             ref = ora.head_backward(*(x[b, h].astype(np.float64) for x in (q, k, v, do)), scale, causal,
                                     keep=K, keep_scale=c)
-            assert np.abs(got["o"][b, h] - ref["o"]).max() <= 2e-2 * c, (b, h)
+            # O grows by c with the kept weights, and so does its bf16 rounding: the fixed
+            # bound applies to O / c
+            assert np.abs(got["o"][b, h] - ref["o"]).max() / c <= 2e-2, (b, h)
             assert np.abs(got["lse"][b, h] - ref["lse"]).max() <= 1e-3, (b, h)
             for n in ("dq", "dk", "dv"):
                 assert _rel(got[n][b, h], ref[n]) <= 2e-2, (b, h, n, _rel(got[n][b, h], ref[n]))

@@ -55,10 +55,30 @@ def _rel(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
 
 
-def check(w: Workload, got: dict, ref: dict, where=""):
-    """Compare the GPU arrays to the oracle's over the same index set."""
+def check_d(got: dict, ref: dict, do, where=""):
+    """D = rowsum(dO * O) from the preprocess pass, against the oracle's D (from its fp64 O).
+
+    The kernel sums dO * O over its own stored O, in fp32, so per row
+      |D - D_ref| <= sum_c |dO_c| |O_c - O_ref_c|  +  d 2^-24 sum_c |dO_c O_c|  (+ 1e-6),
+    the first term from the forward's O error (whatever its size) and the second from the
+    fp32 accumulation. A second check holds the pass to the fp32 term alone against the row
+    dot product of the stored O, in fp64."""
+    do = np.asarray(do, np.float64)
+    dcol = do.shape[-1]
+    o = got["o"]
+    err = np.abs(got["d"] - ref["d"])
+    bound = (np.abs(do) * np.abs(o - ref["o"])).sum(-1) + dcol * 2.0 ** -24 * np.abs(do * o).sum(-1) + 1e-6
+    assert (err <= bound).all(), (where, "D", float((err - bound).max()))
+    own = np.einsum("...c,...c->...", do, o)
+    assert (np.abs(got["d"] - own) <= dcol * 2.0 ** -24 * np.abs(do * o).sum(-1) + 1e-6).all(), (where, "D own")
+
+
+def check(w: Workload, got: dict, ref: dict, where="", do=None):
+    """Compare the GPU arrays to the oracle's over the same index set (D too, given dO)."""
     for n in ("o", "lse", "dq", "dk", "dv"):
         assert np.isfinite(got[n]).all(), (where, n, "non-finite")
+    if do is not None:
+        check_d(got, ref, do, where)
     if w.dtype == "fp32":
         for n in ("o", "lse", "dq", "dk", "dv"):
             err = np.abs(got[n] - ref[n]).max()
@@ -76,7 +96,7 @@ def check(w: Workload, got: dict, ref: dict, where=""):
 def _compare_all(w, x):
     got = run_gpu(w, x)
     ref = ora.backward(*(x[n].astype(np.float64) for n in ("q", "k", "v", "do")), w.scale, w.causal)
-    check(w, got, ref, w.name)
+    check(w, got, ref, w.name, do=x["do"])
     return got, ref
 
 
@@ -220,7 +240,7 @@ def test_workload_full_size(name):
     got = run_gpu(w, x)
     if w.B * w.H * w.N <= 4096:
         ref = ora.backward(*(x[n].astype(np.float64) for n in ("q", "k", "v", "do")), w.scale, w.causal)
-        check(w, got, ref, name)
+        check(w, got, ref, name, do=x["do"])
         return
     heads = _heads_to_check(w)
     if w.N >= 32768:
@@ -228,7 +248,7 @@ def test_workload_full_size(name):
     for b, h in heads:
         args = [x[n][b, h].astype(np.float64) for n in ("q", "k", "v", "do")]
         ref = ora.head_backward(*args, w.scale, w.causal)
-        check(w, {n: got[n][b, h] for n in got}, ref, f"{name} head ({b},{h})")
+        check(w, {n: got[n][b, h] for n in got}, ref, f"{name} head ({b},{h})", do=x["do"][b, h])
     # every head: sampled query rows of O and LSE
     rng = np.random.default_rng(1234)
     rows = np.unique(np.concatenate([[0, w.N - 1], rng.integers(0, w.N, 6)]))
