@@ -58,6 +58,12 @@ def _load():
     L.fa_bwd_workspace_size.restype = sz
     L.fa_bwd.argtypes = [vp] * 11 + [sz, i, i, i, i, f, i, i, vp]
     L.fa_bwd.restype = i
+    L.fa_fwd_rect.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    L.fa_fwd_rect.restype = i
+    L.fa_bwd_rect_workspace_size.argtypes = [i, i, i, i, i, i]
+    L.fa_bwd_rect_workspace_size.restype = sz
+    L.fa_bwd_rect.argtypes = [vp] * 11 + [sz, i, i, i, i, i, f, i, i, vp]
+    L.fa_bwd_rect.restype = i
     L.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i, i]
     L.fa_fwd_splitkv_workspace_size.restype = sz
     L.fa_fwd_splitkv.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -86,6 +92,8 @@ def _load():
     L.fa_get_error_string.restype = ctypes.c_char_p
     L.fa_get_last_device_status.argtypes = []
     L.fa_get_last_device_status.restype = i
+    L.fa_test_inject_timeout.argtypes = [i, ctypes.c_ulonglong]
+    L.fa_test_inject_timeout.restype = i
     _lib = L
     return L
 
@@ -297,6 +305,57 @@ def fa_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None, D=None
     return dq, dk, dv
 
 
+def _rect_shapes(q, k, v, *others_q):
+    """(B, H, Nq, Nk, d) of q [B,H,Nq,d] against k, v [B,H,Nk,d]; checks contiguity, dtype
+    and device, and that the tensors in ``others_q`` have q's shape."""
+    B, H, Nq, d = _shape(q)
+    if k.dim() != 4 or k.shape != v.shape or tuple(k.shape[:2]) != (B, H) or int(k.shape[3]) != d:
+        raise ValueError("k and v must be [B, H, Nk, d] with the batch, heads and d of q")
+    for t in (q, k, v) + tuple(t for t in others_q if t is not None):
+        if not t.is_contiguous() or t.dtype != q.dtype or t.device != q.device:
+            raise ValueError("tensors must be contiguous and share dtype and device")
+    for t in others_q:
+        if t is not None and t.shape != q.shape:
+            raise ValueError("O, dO and dQ must have q's shape")
+    return B, H, Nq, int(k.shape[2]), d
+
+
+def fa_fwd_rect(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None, stream=None):
+    """O, LSE for q [B,H,Nq,d] against k, v [B,H,Nk,d] (see ``fa_fwd_rect`` in fa.h; causal
+    is bottom-right aligned: query i hides keys j > i + Nk - Nq)."""
+    import torch
+    B, H, Nq, Nk, d = _rect_shapes(q, k, v, o)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(_load().fa_fwd_rect(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, Nq, Nk, d, scale, int(bool(causal)),
+                               _dtype_code(q), _stream_ptr(stream)), "fa_fwd_rect")
+    return o, lse
+
+
+def fa_bwd_rect(q, k, v, o, do, lse, causal: bool, scale: float | None = None, D=None, dq=None, dk=None, dv=None,
+                workspace=None, stream=None):
+    """dQ [B,H,Nq,d], dK, dV [B,H,Nk,d] from the outputs of ``fa_fwd_rect`` (see
+    ``fa_bwd_rect`` in fa.h)."""
+    import torch
+    B, H, Nq, Nk, d = _rect_shapes(q, k, v, o, do, dq)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dk.shape != k.shape or dv.shape != v.shape or not dk.is_contiguous() or not dv.is_contiguous():
+        raise ValueError("dK and dV must be contiguous with k's shape")
+    code = _dtype_code(q)
+    need = int(_load().fa_bwd_rect_workspace_size(B, H, Nq, Nk, d, code)) + (0 if D is not None else 4 * B * H * Nq)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_load().fa_bwd_rect(_p(q), _p(k), _p(v), _p(o), _p(do), _p(lse), _p(D), _p(dq), _p(dk), _p(dv),
+                               _p(workspace), wbytes, B, H, Nq, Nk, d, scale, int(bool(causal)), code,
+                               _stream_ptr(stream)), "fa_bwd_rect")
+    return dq, dk, dv
+
+
 def fa_fwd_splitkv(q, k, v, causal: bool, scale: float | None = None, o=None, lse=None, workspace=None,
                    stream=None):
     """O, LSE for a few queries q [B,H,Nq,d] against k, v [B,H,Nk,d] (see ``fa_fwd_splitkv`` in fa.h)."""
@@ -374,3 +433,12 @@ def fa_fwd_bwd_host(q, k, v, do, causal: bool, scale: float | None = None, out=N
 
 def fa_get_last_device_status() -> int:
     return int(_load().fa_get_last_device_status())
+
+
+# Failure-path test hook (see ``fa_test_inject_timeout`` in fa.h): which = 1 makes the
+# first CTA of fa_fwd skip one producer arrival, 2 the same in fa_bwd, 0 turns it off.
+FA_INJECT_OFF, FA_INJECT_FWD, FA_INJECT_BWD = 0, 1, 2
+
+
+def fa_test_inject_timeout(which: int, wait_limit_ns: int = 0) -> None:
+    _check(_load().fa_test_inject_timeout(int(which), int(wait_limit_ns)), "fa_test_inject_timeout")

@@ -3,10 +3,12 @@
 #include <mutex>
 
 #include "fa_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace fa {
 
-__device__ int g_device_status;  // 0 or FA_ERR_DEVICE_TIMEOUT, per device
+// Per device: the status word (0 or FA_ERR_DEVICE_TIMEOUT) and the failure-path test hooks.
+__device__ ptx::StatusBlock g_device_block;
 
 unsigned long long current_context_id() {
   using GetCurrent = CUresult (*)(CUcontext*);
@@ -52,25 +54,29 @@ void* symbol_address_cached(const void* symbol, DeviceAddressCache& cache) {
 
 int* device_status_ptr() {
   static DeviceAddressCache cache;
-  return static_cast<int*>(symbol_address_cached(&g_device_status, cache));
+  void* block = symbol_address_cached(&g_device_block, cache);
+  return block ? &static_cast<ptx::StatusBlock*>(block)->status : nullptr;
 }
 
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Checks sizes, dtype and scale. s.N is the query length; s.keys() the key length (s.Nk
+// is 0 for the square entry points, which makes it N as well; a negative s.Nk is invalid).
 fa_status_t check_shape(const Shape& s, int dtype, float* scale) {
-  if (s.B < 1 || s.H < 1 || s.N < 1 || s.d < 1) return FA_ERR_INVALID_ARG;
+  if (s.B < 1 || s.H < 1 || s.N < 1 || s.d < 1 || s.Nk < 0) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_INVALID_ARG;
   // B*H*N*d must be representable; keep B*H below 2^31 and the element count < 2^60.
   const int64_t bh = (int64_t)s.B * s.H;
+  const int64_t longest = s.N > s.keys() ? s.N : s.keys();
   if (bh >= (int64_t(1) << 31)) return FA_ERR_INVALID_ARG;
-  if (bh * s.N > (int64_t(1) << 50) || s.elems() > (int64_t(1) << 60)) return FA_ERR_INVALID_ARG;
+  if (bh * longest > (int64_t(1) << 50) || bh * longest * s.d > (int64_t(1) << 60)) return FA_ERR_INVALID_ARG;
   if (scale && !(isfinite(*scale) && *scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (s.d != 64 && s.d != 128) return FA_ERR_UNSUPPORTED;
-  // TMA coordinates are 32-bit row indices into the [B*H*N, d] view.
-  if (dtype == FA_DTYPE_BF16 && bh * s.N > INT32_MAX) return FA_ERR_UNSUPPORTED;
-  if (dtype == FA_DTYPE_FP32 && s.N > 4096) return FA_ERR_UNSUPPORTED;
+  // TMA coordinates are 32-bit row indices into the [B*H*rows, d] views.
+  if (dtype == FA_DTYPE_BF16 && bh * longest > INT32_MAX) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_FP32 && longest > 4096) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -87,21 +93,38 @@ fa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_
 
 using fa::Shape;
 
-extern "C" fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                              int B, int H, int N, int d, float scale, int causal, int dtype,
-                              void* stream) {
-  const Shape s{B, H, N, d};
-  fa_status_t r = fa::check_shape(s, dtype, &scale);
+namespace fa {
+namespace {
+fa_status_t fwd_common(const void* Q, const void* K, const void* V, void* O, float* LSE, const Shape& s,
+                       float scale, int causal, int dtype, void* stream) {
+  fa_status_t r = check_shape(s, dtype, &scale);
   if (r != FA_OK) return r;
-  if ((r = fa::check_ptrs({Q, K, V, O, LSE})) != FA_OK) return r;
+  if ((r = check_ptrs({Q, K, V, O, LSE})) != FA_OK) return r;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == FA_DTYPE_BF16) {
-    int* status = fa::device_status_ptr();
+    int* status = device_status_ptr();
     if (!status) return FA_ERR_CUDA;
-    return fa::from_cuda(fa::tc_fwd(Q, K, V, O, LSE, s, scale, causal == 1, status, st));
+    return from_cuda(tc_fwd(Q, K, V, O, LSE, s, scale, causal == 1, status, st));
   }
-  return fa::from_cuda(fa::simt_fwd(Q, K, V, O, LSE, s, scale, causal == 1, st));
+  return from_cuda(simt_fwd(Q, K, V, O, LSE, s, scale, causal == 1, st));
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status_t fa_fwd_rect(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                                   int H, int Nq, int Nk, int d, float scale, int causal, int dtype,
+                                   void* stream) {
+  if (Nk < 1) return FA_ERR_INVALID_ARG;
+  Shape s{B, H, Nq, d};
+  s.Nk = Nk;
+  return fa::fwd_common(Q, K, V, O, LSE, s, scale, causal, dtype, stream);
+}
+
+extern "C" fa_status_t fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                              int B, int H, int N, int d, float scale, int causal, int dtype,
+                              void* stream) {
+  return fa::fwd_common(Q, K, V, O, LSE, Shape{B, H, N, d}, scale, causal, dtype, stream);
 }
 
 extern "C" fa_status_t fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE,
@@ -184,8 +207,9 @@ fa_status_t drop_threshold(float p, int dtype, uint32_t* t) {
 fa_status_t bwd_common(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                        const float* LSE, const float* D, void* dQ, void* dK, void* dV, void* workspace,
                        size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal, int dtype,
-                       const Mask* mask, const Drop* drop, void* stream, const Mask* bits = nullptr) {
-  const Shape s{B, H, N, d};
+                       const Mask* mask, const Drop* drop, void* stream, const Mask* bits = nullptr, int Nk = 0) {
+  Shape s{B, H, N, d};
+  s.Nk = Nk;
   fa_status_t r = check_shape(s, dtype, &scale);
   if (r != FA_OK) return r;
   if ((r = check_ptrs({Q, K, V, O, dO, LSE, dQ, dK, dV})) != FA_OK) return r;
@@ -235,6 +259,23 @@ extern "C" fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const
                               void* stream) {
   return fa::bwd_common(Q, K, V, O, dO, LSE, D, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, scale, causal,
                         dtype, nullptr, nullptr, stream);
+}
+
+extern "C" size_t fa_bwd_rect_workspace_size(int B, int H, int Nq, int Nk, int d, int dtype) {
+  if (Nk < 1) return 0;
+  Shape s{B, H, Nq, d};
+  s.Nk = Nk;
+  if (fa::check_shape(s, dtype, nullptr) != FA_OK) return 0;
+  return dtype == FA_DTYPE_BF16 ? (size_t)s.elems() * sizeof(float) : 0;
+}
+
+extern "C" fa_status_t fa_bwd_rect(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                                   const float* LSE, const float* D, void* dQ, void* dK, void* dV, void* workspace,
+                                   size_t workspace_bytes, int B, int H, int Nq, int Nk, int d, float scale,
+                                   int causal, int dtype, void* stream) {
+  if (Nk < 1) return FA_ERR_INVALID_ARG;
+  return fa::bwd_common(Q, K, V, O, dO, LSE, D, dQ, dK, dV, workspace, workspace_bytes, B, H, Nq, d, scale, causal,
+                        dtype, nullptr, nullptr, stream, nullptr, Nk);
 }
 
 extern "C" fa_status_t fa_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE,
@@ -376,4 +417,15 @@ extern "C" fa_status_t fa_get_last_device_status(void) {
     if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
   }
   return v == 0 ? FA_OK : static_cast<fa_status_t>(v);
+}
+
+extern "C" fa_status_t fa_test_inject_timeout(int which, unsigned long long wait_limit_ns) {
+  if (which != 0 && which != fa::ptx::kInjectFwd && which != fa::ptx::kInjectBwd) return FA_ERR_INVALID_ARG;
+  int* p = fa::device_status_ptr();
+  if (!p) return FA_ERR_CUDA;
+  fa::ptx::StatusBlock* b = reinterpret_cast<fa::ptx::StatusBlock*>(p);
+  if (cudaMemcpy(&b->inject, &which, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(&b->limit_ns, &wait_limit_ns, sizeof(unsigned long long), cudaMemcpyHostToDevice) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
 }

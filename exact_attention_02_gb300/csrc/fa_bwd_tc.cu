@@ -34,9 +34,15 @@
 // boolean mask (packed bits, as the forward reads them) and dropout zero P for hidden or
 // dropped keys, so their dS is 0 as well; kept dropout weights are scaled by 256 / (256 - t).
 //
-// Any N: Q/K/V/dO are read through [heads, N, d] tensor maps (rows past the end of a head
-// arrive as zeros), queries past the end get LSE = +inf (P = 0), and dQ/dK/dV rows past
-// the end are neither accumulated nor stored.
+// Query and key lengths: Nq query rows against Nk key/value rows per head (Nq = Nk for
+// fa_bwd); causal is bottom-right aligned (query i hides keys j > i + Nk - Nq), so a key
+// tile starts at the first query tile that sees any of its keys (with this alignment every
+// key is seen by the last query; a tile that no query saw would get dK = dV = 0). Queries
+// that see no key (Nq > Nk) have LSE = -inf from the
+// forward; every one of their keys is hidden by the causal rule, so their P is 0.
+// Any lengths: Q/K/V/dO are read through [heads, rows, d] tensor maps (rows past the end of
+// a head arrive as zeros), queries past the end get LSE = +inf (P = 0), and dQ/dK/dV rows
+// past the end are neither accumulated nor stored.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -104,11 +110,13 @@ struct BwdParams {
   __nv_bfloat16* dK;
   __nv_bfloat16* dV;
   int* status;
-  int N;
+  int Nq;      // query rows per head
+  int Nk;      // key / value rows per head
   int heads;
   int kvtiles;
   int qtiles;
   int causal;
+  int offset;  // causal: query i hides keys j > i + offset (offset = Nk - Nq, bottom-right)
   float scale;
   float sl2;  // scale * log2(e)
   // additive mask (kMask): element (b, h, i, j) at mask[b*mask_sb + h*mask_sh + i*mask_srow + j]
@@ -185,9 +193,23 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     kt = (int)(blockIdx.x % p.kvtiles);
     head = (int)(blockIdx.x / p.kvtiles);
   }
-  const int row_base = head * p.N;
-  const int q_first = p.causal ? (kt * BN) / BQ : 0;
+  const int qrow_base = head * p.Nq;  // LSE, D and dQ rows of the head
+  const int krow_base = head * p.Nk;  // dK and dV rows of the head
+  // causal: the first query tile holding a query that sees key kt * BN (query + offset >= key)
+  const int q_first = p.causal ? max(0, kt * BN - p.offset) / BQ : 0;
   const int nq = p.qtiles - q_first;
+  if (nq <= 0) {
+    // No query sees a key of this tile (causal with more keys past the last query's limit
+    // than the tile start): dK = dV = 0 for its rows, nothing else to do.
+    if (threadIdx.x < BN && kt * BN + (int)threadIdx.x < p.Nk) {
+      const size_t row = (size_t)krow_base + kt * BN + threadIdx.x;
+      uint4* dk = reinterpret_cast<uint4*>(p.dK + row * D);
+      uint4* dv = reinterpret_cast<uint4*>(p.dV + row * D);
+#pragma unroll
+      for (int u = 0; u < D / 8; ++u) dk[u] = dv[u] = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl.kv_full, 1);
@@ -233,8 +255,11 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
     }
     int last[3] = {-1, -1, -1};
+    // Test hook of the failure path: never arm the first Q/dO stage, so the MMA thread's
+    // wait for it runs out (see StatusBlock); off unless a test sets it.
+    const bool skip_first = injected(p.status, kInjectBwd);
     // When every tile of the head takes the bulk path, lane 0 runs the loop alone.
-    const bool all_bulk = !kTail || ((p.N % BQ) == 0 && (p.N % 4) == 0);
+    const bool all_bulk = !kTail || ((p.Nq % BQ) == 0 && (p.Nq % 4) == 0);
     for (int it = 0; it < nq && (lane == 0 || !all_bulk); ++it) {
       const int s = it % C::kStages;
       bool ok = true;
@@ -245,15 +270,16 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const int q0 = (q_first + it) * BQ;  // first query of the tile, within the head
       uint8_t* st = smem + C::kStageOff + s * C::kStageBytes;
       float* vec = reinterpret_cast<float*>(smem + C::kVecOff + s * C::kVecBytes);
-      const bool bulk = !kTail || (q0 + BQ <= p.N && (p.N % 4) == 0);
+      const bool bulk = !kTail || (q0 + BQ <= p.Nq && (p.Nq % 4) == 0);
       if (!bulk) {
         for (int c = lane; c < BQ; c += 32) {
-          const bool in = q0 + c < p.N;
-          vec[c] = in ? p.LSE[row_base + q0 + c] : INFINITY;
-          vec[BQ + c] = in ? p.Dvec[row_base + q0 + c] : 0.f;
+          const bool in = q0 + c < p.Nq;
+          vec[c] = in ? p.LSE[qrow_base + q0 + c] : INFINITY;
+          vec[BQ + c] = in ? p.Dvec[qrow_base + q0 + c] : 0.f;
         }
         __syncwarp();
       }
+      if (it == 0 && skip_first) continue;
       if (lane == 0) {
         mbar_expect_tx(&ctl.stage_full[s], C::kStageBytes + (bulk ? C::kVecBytes : 0));
         for (int b = 0; b < C::kBoxes; ++b) {
@@ -261,8 +287,8 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           tma_load_3d(st + C::kQBytes + b * C::kQBox, &tmdO, &ctl.stage_full[s], b * 64, q0, head);
         }
         if (bulk) {
-          bulk_load(vec, p.LSE + row_base + q0, BQ * 4, &ctl.stage_full[s]);
-          bulk_load(vec + BQ, p.Dvec + row_base + q0, BQ * 4, &ctl.stage_full[s]);
+          bulk_load(vec, p.LSE + qrow_base + q0, BQ * 4, &ctl.stage_full[s]);
+          bulk_load(vec + BQ, p.Dvec + qrow_base + q0, BQ * 4, &ctl.stage_full[s]);
         }
       }
       last[s] = it;
@@ -385,7 +411,7 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         kBits ? p.bits + (int64_t)(head / p.H) * p.mask_sb + (int64_t)(head % p.H) * p.mask_sh + kword : nullptr;
     auto bits_word = [&](int it) -> uint32_t {
       const int q = (q_first + it) * BQ + wg * kCols + lane;
-      return (it < nq && (!kTail || (q < p.N && kword * 32 < p.N))) ? bcol[(int64_t)q * p.mask_srow] : 0u;
+      return (it < nq && (!kTail || (q < p.Nq && kword * 32 < p.Nk))) ? bcol[(int64_t)q * p.mask_srow] : 0u;
     };
     uint32_t bword = kBits ? bits_word(0) : 0u;
     bool ok = true;
@@ -399,7 +425,8 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       tc_fence_after();
       const float* vec = reinterpret_cast<const float*>(smem + C::kVecOff + s * C::kVecBytes);
       const int q0 = (q_first + it) * BQ;
-      const bool diag = p.causal && q0 < kt * BN + BN;  // some key of the tile exceeds some query
+      // some key of the tile exceeds the limit of some query of the tile
+      const bool diag = p.causal && q0 + p.offset < kt * BN + BN - 1;
       uint8_t* dsrow = smem + C::kDsOff + (it & 1) * C::kDsBytes + r * 128;
 #pragma unroll
       for (int ch = 0; ch < kCols / 32; ++ch) {
@@ -414,7 +441,7 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int q = q0 + c0 + c;
-            mk[c] = (!kTail || (key < p.N && q < p.N))
+            mk[c] = (!kTail || (key < p.Nk && q < p.Nq))
                         ? __bfloat162float(mcol[(int64_t)q * p.mask_srow]) * kLog2e
                         : 0.f;
           }
@@ -465,8 +492,8 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             if (!((vbits >> (2 * u + 1)) & 1u)) pr.y = 0.f;
           }
           if (diag) {
-            if (key > q0 + c) pr.x = 0.f;
-            if (key > q0 + c + 1) pr.y = 0.f;
+            if (key > q0 + c + p.offset) pr.x = 0.f;
+            if (key > q0 + c + 1 + p.offset) pr.y = 0.f;
           }
           float2 dd;
           if constexpr (kDrop) {  // dP of a dropped key is 0; a kept one is scaled
@@ -512,8 +539,8 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       // at d = 128 one dQ thread frees that stage here instead of a separate MMA commit: one
       // commit fewer per tile, measured 1% faster at d = 128 (and 2% slower at d = 64).
       if (D == 128 && warp == kDqWarp0 && lane == 0) mbar_arrive(&ctl.stage_empty[it % C::kStages]);
-      const int q0 = row_base + (q_first + it) * BQ;
-      const int nvalid = p.N - (q_first + it) * BQ;  // queries of the tile inside the head
+      const int q0 = qrow_base + (q_first + it) * BQ;
+      const int nvalid = p.Nq - (q_first + it) * BQ;  // queries of the tile inside the head
       const uint32_t colQ = C::colS(it % C::NB);
       // lane = head-dim index r; columns = the BQ queries of the tile, released as soon as
       // they are in registers
@@ -544,8 +571,8 @@ fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.kv_done, 0, p.status, abort));
     if (ok) {
       tc_fence_after();
-      const size_t row = (size_t)row_base + kt * BN + r;
-      const bool in = !kTail || kt * BN + r < p.N;  // key rows past the end are not stored
+      const size_t row = (size_t)krow_base + kt * BN + r;
+      const bool in = !kTail || kt * BN + r < p.Nk;  // key rows past the end are not stored
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         float v[32];
@@ -617,8 +644,8 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
   using C = BwdCfg<D>;
   CUtensorMap mq, mk, mv, mdo;
   const int64_t heads = s.heads();
-  if (!make_map_bf16_3d(&mq, Q, heads, s.N, D, C::BQ) || !make_map_bf16_3d(&mk, K, heads, s.N, D, BN) ||
-      !make_map_bf16_3d(&mv, V, heads, s.N, D, BN) || !make_map_bf16_3d(&mdo, dO, heads, s.N, D, C::BQ))
+  if (!make_map_bf16_3d(&mq, Q, heads, s.N, D, C::BQ) || !make_map_bf16_3d(&mk, K, heads, s.keys(), D, BN) ||
+      !make_map_bf16_3d(&mv, V, heads, s.keys(), D, BN) || !make_map_bf16_3d(&mdo, dO, heads, s.N, D, C::BQ))
     return cudaErrorInvalidValue;
   static bool attr = [] {
     return cudaFuncSetAttribute(fa_bwd_tc_kernel<D, false, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -636,11 +663,13 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
   p.dK = static_cast<__nv_bfloat16*>(dK);
   p.dV = static_cast<__nv_bfloat16*>(dV);
   p.status = status;
-  p.N = s.N;
+  p.Nq = s.N;
+  p.Nk = s.keys();
   p.heads = (int)s.heads();
-  p.kvtiles = (s.N + BN - 1) / BN;
+  p.kvtiles = (s.keys() + BN - 1) / BN;
   p.qtiles = (s.N + C::BQ - 1) / C::BQ;
   p.causal = causal ? 1 : 0;
+  p.offset = causal ? s.keys() - s.N : 0;
   p.scale = scale;
   p.sl2 = scale * kLog2e;
   p.mask = static_cast<const __nv_bfloat16*>(mask.ptr);
@@ -654,7 +683,7 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
   p.drop_tt = drop.t * 0x01010101u;
   p.drop_scale = (float)(256.0 / (256.0 - (double)drop.t));
   const int64_t grid = (int64_t)p.kvtiles * p.heads;
-  if (s.N % 128 != 0)
+  if (s.N % 128 != 0 || s.keys() % 128 != 0)
     fa_bwd_tc_kernel<D, true, kVar><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
   else
     fa_bwd_tc_kernel<D, false, kVar><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);

@@ -50,9 +50,14 @@
 // (8 Philox calls of 16 keys, see philox.cuh) while the tile's S is being computed, stores
 // p only for kept keys (row sums l still take every p) and scales O by 256 / (256 - t).
 //
-// Causal: tile t sees K tiles 0..qtile_t; the diagonal tile masks key > query.
-// Any N: Q/K/V are read through [heads, N, d] tensor maps, so rows past the end of a head
-// arrive as zeros; keys past the end are masked and rows past the end are not stored.
+// Query and key lengths: Nq query rows against Nk key/value rows per head (Nq = Nk for
+// fa_fwd). Causal is bottom-right aligned: query i hides keys j > i + Nk - Nq ("知识点13"
+// 代码手撕 gives the square rule j > i; the offset places the queries at the end of the
+// sequence, as when a prefill continues a cached prefix), so Q tile t sees the K tiles up to
+// the limit of its last query, and only the tiles that cross that limit mask anything.
+// With Nq > Nk the first Nq - Nk queries see no key: they get O = 0 and LSE = -inf.
+// Any lengths: Q/K/V are read through [heads, rows, d] tensor maps, so rows past the end of
+// a head arrive as zeros; keys past the end are masked and rows past the end are not stored.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -105,11 +110,15 @@ struct FwdParams {
   __nv_bfloat16* O;
   float* LSE;
   int* status;
-  int N;
+  int Nq;       // query rows per head
+  int Nk;       // key / value rows per head
   int heads;
   int qtiles;
+  int kvtiles;
   int pairs;
   int causal;
+  int offset;   // causal: query i hides keys j > i + offset (offset = Nk - Nq, bottom-right)
+  int hides;    // some query may see no key at all (causal with Nq > Nk)
   float sl2;      // scale * log2(e) (* the Q and K factors for e4m3)
   float o_scale;  // V's factor for e4m3, else 1
   // additive mask (kMask): element (b, h, i, j) at mask[b*mask_sb + h*mask_sh + i*mask_srow + j]
@@ -160,10 +169,32 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   }
   const int qt0 = 2 * pair;
   const bool act1 = qt0 + 1 < p.qtiles;
-  const int nkv0 = p.causal ? qt0 + 1 : p.qtiles;
-  const int nkv1 = act1 ? (p.causal ? qt0 + 2 : p.qtiles) : 0;
+  // K/V tiles Q tile qt sees: causal, up to the limit of its last query (none when even
+  // that query sees no key, which only happens with more queries than keys)
+  auto kv_tiles_of = [&](int qt) {
+    if (!p.causal) return p.kvtiles;
+    const int lim = min((qt + 1) * BM, p.Nq) - 1 + p.offset;
+    return lim < 0 ? 0 : min(p.kvtiles, lim / BN + 1);
+  };
+  const int nkv0 = kv_tiles_of(qt0);
+  const int nkv1 = act1 ? kv_tiles_of(qt0 + 1) : 0;
   const int nkv = max(nkv0, nkv1);
-  const int row_base = head * p.N;
+  const int row_base = head * p.Nq;
+  if (nkv == 0) {
+    // No query of this CTA sees a key: O = 0 and LSE = -inf, nothing else to do.
+    if (warp < 8) {
+      const int qrow = (qt0 + (warp >> 2)) * BM + (warp & 3) * 32 + lane;
+      if ((warp >> 2) == 0 || act1) {
+        if (qrow < p.Nq) {
+          uint4* dst = reinterpret_cast<uint4*>(p.O + (size_t)(row_base + qrow) * D);
+#pragma unroll
+          for (int u = 0; u < D / 8; ++u) dst[u] = make_uint4(0, 0, 0, 0);
+          p.LSE[row_base + qrow] = -INFINITY;
+        }
+      }
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl.q_full, 1);
@@ -200,17 +231,22 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           tma_load_3d(smem + C::kQOff + (t * C::kBoxes + b) * kBoxBytes, &tmQ, &ctl.q_full, b * C::kBoxElems,
                       (qt0 + t) * BM, head);
       int last_k[4] = {-1, -1, -1, -1}, last_v[4] = {-1, -1, -1, -1};
+      // Test hook of the failure path: never arm K_0, so the MMA thread's wait for it runs
+      // out (see StatusBlock); off unless a test sets it.
+      const bool skip_k0 = injected(p.status, kInjectFwd);
       // K_j's slot frees once the S products that read K_{j-stages} have run, V_j's once
       // the PV products have: K is read a whole tile earlier than V, so it loads earlier.
       for (int j = 0; j < nkv; ++j) {
         const int sk = j % C::kKStages, sv = j % C::kVStages;
         if (j >= C::kKStages && !mbar_wait(&ctl.k_empty[sk], ((j / C::kKStages) - 1) & 1, p.status, abort))
           break;
-        mbar_expect_tx(&ctl.k_full[sk], C::kTileBytes);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(smem + C::kKOff + (sk * C::kBoxes + b) * kBoxBytes, &tmK, &ctl.k_full[sk], b * C::kBoxElems,
-                      j * BN, head);
-        last_k[sk] = j;
+        if (j > 0 || !skip_k0) {
+          mbar_expect_tx(&ctl.k_full[sk], C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(smem + C::kKOff + (sk * C::kBoxes + b) * kBoxBytes, &tmK, &ctl.k_full[sk],
+                        b * C::kBoxElems, j * BN, head);
+          last_k[sk] = j;
+        }
         if (j >= C::kVStages && !mbar_wait(&ctl.v_empty[sv], ((j / C::kVStages) - 1) & 1, p.status, abort))
           break;
         mbar_expect_tx(&ctl.v_full[sv], C::kTileBytes);
@@ -264,8 +300,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       bool ok = mbar_wait(&ctl.q_full, 0, p.status, abort) && mbar_wait(&ctl.k_full[0], 0, p.status, abort);
       if (ok) {
         tc_fence_after();
-        issue_S(0, 0);
-        mma_commit(&ctl.s_full[0]);
+        if (nkv0 > 0) {
+          issue_S(0, 0);
+          mma_commit(&ctl.s_full[0]);
+        }
         if (nkv1 > 0) {
           issue_S(1, 0);
           mma_commit(&ctl.s_full[1]);
@@ -307,7 +345,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int t = warp >> 2;
     const int nk = t ? nkv1 : nkv0;
     const int r = (warp & 3) * 32 + lane;       // row in the tile = TMEM lane
-    const int qrow = (qt0 + t) * BM + r;        // query position in the head
+    const int qrow = (qt0 + t) * BM + r;        // query row in the head
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::colS(t);
     const uint32_t tO = tmem + lane_off + C::colO(t);
@@ -320,19 +358,19 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     uint4 mreg[kMask ? BN / 8 : 1];
     const __nv_bfloat16* mrow = nullptr;
     if constexpr (kMask) {
-      if (qrow < p.N)
+      if (qrow < p.Nq)
         mrow = p.mask + (int64_t)(head / p.H) * p.mask_sb + (int64_t)(head % p.H) * p.mask_sh +
                (int64_t)qrow * p.mask_srow;
 #pragma unroll
       for (int c8 = 0; c8 < BN / 8; ++c8)
-        mreg[c8] = (mrow && 8 * c8 < p.N && nk > 0) ? ld_global_v4_ordered(mrow + 8 * c8) : make_uint4(0, 0, 0, 0);
+        mreg[c8] = (mrow && 8 * c8 < p.Nk && nk > 0) ? ld_global_v4_ordered(mrow + 8 * c8) : make_uint4(0, 0, 0, 0);
     }
     // kBits: this row's visibility bits for the K tile about to be processed (words
     // 4j .. 4j+3 of the row; rows hold at least 4 words per K tile of the head).
     uint4 breg = make_uint4(0, 0, 0, 0);
     const uint32_t* brow = nullptr;
     if constexpr (kBits) {
-      if (qrow < p.N)
+      if (qrow < p.Nq)
         brow = p.bits + (int64_t)(head / p.H) * p.mask_sb + (int64_t)(head % p.H) * p.mask_sh +
                (int64_t)qrow * p.mask_srow;
       if (brow && nk > 0) breg = ld_global_v4_ordered(brow);
@@ -387,13 +425,15 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         for (int c = 0; c < BN; ++c)
           if (!((bw[c / 32] >> (c % 32)) & 1u)) sv[c] = -INFINITY;
       }
-      // Hidden keys: key > query on the diagonal tile (causal), and keys past the end of
-      // the head in its last, partial tile (their rows were read as zeros). Without a mask
-      // every row keeps at least key 0 of the tile visible.
-      const bool diag = p.causal && j == qt0 + t;
-      const int valid = p.N - j * BN;
+      // Hidden keys: key > query + offset (causal), and keys past the end of the head in
+      // its last, partial tile (their rows were read as zeros). Keep columns c <= lim. With
+      // Nq <= Nk and no mask every row keeps at least key 0 of its first tile visible.
+      // (The test is tile-uniform: only the tiles that cross the limit of the tile's first
+      // query, or the end of the keys, compute a per-row limit.)
+      const bool diag = p.causal && j * BN + BN - 1 > (qt0 + t) * BM + p.offset;
+      const int valid = p.Nk - j * BN;
       if (diag || valid < BN) {
-        const int lim = min(diag ? r : BN - 1, valid - 1);  // keep columns c <= lim
+        const int lim = min(diag ? qrow + p.offset - j * BN : BN - 1, valid - 1);
 #pragma unroll
         for (int c = 0; c < BN; ++c)
           if (c > lim) sv[c] = -INFINITY;
@@ -435,7 +475,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const float2 sl2v = make_float2(sl2, sl2);
       // a row with no visible key so far (only possible with a mask) exponentiates
       // against 0: its scores are all -inf, so every p is 0
-      const float m_use = (kHides && m == -INFINITY) ? 0.f : m;
+      const float m_use = ((kHides || p.hides) && m == -INFINITY) ? 0.f : m;
       const float2 neg_m = make_float2(C::kPShift - m_use, C::kPShift - m_use);
       float2 rs0 = make_float2(0.f, 0.f), rs1 = make_float2(0.f, 0.f);
       if constexpr (!F8) {
@@ -484,7 +524,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int c8 = 0; c8 < BN / 8; ++c8) {
           const int col = (j + 1) * BN + 8 * c8;
-          mreg[c8] = (mrow && col < p.N && j + 1 < nk) ? ld_global_v4_ordered(mrow + col) : make_uint4(0, 0, 0, 0);
+          mreg[c8] = (mrow && col < p.Nk && j + 1 < nk) ? ld_global_v4_ordered(mrow + col) : make_uint4(0, 0, 0, 0);
         }
       }
       tmem_wait_st();
@@ -494,7 +534,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.o_full[t], 0, p.status, abort));
     if (ok) {
       tc_fence_after();
-      const float inv_l = (!kHides || l > 0.f) ? (kDrop ? p.drop_scale : p.o_scale) / l : 0.f;  // no visible key: O = 0
+      const float inv_l = (!(kHides || p.hides) || l > 0.f) ? (kDrop ? p.drop_scale : p.o_scale) / l : 0.f;  // no visible key: O = 0
       __nv_bfloat16* orow = p.O + (size_t)(row_base + qrow) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -505,12 +545,18 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(ov[2 * u] * inv_l, ov[2 * u + 1] * inv_l);
         uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-        if (qrow < p.N) {  // rows past the end of the head belong to no query
+        if (qrow < p.Nq) {  // rows past the end of the head belong to no query
 #pragma unroll
           for (int u = 0; u < 4; ++u) dst[u] = w[u];
         }
       }
-      if (qrow < p.N) p.LSE[row_base + qrow] = (m - C::kPShift + log2f(l)) * kLn2;
+      if (qrow < p.Nq) p.LSE[row_base + qrow] = (m - C::kPShift + log2f(l)) * kLn2;
+    } else if (nk == 0 && qrow < p.Nq) {
+      // this Q tile sees no key (its CTA partner does): O = 0, LSE = -inf
+      uint4* dst = reinterpret_cast<uint4*>(p.O + (size_t)(row_base + qrow) * D);
+#pragma unroll
+      for (int u = 0; u < D / 8; ++u) dst[u] = make_uint4(0, 0, 0, 0);
+      p.LSE[row_base + qrow] = -INFINITY;
     }
   }
 
@@ -544,11 +590,11 @@ cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   const int64_t heads = s.heads();
   bool maps;
   if constexpr (F8)
-    maps = make_map_u8_3d(&mq, Q, heads, s.N, D, BM) && make_map_u8_3d(&mk, K, heads, s.N, D, BN) &&
-           make_map_u8_3d(&mv, V, heads, s.N, D, BN);
+    maps = make_map_u8_3d(&mq, Q, heads, s.N, D, BM) && make_map_u8_3d(&mk, K, heads, s.keys(), D, BN) &&
+           make_map_u8_3d(&mv, V, heads, s.keys(), D, BN);
   else
-    maps = make_map_bf16_3d(&mq, Q, heads, s.N, D, BM) && make_map_bf16_3d(&mk, K, heads, s.N, D, BN) &&
-           make_map_bf16_3d(&mv, V, heads, s.N, D, BN);
+    maps = make_map_bf16_3d(&mq, Q, heads, s.N, D, BM) && make_map_bf16_3d(&mk, K, heads, s.keys(), D, BN) &&
+           make_map_bf16_3d(&mv, V, heads, s.keys(), D, BN);
   if (!maps) return cudaErrorInvalidValue;
   static bool attr = [] {
     return cudaFuncSetAttribute(fa_fwd_tc_kernel<D, F8, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -559,11 +605,15 @@ cudaError_t launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.O = static_cast<__nv_bfloat16*>(O);
   p.LSE = LSE;
   p.status = status;
-  p.N = s.N;
+  p.Nq = s.N;
+  p.Nk = s.keys();
   p.heads = (int)s.heads();
   p.qtiles = (s.N + BM - 1) / BM;
+  p.kvtiles = (s.keys() + BN - 1) / BN;
   p.pairs = (p.qtiles + 1) / 2;
   p.causal = causal ? 1 : 0;
+  p.offset = causal ? s.keys() - s.N : 0;
+  p.hides = causal && s.N > s.keys() ? 1 : 0;
   p.sl2 = sl2;
   p.o_scale = o_scale;
   p.mask = static_cast<const __nv_bfloat16*>(mask.ptr);

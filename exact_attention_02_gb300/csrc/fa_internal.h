@@ -11,12 +11,16 @@
 
 namespace fa {
 
-// Sizes of one call, validated on the host.
+// Sizes of one call, validated on the host. N is the number of query rows per head; Nk,
+// when set (> 0), the number of key/value rows, which is otherwise N as well.
 struct Shape {
   int B, H, N, d;
+  int Nk = 0;
+  int keys() const { return Nk > 0 ? Nk : N; }
   int64_t heads() const { return (int64_t)B * H; }
   int64_t rows() const { return heads() * N; }
   int64_t elems() const { return rows() * d; }
+  int64_t key_elems() const { return heads() * keys() * d; }
 };
 
 // Device status word: bounded waits that give up write FA_ERR_DEVICE_TIMEOUT here.

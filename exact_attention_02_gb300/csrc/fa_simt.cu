@@ -37,12 +37,15 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Shapes: Nq query rows and Nk key/value rows per head; causal hides key j from query i
+// when j > i + offset (offset = Nk - Nq: the queries are the last Nq positions).
+
 // Forward: grid = tiles * heads (flattened), block = kWarps warps, warp w -> query row.
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32)
 simt_fwd_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
-                T* __restrict__ O, float* __restrict__ LSE, int N, int tiles, float scale,
-                int causal) {
+                T* __restrict__ O, float* __restrict__ LSE, int Nq, int Nk, int offset, int tiles,
+                float scale, int causal) {
   __shared__ float ks[kChunk][D + 1];
   __shared__ float vs[kChunk][D];
   __shared__ float qs[kWarps][D];
@@ -50,8 +53,8 @@ simt_fwd_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __res
   const int64_t head = blockIdx.x / tiles;
   const int row0 = (blockIdx.x % tiles) * kWarps;
   const int row = row0 + warp;
-  const bool active = row < N;
-  const size_t base = (size_t)head * N * D;
+  const bool active = row < Nq;
+  const size_t base = (size_t)head * Nq * D, kbase = (size_t)head * Nk * D;
   const float sl2 = scale * kLog2e;
   for (int c = lane; c < D; c += 32)
     qs[warp][c] = active ? ldf(Q + base + (size_t)row * D + c) * sl2 : 0.f;
@@ -60,15 +63,15 @@ simt_fwd_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __res
 #pragma unroll
   for (int t = 0; t < D / 32; ++t) acc[t] = 0.f;
 
-  const int kv_end = causal ? min(N, row0 + kWarps) : N;
+  const int kv_end = causal ? min(Nk, row0 + kWarps + offset) : Nk;
   for (int j0 = 0; j0 < kv_end; j0 += kChunk) {
     __syncthreads();
     for (int e = threadIdx.x; e < kChunk * D; e += blockDim.x) {
       const int r = e / D, c = e % D, j = j0 + r;
       float kv = 0.f, vv = 0.f;
-      if (j < N) {
-        kv = ldf(K + base + (size_t)j * D + c);
-        vv = ldf(V + base + (size_t)j * D + c);
+      if (j < Nk) {
+        kv = ldf(K + kbase + (size_t)j * D + c);
+        vv = ldf(V + kbase + (size_t)j * D + c);
       }
       ks[r][c] = kv;
       vs[r][c] = vv;
@@ -78,7 +81,7 @@ simt_fwd_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __res
     float s = 0.f;
 #pragma unroll 16
     for (int c = 0; c < D; ++c) s = fmaf(qs[warp][c], ks[lane][c], s);
-    const bool vis = active && j < N && (!causal || j <= row);
+    const bool vis = active && j < Nk && (!causal || j <= row + offset);
     s = vis ? s : -INFINITY;
     const float mnew = fmaxf(m, warp_max(s));
     if (mnew == -INFINITY) continue;  // nothing visible yet in this row (warp-uniform)
@@ -96,10 +99,10 @@ simt_fwd_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __res
     m = mnew;
   }
   if (active) {
-    const float inv = 1.f / l;
+    const float inv = l > 0.f ? 1.f / l : 0.f;  // a query that sees no key: O = 0, LSE = -inf
 #pragma unroll
     for (int t = 0; t < D / 32; ++t) stf(O + base + (size_t)row * D + lane + 32 * t, acc[t] * inv);
-    if (lane == 0) LSE[head * N + row] = (m + log2f(l)) * kLn2;
+    if (lane == 0) LSE[head * Nq + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
   }
 }
 
@@ -108,8 +111,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32)
 simt_bwd_dkdv_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                      const T* __restrict__ dO, const float* __restrict__ LSE,
-                     const float* __restrict__ Dr, T* __restrict__ dK, T* __restrict__ dV, int N,
-                     int tiles, float scale, int causal) {
+                     const float* __restrict__ Dr, T* __restrict__ dK, T* __restrict__ dV, int Nq,
+                     int Nk, int offset, int tiles, float scale, int causal) {
   __shared__ float qs[kChunk][D + 1];
   __shared__ float dos[kChunk][D + 1];
   __shared__ float kr[kWarps][D];
@@ -119,24 +122,24 @@ simt_bwd_dkdv_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* 
   const int64_t head = blockIdx.x / tiles;
   const int key0 = (blockIdx.x % tiles) * kWarps;
   const int key = key0 + warp;
-  const bool active = key < N;
-  const size_t base = (size_t)head * N * D;
+  const bool active = key < Nk;
+  const size_t base = (size_t)head * Nq * D, kbase = (size_t)head * Nk * D;
   const float sl2 = scale * kLog2e;
   for (int c = lane; c < D; c += 32) {
-    kr[warp][c] = active ? ldf(K + base + (size_t)key * D + c) * sl2 : 0.f;
-    vr[warp][c] = active ? ldf(V + base + (size_t)key * D + c) : 0.f;
+    kr[warp][c] = active ? ldf(K + kbase + (size_t)key * D + c) * sl2 : 0.f;
+    vr[warp][c] = active ? ldf(V + kbase + (size_t)key * D + c) : 0.f;
   }
   float dk[D / 32], dv[D / 32];
 #pragma unroll
   for (int t = 0; t < D / 32; ++t) dk[t] = dv[t] = 0.f;
 
-  const int i_start = causal ? (key0 / kChunk) * kChunk : 0;
-  for (int i0 = i_start; i0 < N; i0 += kChunk) {
+  const int i_start = causal ? (max(0, key0 - offset) / kChunk) * kChunk : 0;
+  for (int i0 = i_start; i0 < Nq; i0 += kChunk) {
     __syncthreads();
     for (int e = threadIdx.x; e < kChunk * D; e += blockDim.x) {
       const int r = e / D, c = e % D, i = i0 + r;
       float qv = 0.f, dov = 0.f;
-      if (i < N) {
+      if (i < Nq) {
         qv = ldf(Q + base + (size_t)i * D + c);
         dov = ldf(dO + base + (size_t)i * D + c);
       }
@@ -145,8 +148,8 @@ simt_bwd_dkdv_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* 
     }
     if (threadIdx.x < kChunk) {
       const int i = i0 + threadIdx.x;
-      lse2[threadIdx.x] = i < N ? LSE[head * N + i] * kLog2e : 0.f;
-      dd[threadIdx.x] = i < N ? Dr[head * N + i] : 0.f;
+      lse2[threadIdx.x] = i < Nq ? LSE[head * Nq + i] * kLog2e : 0.f;
+      dd[threadIdx.x] = i < Nq ? Dr[head * Nq + i] : 0.f;
     }
     __syncthreads();
     const int i = i0 + lane;
@@ -156,7 +159,7 @@ simt_bwd_dkdv_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* 
       s = fmaf(qs[lane][c], kr[warp][c], s);
       dp = fmaf(dos[lane][c], vr[warp][c], dp);
     }
-    const bool vis = active && i < N && (!causal || key <= i);
+    const bool vis = active && i < Nq && (!causal || key <= i + offset);
     const float p = vis ? exp2f(s - lse2[lane]) : 0.f;
     const float ds = p * (dp - dd[lane]);
 #pragma unroll 8
@@ -173,8 +176,8 @@ simt_bwd_dkdv_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* 
   if (active) {
 #pragma unroll
     for (int t = 0; t < D / 32; ++t) {
-      stf(dV + base + (size_t)key * D + lane + 32 * t, dv[t]);
-      stf(dK + base + (size_t)key * D + lane + 32 * t, dk[t] * scale);
+      stf(dV + kbase + (size_t)key * D + lane + 32 * t, dv[t]);
+      stf(dK + kbase + (size_t)key * D + lane + 32 * t, dk[t] * scale);
     }
   }
 }
@@ -184,8 +187,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32)
 simt_bwd_dq_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                    const T* __restrict__ dO, const float* __restrict__ LSE,
-                   const float* __restrict__ Dr, T* __restrict__ dQ, int N, int tiles, float scale,
-                   int causal) {
+                   const float* __restrict__ Dr, T* __restrict__ dQ, int Nq, int Nk, int offset,
+                   int tiles, float scale, int causal) {
   __shared__ float ks[kChunk][D + 1];
   __shared__ float vs[kChunk][D + 1];
   __shared__ float qr[kWarps][D];
@@ -194,28 +197,28 @@ simt_bwd_dq_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __
   const int64_t head = blockIdx.x / tiles;
   const int row0 = (blockIdx.x % tiles) * kWarps;
   const int row = row0 + warp;
-  const bool active = row < N;
-  const size_t base = (size_t)head * N * D;
+  const bool active = row < Nq;
+  const size_t base = (size_t)head * Nq * D, kbase = (size_t)head * Nk * D;
   const float sl2 = scale * kLog2e;
   for (int c = lane; c < D; c += 32) {
     qr[warp][c] = active ? ldf(Q + base + (size_t)row * D + c) * sl2 : 0.f;
     dor[warp][c] = active ? ldf(dO + base + (size_t)row * D + c) : 0.f;
   }
-  const float lse2 = active ? LSE[head * N + row] * kLog2e : 0.f;
-  const float drow = active ? Dr[head * N + row] : 0.f;
+  const float lse2 = active ? LSE[head * Nq + row] * kLog2e : 0.f;
+  const float drow = active ? Dr[head * Nq + row] : 0.f;
   float dq[D / 32];
 #pragma unroll
   for (int t = 0; t < D / 32; ++t) dq[t] = 0.f;
 
-  const int kv_end = causal ? min(N, row0 + kWarps) : N;
+  const int kv_end = causal ? min(Nk, row0 + kWarps + offset) : Nk;
   for (int j0 = 0; j0 < kv_end; j0 += kChunk) {
     __syncthreads();
     for (int e = threadIdx.x; e < kChunk * D; e += blockDim.x) {
       const int r = e / D, c = e % D, j = j0 + r;
       float kv = 0.f, vv = 0.f;
-      if (j < N) {
-        kv = ldf(K + base + (size_t)j * D + c);
-        vv = ldf(V + base + (size_t)j * D + c);
+      if (j < Nk) {
+        kv = ldf(K + kbase + (size_t)j * D + c);
+        vv = ldf(V + kbase + (size_t)j * D + c);
       }
       ks[r][c] = kv;
       vs[r][c] = vv;
@@ -228,7 +231,7 @@ simt_bwd_dq_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __
       s = fmaf(qr[warp][c], ks[lane][c], s);
       dp = fmaf(dor[warp][c], vs[lane][c], dp);
     }
-    const bool vis = active && j < N && (!causal || j <= row);
+    const bool vis = active && j < Nk && (!causal || j <= row + offset);
     const float p = vis ? exp2f(s - lse2) : 0.f;
     const float ds = p * (dp - drow);
 #pragma unroll 8
@@ -303,8 +306,9 @@ cudaError_t launch_fwd(const void* Q, const void* K, const void* V, void* O, flo
                        const Shape& s, float scale, bool causal, cudaStream_t st) {
   const int tiles = (s.N + kWarps - 1) / kWarps;
   const int64_t grid = (int64_t)tiles * s.heads();
+  const int offset = causal ? s.keys() - s.N : 0;
   simt_fwd_kernel<T, D><<<(unsigned)grid, kWarps * 32, 0, st>>>(
-      (const T*)Q, (const T*)K, (const T*)V, (T*)O, LSE, s.N, tiles, scale, causal ? 1 : 0);
+      (const T*)Q, (const T*)K, (const T*)V, (T*)O, LSE, s.N, s.keys(), offset, tiles, scale, causal ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -312,15 +316,15 @@ template <typename T, int D>
 cudaError_t launch_bwd(const void* Q, const void* K, const void* V, const void* dO,
                        const float* LSE, const float* Dr, void* dQ, void* dK, void* dV,
                        const Shape& s, float scale, bool causal, cudaStream_t st) {
-  const int tiles = (s.N + kWarps - 1) / kWarps;
-  const int64_t grid = (int64_t)tiles * s.heads();
-  simt_bwd_dkdv_kernel<T, D><<<(unsigned)grid, kWarps * 32, 0, st>>>(
-      (const T*)Q, (const T*)K, (const T*)V, (const T*)dO, LSE, Dr, (T*)dK, (T*)dV, s.N, tiles,
-      scale, causal ? 1 : 0);
+  const int qtiles = (s.N + kWarps - 1) / kWarps, ktiles = (s.keys() + kWarps - 1) / kWarps;
+  const int offset = causal ? s.keys() - s.N : 0;
+  simt_bwd_dkdv_kernel<T, D><<<(unsigned)((int64_t)ktiles * s.heads()), kWarps * 32, 0, st>>>(
+      (const T*)Q, (const T*)K, (const T*)V, (const T*)dO, LSE, Dr, (T*)dK, (T*)dV, s.N, s.keys(), offset,
+      ktiles, scale, causal ? 1 : 0);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  simt_bwd_dq_kernel<T, D><<<(unsigned)grid, kWarps * 32, 0, st>>>(
-      (const T*)Q, (const T*)K, (const T*)V, (const T*)dO, LSE, Dr, (T*)dQ, s.N, tiles, scale,
+  simt_bwd_dq_kernel<T, D><<<(unsigned)((int64_t)qtiles * s.heads()), kWarps * 32, 0, st>>>(
+      (const T*)Q, (const T*)K, (const T*)V, (const T*)dO, LSE, Dr, (T*)dQ, s.N, s.keys(), offset, qtiles, scale,
       causal ? 1 : 0);
   return cudaGetLastError();
 }

@@ -23,6 +23,33 @@ namespace ptx {
 constexpr int kErrTimeout = 4;                        // FA_ERR_DEVICE_TIMEOUT
 constexpr uint64_t kWaitLimitNs = 4000000000ull;     // 4 s: far beyond any legal stall
 
+// The per-device block that every kernel's `status` pointer addresses (status is its first
+// member). The two other members exist for the tests of the failure path only: `inject`
+// names a kernel whose first CTA skips one producer arrival (0: none; kInjectFwd,
+// kInjectBwd), and `limit_ns` replaces kWaitLimitNs when non-zero. Both are 0 unless a
+// test sets them through fa_test_inject_timeout().
+struct StatusBlock {
+  int status;                   // 0, or FA_ERR_DEVICE_TIMEOUT once a bounded wait gave up
+  int inject;
+  unsigned long long limit_ns;
+};
+constexpr int kInjectFwd = 1;  // fa_fwd_tc_kernel: CTA 0 never arms its first K stage
+constexpr int kInjectBwd = 2;  // fa_bwd_tc_kernel: CTA 0 never arms its first Q/dO stage
+
+// The wait limit in force: the test override if one is set, else kWaitLimitNs.
+__device__ __forceinline__ uint64_t wait_limit(const int* status) {
+  if (!status) return kWaitLimitNs;
+  const unsigned long long v =
+      *reinterpret_cast<const volatile unsigned long long*>(&reinterpret_cast<const StatusBlock*>(status)->limit_ns);
+  return v ? v : kWaitLimitNs;
+}
+
+// True in the first CTA of a kernel that the failure-path test hook names.
+__device__ __forceinline__ bool injected(const int* status, int which) {
+  return status && blockIdx.x == 0 &&
+         *reinterpret_cast<const volatile int*>(&reinterpret_cast<const StatusBlock*>(status)->inject) == which;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -74,22 +101,23 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
-// Waits until the phase with parity `parity` of `bar` has completed. Gives up after
-// kWaitLimitNs, or soon after *abort is set by another role of the CTA; on giving up it
-// records FA_ERR_DEVICE_TIMEOUT in *status, sets *abort and returns false. A null
-// `abort` means: ignore other roles and wait (still bounded), as the drain paths need.
-// Each poll may sleep up to kSuspendNs; the global timer and the abort flag are checked
-// every 8 polls, so the limit holds within a millisecond.
+// Waits until the phase with parity `parity` of `bar` has completed. Gives up after the
+// wait limit (kWaitLimitNs unless a test set a shorter one), or soon after *abort is set by
+// another role of the CTA; on giving up it records FA_ERR_DEVICE_TIMEOUT in *status, sets
+// *abort and returns false. A null `abort` means: ignore other roles and wait (still
+// bounded), as the drain paths need. Each poll may sleep up to kSuspendNs; the global timer
+// and the abort flag are checked every 8 polls, so the limit holds within a millisecond.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const uint64_t limit = wait_limit(status);
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 8; ++i)
       if (mbar_try_wait_sleep(bar, parity)) return true;
     if (abort && *abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit) {
       if (status) atomicExch(status, kErrTimeout);
       if (abort) *abort = 1;
       return false;

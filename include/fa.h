@@ -104,6 +104,35 @@ FA_API fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const voi
                    void* stream);
 
 /*
+ * fa_fwd_rect / fa_bwd_rect — fa_fwd / fa_bwd with Nq query rows against Nk key/value rows
+ * per head (cross-attention, or a prefill of Nq new tokens that continues a cached prefix
+ * of Nk - Nq tokens: "flash-attention-v2-sram-tiling" 场景二 serves long documents against
+ * a key/value cache; "知识点13 FlashAttention深度攻略" 代码手撕 tiles the query and key ranges
+ * separately, with min() tails). fa_fwd and fa_bwd are the case Nq = Nk.
+ * causal: the queries are the last Nq positions of the sequence (bottom-right alignment):
+ *      query i hides keys j > i + Nk - Nq. With Nq = Nk this is the rule of fa_fwd. With
+ *      Nq > Nk the first Nq - Nk queries see no key: they get O = 0 and LSE = -inf, their
+ *      dQ rows are 0 and they add nothing to dK or dV.
+ * In:  Q, dO [B,H,Nq,d]; K, V [B,H,Nk,d] (dtype); LSE, D [B,H,Nq] float32 (D from
+ *      fa_bwd_preprocess on O, dO with N = Nq, or NULL as for fa_bwd).
+ * Out: O, dQ [B,H,Nq,d]; dK, dV [B,H,Nk,d] (dtype); LSE [B,H,Nq] float32.
+ * Shapes: Nq, Nk >= 1; the limits of fa_fwd apply to the longer of the two (bf16:
+ *      B*H*max(Nq, Nk) < 2^31; fp32: max(Nq, Nk) <= 4096).
+ * workspace: at least fa_bwd_rect_workspace_size(...) bytes (the float32 dQ accumulator,
+ *      4*B*H*Nq*d bytes for bf16), plus 4*B*H*Nq bytes when D is NULL. The remaining
+ *      arguments and errors are those of fa_fwd and fa_bwd.
+ */
+FA_API fa_status_t fa_fwd_rect(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                               int B, int H, int Nq, int Nk, int d, float scale, int causal, int dtype,
+                               void* stream);
+FA_API size_t fa_bwd_rect_workspace_size(int B, int H, int Nq, int Nk, int d, int dtype);
+FA_API fa_status_t fa_bwd_rect(const void* Q, const void* K, const void* V, const void* O,
+                               const void* dO, const float* LSE, const float* D,
+                               void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes,
+                               int B, int H, int Nq, int Nk, int d, float scale, int causal, int dtype,
+                               void* stream);
+
+/*
  * fa_bwd_noalloc — fa_bwd for callers that must not allocate device memory.
  * The pages have no counterpart: this is a packaging of fa_bwd, not a step of the method.
  * Some callers cannot call cudaMalloc: code hosted by a framework that owns all device
@@ -288,6 +317,24 @@ FA_API const char* fa_get_error_string(fa_status_t status);
  * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, or FA_ERR_CUDA if the read itself failed.
  */
 FA_API fa_status_t fa_get_last_device_status(void);
+
+/*
+ * fa_test_inject_timeout — for tests of the failure path only; not part of the method (the
+ * pages have no counterpart). Every device-side wait of the tensor-core kernels is bounded
+ * (4 s by default); when a wait gives up, the kernel records FA_ERR_DEVICE_TIMEOUT in the
+ * device status word, stops its other roles, waits (bounded) for its own copies and
+ * products in flight, releases its tensor memory and returns. This call lets a test
+ * exercise that path on the current device without faulting or hanging the GPU:
+ *   which = 1: in the next fa_fwd (bf16) launches, the first CTA never arms its first K
+ *              tile, so the MMA thread's wait for it runs out;
+ *   which = 2: the same for the first Q/dO tile of fa_bwd (bf16);
+ *   which = 0: off (the normal state).
+ * wait_limit_ns: the wait limit in force while set (0 restores the default of 4 s).
+ * The call synchronises with the device (it writes device memory with cudaMemcpy). Results
+ * of calls made while an injection is on are undefined; turn it off before any other use.
+ * Returns FA_ERR_INVALID_ARG for another `which`, FA_ERR_CUDA if the write fails.
+ */
+FA_API fa_status_t fa_test_inject_timeout(int which, unsigned long long wait_limit_ns);
 
 #ifdef __cplusplus
 }

@@ -33,9 +33,11 @@ Readings where the pages leave a choice open:
     D_i = dO_i . O_i of the dropped O. The keep matrix comes from oracle/philox.py.
   * Causal attention hides key j from query i iff j > i (queries and keys share
     the same positions; the diagonal is always visible, so no row is empty). With
-    fewer queries than keys (N_q < N_k, e.g. decoding against a cache) the queries are
+    N_q != N_k (a decode or a prefill against a cache; cross-attention) the queries are
     the last N_q positions: query row i sits at position i + N_k - N_q and hides keys
-    j > i + N_k - N_q (bottom-right alignment; the pages only show N_q = N_k).
+    j > i + N_k - N_q (bottom-right alignment; the pages only show N_q = N_k). With
+    N_q > N_k the first N_q - N_k queries see no key: their rows are wholly hidden and
+    take the rule above (O = 0, LSE = -inf, no gradient).
 
 Evaluation order: every quantity is computed from its definition, a whole row of
 scores at a time. To bound memory the rows of a head are taken in groups; rows
@@ -137,8 +139,8 @@ def head_backward(q, k, v, do, scale, causal, return_ds=False, mask=None, keep=N
     dQ = np.empty_like(q)
     dK = np.zeros_like(k)
     dV = np.zeros_like(v)
-    dS_all = np.empty((N, N)) if return_ds else None
-    g = _group_rows(N)
+    dS_all = np.empty((N, k.shape[0])) if return_ds else None
+    g = _group_rows(k.shape[0])  # each row of scores holds one value per key
     for a in range(0, N, g):
         r = np.arange(a, min(N, a + g))
         P, _, _ = softmax_rows(scores(q, k, scale, causal, r, mask))

@@ -253,3 +253,37 @@ def test_dropout_rejects_before_launch(lib):
     assert call(p=float("nan")) == fa.FA_ERR_INVALID_ARG
     assert call(dtype=1) == fa.FA_ERR_UNSUPPORTED
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+
+
+def _fwd_rect(lib, ptrs=(P, P, P, P, P), Nq=128, Nk=256, **kw):
+    a = dict(GOOD, **kw)
+    return lib.fa_fwd_rect(*[ctypes.c_void_p(p) for p in ptrs], a["B"], a["H"], Nq, Nk, a["d"],
+                           ctypes.c_float(a["scale"]), a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Nq=0), 1), (dict(Nk=0), 1), (dict(Nk=-5), 1), (dict(d=96), 2),
+    (dict(dtype=1, Nk=5000), 2), (dict(dtype=1, Nq=5000), 2), (dict(causal=3), 1),
+    (dict(scale=0.0), 1), (dict(B=1 << 16, H=1 << 15), 1),
+    # bf16 rows: the longer length counts against the 32-bit row limit
+    (dict(B=1 << 10, H=1 << 10, Nq=1, Nk=1 << 12), 2),
+])
+def test_fwd_rect_rejects(lib, kw, code):
+    assert _fwd_rect(lib, **kw) == code
+
+
+@pytest.mark.parametrize("ptrs", [(0, P, P, P, P), (P, P, P, P, 0), (P + 8, P, P, P, P)])
+def test_fwd_rect_rejects_pointers(lib, ptrs):
+    assert _fwd_rect(lib, ptrs=ptrs) == 1
+
+
+def test_bwd_rect_workspace_and_rejects(lib):
+    assert lib.fa_bwd_rect_workspace_size(2, 4, 1000, 8192, 128, 0) == 2 * 4 * 1000 * 128 * 4  # dQ rows only
+    assert lib.fa_bwd_rect_workspace_size(1, 1, 100, 300, 64, 1) == 0  # fp32: none
+    assert lib.fa_bwd_rect_workspace_size(1, 1, 100, 0, 64, 0) == 0  # rejected
+    v = [ctypes.c_void_p(P)] * 10
+    ws = ctypes.c_void_p(P)
+    need = lib.fa_bwd_rect_workspace_size(1, 1, 128, 256, 64, 0)
+    # too small a workspace, and a zero key length
+    assert lib.fa_bwd_rect(*v, ws, need - 16, 1, 1, 128, 256, 64, ctypes.c_float(0.125), 0, 0, None) == 5
+    assert lib.fa_bwd_rect(*v, ws, need, 1, 1, 128, 0, 64, ctypes.c_float(0.125), 0, 0, None) == 1

@@ -346,6 +346,52 @@ def pin_fewer_queries_than_keys(m):
     assert np.allclose(O[0], (p0 / p0.sum()) @ v[:vis], rtol=0, atol=1e-14)
 
 
+def pin_more_queries_than_keys(m):
+    """N_q > N_k, causal, bottom-right: query i sits at position i - (N_q - N_k), so the first
+    N_q - N_k queries see no key (no softmax: O = 0, LSE = -inf, dQ = 0, no share of dK or
+    dV), and the last N_k queries are exactly the square causal problem on those queries."""
+    Nq, Nk, d = 9, 4, 3
+    q, do = (_rand((Nq, d), 520 + s) for s in range(2))
+    k, v = (_rand((Nk, d), 530 + s) for s in range(2))
+    r = m.head_backward(q, k, v, do, 0.7, True)
+    hid = Nq - Nk
+    assert np.array_equal(r["o"][:hid], np.zeros((hid, d))) and np.all(r["lse"][:hid] == -np.inf)
+    assert np.array_equal(r["dq"][:hid], np.zeros((hid, d)))
+    sq = m.head_backward(q[hid:], k, v, do[hid:], 0.7, True)
+    for n in ("o", "lse", "dq"):
+        assert np.allclose(r[n][hid:], sq[n], rtol=0, atol=1e-14), n
+    for n in ("dk", "dv"):
+        assert np.allclose(r[n], sq[n], rtol=0, atol=1e-14), n
+    # non-causal: every query sees every key; brute force on each row
+    On, Ln = m.head_forward(q, k, v, 0.7, False)
+    for i in range(Nq):
+        s = [0.7 * sum(q[i, c] * k[j, c] for c in range(d)) for j in range(Nk)]
+        mx = max(s)
+        w = [np.exp(x - mx) for x in s]
+        tot = sum(w)
+        assert abs(Ln[i] - (mx + np.log(tot))) < 1e-13
+        for c in range(d):
+            assert abs(On[i, c] - sum(w[j] * v[j, c] for j in range(Nk)) / tot) < 1e-13
+
+
+def pin_rectangular_torch_autograd(m):
+    """N_q != N_k: outputs and gradients equal PyTorch's CPU float64 attention with
+    autograd; causal through an explicit bottom-right mask (N_q <= N_k, so no row is empty)."""
+    torch = pytest.importorskip("torch")
+    for Nq, Nk, causal in ((5, 11, False), (5, 11, True), (12, 7, False), (1, 6, True)):
+        arrs = [_rand((Nq, 4), 540 + Nq), _rand((Nk, 4), 541 + Nk), _rand((Nk, 4), 542 + Nk), _rand((Nq, 4), 543)]
+        t = [torch.tensor(a, dtype=torch.float64, requires_grad=(i < 3)) for i, a in enumerate(arrs)]
+        mask = None
+        if causal:
+            mask = torch.arange(Nk)[None, :] <= torch.arange(Nq)[:, None] + (Nk - Nq)
+        o = torch.nn.functional.scaled_dot_product_attention(t[0], t[1], t[2], attn_mask=mask, scale=0.4)
+        (o * t[3]).sum().backward()
+        r = m.head_backward(*arrs, 0.4, causal)
+        assert np.allclose(r["o"], o.detach().numpy(), rtol=0, atol=1e-12), (Nq, Nk, causal)
+        for name, ten in zip(("dq", "dk", "dv"), t[:3]):
+            assert np.allclose(r[name], ten.grad.numpy(), rtol=0, atol=1e-12), (Nq, Nk, causal, name)
+
+
 # -- the additive mask ("知识点13" section 7: the mask fused into the softmax step) ---------
 def _mask(N, seed, p_hide=0.2):
     """A random finite mask with about p_hide of its entries -inf; the diagonal stays
@@ -586,6 +632,7 @@ MUTATIONS = [
     ("mask hides diagonal", "j[None, :] > rows[:, None]", "j[None, :] >= rows[:, None]"),
     ("mask keeps the future", "j[None, :] > rows[:, None]", "j[None, :] < rows[:, None]"),
     ("top-left alignment for fewer queries", "offset = k.shape[0] - q.shape[0]", "offset = 0"),
+    ("offset with the wrong sign", "offset = k.shape[0] - q.shape[0]", "offset = q.shape[0] - k.shape[0]"),
     ("max not subtracted from LSE", "LSE[a:a + g] = m + np.log(l)", "LSE[a:a + g] = np.log(l)"),
     ("log2 in LSE", "LSE[a:a + g] = m + np.log(l)", "LSE[a:a + g] = m + np.log2(l)"),
     ("D from dO.dO", 'np.einsum("ic,ic->i", np.asarray(do, np.float64), np.asarray(o, np.float64))',
@@ -619,6 +666,6 @@ def test_planted_mistakes_are_caught(mut):
         try:
             with np.errstate(all="ignore"):
                 pin(mod)
-        except (AssertionError, FloatingPointError, ValueError):
+        except (AssertionError, FloatingPointError, ValueError, IndexError):  # a crash on a shape counts
             failed.append(pin.__name__)
     assert failed, f"no pin caught: {mut[0]}"
