@@ -636,11 +636,12 @@ struct DropArg {
   uint32_t t = 0;
 };
 
+// The 64-query-tile kernel: d = 64, and every call with a mask or dropout.
 template <int D, int kVar>
-cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
-                   const float* Dv, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
-                   float scale, bool causal, const MaskArg& mask, const DropArg& drop, int* status,
-                   cudaStream_t st) {
+cudaError_t launch_narrow(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                          const float* Dv, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
+                          float scale, bool causal, const MaskArg& mask, const DropArg& drop, int* status,
+                          cudaStream_t st) {
   using C = BwdCfg<D>;
   CUtensorMap mq, mk, mv, mdo;
   const int64_t heads = s.heads();
@@ -692,6 +693,24 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
   dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(dQacc, static_cast<__nv_bfloat16*>(dQ),
                                                                   n8, scale);
   return cudaGetLastError();
+}
+
+template <int D, int kVar>
+cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                   const float* Dv, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
+                   float scale, bool causal, const MaskArg& mask, const DropArg& drop, int* status,
+                   cudaStream_t st) {
+  if constexpr (D == 128 && kVar == 0) {
+    // d = 128 without a mask or dropout: the 128-query-tile kernel (fa_bwd_wide.cu)
+    cudaError_t e = cudaMemsetAsync(dQacc, 0, (size_t)s.elems() * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    if ((e = tc_bwd_wide(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, status, st)) != cudaSuccess) return e;
+    const int64_t n8 = s.elems() / 8;
+    dq_convert_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(dQacc, static_cast<__nv_bfloat16*>(dQ), n8, scale);
+    return cudaGetLastError();
+  } else {
+    return launch_narrow<D, kVar>(Q, K, V, dO, LSE, Dv, dQ, dK, dV, dQacc, s, scale, causal, mask, drop, status, st);
+  }
 }
 
 }  // namespace

@@ -1,0 +1,550 @@
+// Attention backward for head dimension 128 on 128-query tiles (bf16 in, fp32 accumulate);
+// what it computes is fa_bwd in include/fa.h, for the calls without a mask or dropout.
+//
+// Method ("flash-attention-backpropagation", 反向总览 / Softmax梯度 / QKV梯度; the single
+// recompute per tile of "FlashAttention 反向传播" 踩坑二): one CTA owns a 128-key tile of
+// one head and loops over the 128-row query tiles that see it; P is rebuilt from the
+// forward's LSE, and each recompute of a tile feeds dV, dK and dQ.
+//
+// Keys sit on the 128 TMEM lanes, so dV and dK accumulate in TMEM:
+//   S^T  = K_j Q_i^T                 [keys x queries]  tcgen05, A, B from smem (K-major)
+//   dP^T = V_j dO_i^T                [keys x queries]  tcgen05
+//   P^T  = exp2(S^T * scale*log2e - LSE_i*log2e)       softmax warps, phase A
+//   dS^T = P^T * (dP^T - D_i)                          softmax warps, phase B
+//   dV_j += P^T dO_i                 A = P^T from TMEM (bf16, packed over S^T)
+//   dK_j += dS^T Q_i                 A = dS^T from smem (K-major)
+//   dQ_i^T = K_j^T dS^T              [head dim x queries]  A = K_j (MN-major), B = dS^T (MN-major)
+// and every dQ partial is added into an fp32 accumulator in global memory (red.add); a
+// last pass scales it by `scale` and rounds it to bf16 (fa_bwd_tc.cu).
+//
+// Every product is M = 128, N = 128: a tcgen05.mma of that shape runs at the full math
+// rate, while the N = 64 products of 64-query tiles are bound by shared-memory operand
+// reads. The price is TMEM room: dV | dK | S^T | dP^T fill the 512 columns, so there is one
+// S^T and one dP^T buffer. The softmax is therefore split in two phases, so that the
+// tensor core always has a product that does not wait for it:
+//   phase A (needs S^T):  P^T, written over S^T in TMEM (dV reads it from there);
+//   phase B (needs dP^T): dS^T, written to shared memory only (dK and dQ read it there),
+//                         which frees the dP^T columns for the dQ^T partial.
+// Issue order for tile i (all products of a tile after its own inputs, in this order):
+//   S(i+1) | dK(i) dQ(i) | dV(i+1) | dP(i+1)
+// so phase A of tile i+1 runs beside dK(i) and dQ(i), the softmax warps read the dQ(i)
+// partial out of the dP^T columns beside dV(i+1), and phase B of tile i+1 runs beside S(i+2).
+//
+// CTA = 10 warps: 0-7 softmax (two warpgroups over query columns 0-63 and 64-127; a thread
+// owns one key row = TMEM lane), which also read the dQ^T partials out of TMEM (between
+// phases A and B, when they would otherwise wait) and write dK and dV at the end; 8 TMA
+// producer; 9 MMA issuer. Shared memory: K, V (32 KB each), two Q/dO stages (64 KB each),
+// dS^T (32 KB) and LSE/D per stage.
+//
+// Query and key lengths as in fa_bwd_tc.cu: Nq query rows against Nk key rows per head,
+// causal bottom-right aligned (query i hides keys j > i + Nk - Nq); rows past the end of a
+// head arrive as zeros from the tensor maps, queries past the end get LSE = +inf (P = 0),
+// and rows past the end are neither accumulated nor stored.
+#include <cuda_bf16.h>
+
+#include "fa_internal.h"
+#include "sm100_ptx.cuh"
+#include "tma_host.h"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+constexpr int D = 128;   // head dimension
+constexpr int BN = 128;  // keys per CTA
+constexpr int BQ = 128;  // queries per tile
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kStages = 2;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Shared memory (1024-byte aligned base; control block last).
+constexpr int kBox = 128 * 128;       // one [128 rows x 64 columns] bf16 box, 128-byte swizzle
+constexpr int kTile = 2 * kBox;       // a [128 rows x 128 columns] tile: two boxes of 64 columns
+constexpr int kKOff = 0;
+constexpr int kVOff = kKOff + kTile;
+constexpr int kStageOff = kVOff + kTile;  // stage s: Q_i at + s * 2 * kTile, dO_i right after it
+constexpr int kDsOff = kStageOff + kStages * 2 * kTile;
+constexpr int kVecOff = kDsOff + kTile;   // LSE_i then D_i of each stage
+constexpr int kVecBytes = 2 * BQ * 4;
+constexpr int kCtlOff = kVecOff + kStages * kVecBytes;
+
+struct WideCtl {
+  uint64_t kv_full, q_full[kStages], do_full[kStages], q_empty[kStages], do_empty[kStages];
+  uint64_t s_full, dp_full, p_done, ds_done, dq_full, dq_empty, kv_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr int kSmemBytes = kCtlOff + (int)sizeof(WideCtl);
+static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
+
+// TMEM columns.
+constexpr uint32_t kColDV = 0;
+constexpr uint32_t kColDK = 128;
+constexpr uint32_t kColS = 256;   // S^T, then P^T (bf16 pairs) in its first half of each 64
+constexpr uint32_t kColDP = 384;  // dP^T, then the dQ^T partial
+constexpr uint32_t kTmemCols = 512;
+
+struct WideParams {
+  const float* LSE;
+  const float* Dvec;
+  float* dQacc;
+  __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+  int* status;
+  int Nq, Nk;
+  int heads;
+  int kvtiles;
+  int qtiles;
+  int causal;
+  int offset;  // causal: query i hides keys j > i + offset
+  float scale;
+  float sl2;   // scale * log2(e)
+};
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// TMEM column of the packed bf16 P^T for query block k (16 queries): each softmax
+// warpgroup packs its 64 queries into the first 32 columns of its 64-column half.
+__device__ __forceinline__ uint32_t packed_col(uint32_t base, int k) { return base + (k / 4) * 64 + (k % 4) * 8; }
+
+// 10 warps put at most 3 warps on each of the SM's four sub-partitions (16 K registers each),
+// which allows 168 registers per thread: a softmax thread holds its 64 weights from phase A
+// to phase B and, between the two, a 64-column row of the dQ partial.
+template <bool kTail>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                   const WideParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The swizzled operand layout needs a 1024-byte aligned base; the runtime provides it for
+  // this declaration, and the kernel refuses to run (status word) if it did not.
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0 && p.status) atomicExch(p.status, 3 /* FA_ERR_CUDA */);
+    return;
+  }
+  WideCtl& ctl = *reinterpret_cast<WideCtl*>(smem + kCtlOff);
+
+  int kt, head;
+  if (p.causal) {  // key tiles near the start see the most queries: launch them first
+    kt = (int)(blockIdx.x / p.heads);
+    head = (int)(blockIdx.x % p.heads);
+  } else {
+    kt = (int)(blockIdx.x % p.kvtiles);
+    head = (int)(blockIdx.x / p.kvtiles);
+  }
+  const int qrow_base = head * p.Nq;
+  const int krow_base = head * p.Nk;
+  // causal: the first query tile holding a query that sees key kt * BN (query + offset >= key)
+  const int q_first = p.causal ? max(0, kt * BN - p.offset) / BQ : 0;
+  const int nq = p.qtiles - q_first;
+  if (nq <= 0) {  // no query sees these keys: dK = dV = 0
+    if (threadIdx.x < BN && kt * BN + (int)threadIdx.x < p.Nk) {
+      const size_t row = (size_t)krow_base + kt * BN + threadIdx.x;
+      uint4* dk = reinterpret_cast<uint4*>(p.dK + row * D);
+      uint4* dv = reinterpret_cast<uint4*>(p.dV + row * D);
+#pragma unroll
+      for (int u = 0; u < D / 8; ++u) dk[u] = dv[u] = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl.kv_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl.q_full[s], 1);
+      mbar_init(&ctl.do_full[s], 1);
+      mbar_init(&ctl.q_empty[s], 1);
+      mbar_init(&ctl.do_empty[s], 1);
+    }
+    mbar_init(&ctl.s_full, 1);
+    mbar_init(&ctl.dp_full, 1);
+    mbar_init(&ctl.p_done, 256);
+    mbar_init(&ctl.ds_done, 256);
+    mbar_init(&ctl.dq_full, 1);
+    mbar_init(&ctl.dq_empty, 256);
+    mbar_init(&ctl.kv_done, 1);
+    mbar_init(&ctl.drain, 1);
+    ctl.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&ctl.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int* abort = &ctl.abort;
+
+  if (warp == kLoadWarp) {
+    // Lane 0 drives the copies and barriers. LSE_i and D_i of a whole tile whose rows start
+    // 16-byte aligned arrive by bulk copy with Q_i; otherwise (the last, partial tile of a
+    // head, or Nq not a multiple of 4) the warp stages them with bounds-checked loads:
+    // queries past the end of the head get LSE = +inf and D = 0, so P = dS = 0.
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmdO);
+      mbar_expect_tx(&ctl.kv_full, 2 * kTile);
+      for (int b = 0; b < 2; ++b) {
+        tma_load_3d(smem + kKOff + b * kBox, &tmK, &ctl.kv_full, b * 64, kt * BN, head);
+        tma_load_3d(smem + kVOff + b * kBox, &tmV, &ctl.kv_full, b * 64, kt * BN, head);
+      }
+    }
+    int last_q[kStages] = {-1, -1}, last_do[kStages] = {-1, -1};
+    // Test hook of the failure path: never arm the first Q stage, so the MMA thread's wait
+    // for it runs out (see StatusBlock); off unless a test sets it.
+    const bool skip_first = injected(p.status, kInjectBwd);
+    const bool all_bulk = !kTail || ((p.Nq % BQ) == 0 && (p.Nq % 4) == 0);
+    for (int it = 0; it < nq && (lane == 0 || !all_bulk); ++it) {
+      const int s = it % kStages;
+      const uint32_t par = ((it / kStages) - 1) & 1;
+      // Q_i's slot (and its LSE/D) frees once dK of the tile two back has run.
+      bool ok = true;
+      if (lane == 0 && it >= kStages) ok = mbar_wait(&ctl.q_empty[s], par, p.status, abort);
+      if (!all_bulk) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      const int q0 = (q_first + it) * BQ;  // first query of the tile, within the head
+      uint8_t* st = smem + kStageOff + s * 2 * kTile;
+      float* vec = reinterpret_cast<float*>(smem + kVecOff + s * kVecBytes);
+      const bool bulk = !kTail || (q0 + BQ <= p.Nq && (p.Nq % 4) == 0);
+      if (!bulk) {
+        for (int c = lane; c < BQ; c += 32) {
+          const bool in = q0 + c < p.Nq;
+          vec[c] = in ? p.LSE[qrow_base + q0 + c] : INFINITY;
+          vec[BQ + c] = in ? p.Dvec[qrow_base + q0 + c] : 0.f;
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        if (it > 0 || !skip_first) {
+          mbar_expect_tx(&ctl.q_full[s], kTile + (bulk ? kVecBytes : 0));
+          for (int b = 0; b < 2; ++b) tma_load_3d(st + b * kBox, &tmQ, &ctl.q_full[s], b * 64, q0, head);
+          if (bulk) {
+            bulk_load(vec, p.LSE + qrow_base + q0, BQ * 4, &ctl.q_full[s]);
+            bulk_load(vec + BQ, p.Dvec + qrow_base + q0, BQ * 4, &ctl.q_full[s]);
+          }
+          last_q[s] = it;
+        }
+        // dO_i's slot frees once dV of the tile two back has run (earlier than Q's).
+        if (it >= kStages && !mbar_wait(&ctl.do_empty[s], par, p.status, abort)) ok = false;
+        if (ok) {
+          mbar_expect_tx(&ctl.do_full[s], kTile);
+          for (int b = 0; b < 2; ++b) tma_load_3d(st + kTile + b * kBox, &tmdO, &ctl.do_full[s], b * 64, q0, head);
+          last_do[s] = it;
+        }
+      }
+      if (!all_bulk) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+    }
+    if (lane == 0) {  // every issued copy must land before the CTA may exit
+      mbar_wait(&ctl.kv_full, 0, p.status, nullptr);
+      for (int s = 0; s < kStages; ++s) {
+        if (last_q[s] >= 0) mbar_wait(&ctl.q_full[s], (last_q[s] / kStages) & 1, p.status, nullptr);
+        if (last_do[s] >= 0) mbar_wait(&ctl.do_full[s], (last_do[s] / kStages) & 1, p.status, nullptr);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idSP = idesc_bf16(BN, BQ, false, false);  // S^T, dP^T
+      constexpr uint32_t idKV = idesc_bf16(BN, D, false, true);    // dV, dK (B MN-major)
+      constexpr uint32_t idQ = idesc_bf16(D, BQ, true, true);      // dQ^T (A and B MN-major)
+      const uint32_t aStage = smem_u32(smem + kStageOff);
+      // Base descriptors; each MMA below only advances the start address.
+      const uint64_t dKk = sdesc_sw128(smem_u32(smem + kKOff), 16, 1024);     // K_j, K-major
+      const uint64_t dKmn = sdesc_sw128(smem_u32(smem + kKOff), kBox, 1024);  // K_j^T, MN-major
+      const uint64_t dVk = sdesc_sw128(smem_u32(smem + kVOff), 16, 1024);
+      const uint64_t dSk = sdesc_sw128(smem_u32(smem + kDsOff), 16, 1024);    // dS^T as A, K-major
+      const uint64_t dSmn = sdesc_sw128(smem_u32(smem + kDsOff), kBox, 1024); // dS^T as B, MN-major
+      auto stage_k = [&](int s, bool dO) { return sdesc_sw128(aStage + s * 2 * kTile + (dO ? kTile : 0), 16, 1024); };
+      auto stage_mn = [&](int s, bool dO) {
+        return sdesc_sw128(aStage + s * 2 * kTile + (dO ? kTile : 0), kBox, 1024);
+      };
+      // K = d: 16 columns (32 bytes) per step inside a box, the next box after 4 steps
+      auto issue_S = [&](int s) {
+        const uint64_t qd = stage_k(s, false);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tmem + kColS, sdesc_add(dKk, (k / 4) * kBox + (k % 4) * 32), sdesc_add(qd, (k / 4) * kBox + (k % 4) * 32),
+                 idSP, k > 0);
+      };
+      auto issue_dP = [&](int s) {
+        const uint64_t od = stage_k(s, true);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tmem + kColDP, sdesc_add(dVk, (k / 4) * kBox + (k % 4) * 32),
+                 sdesc_add(od, (k / 4) * kBox + (k % 4) * 32), idSP, k > 0);
+      };
+      // K = queries: 16 rows (2048 bytes) of the MN-major dO_i / Q_i per step
+      auto issue_dV = [&](int it, int s) {
+        const uint64_t bd = stage_mn(s, true);
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k)
+          mma_ts(tmem + kColDV, packed_col(tmem + kColS, k), sdesc_add(bd, k * 2048), idKV, (it > 0 || k > 0) ? 1u : 0u);
+      };
+      auto issue_dK = [&](int it, int s) {
+        const uint64_t bd = stage_mn(s, false);
+#pragma unroll
+        for (int k = 0; k < BQ / 16; ++k)
+          mma_ss(tmem + kColDK, sdesc_add(dSk, (k / 4) * kBox + (k % 4) * 32), sdesc_add(bd, k * 2048), idKV,
+                 (it > 0 || k > 0) ? 1u : 0u);
+      };
+      // K = keys: 16 rows (2048 bytes) of K_j and of dS^T per step
+      auto issue_dQ = [&]() {
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ss(tmem + kColDP, sdesc_add(dKmn, k * 2048), sdesc_add(dSmn, k * 2048), idQ, k > 0);
+      };
+      bool ok = mbar_wait(&ctl.kv_full, 0, p.status, abort);
+      // prologue: S(0), dP(0), dV(0)
+      if (ok && (ok = mbar_wait(&ctl.q_full[0], 0, p.status, abort))) {
+        tc_fence_after();
+        issue_S(0);
+        mma_commit(&ctl.s_full);
+      }
+      if (ok && (ok = mbar_wait(&ctl.do_full[0], 0, p.status, abort))) {
+        tc_fence_after();
+        issue_dP(0);
+        mma_commit(&ctl.dp_full);
+      }
+      if (ok && (ok = mbar_wait(&ctl.p_done, 0, p.status, abort))) {
+        tc_fence_after();
+        issue_dV(0, 0);
+        mma_commit(&ctl.do_empty[0]);  // dP(0) and dV(0), the readers of dO(0), issued
+      }
+      for (int it = 0; ok && it < nq; ++it) {
+        const int s = it % kStages, s1 = (it + 1) % kStages;
+        const bool next = it + 1 < nq;
+        const uint32_t par1 = ((it + 1) / kStages) & 1;
+        // S(i+1) over the S^T columns: P^T(i) was read by dV(i), issued before
+        if (next) {
+          if (!(ok = mbar_wait(&ctl.q_full[s1], par1, p.status, abort))) break;
+          tc_fence_after();
+          issue_S(s1);
+          mma_commit(&ctl.s_full);
+        }
+        // dK(i) and dQ(i) read dS^T(i) from shared memory; dQ^T(i) lands in the dP^T
+        // columns, which phase B of tile i has read
+        if (!(ok = mbar_wait(&ctl.ds_done, it & 1, p.status, abort))) break;
+        tc_fence_after();
+        issue_dK(it, s);
+        mma_commit(&ctl.q_empty[s]);
+        issue_dQ();
+        mma_commit(&ctl.dq_full);
+        if (next) {
+          if (!(ok = mbar_wait(&ctl.p_done, (it + 1) & 1, p.status, abort))) break;
+          tc_fence_after();
+          issue_dV(it + 1, s1);
+          // dP(i+1) once the dQ warps have read the dQ^T(i) partial out of its columns
+          if (!(ok = mbar_wait(&ctl.dq_empty, it & 1, p.status, abort))) break;
+          if (!(ok = mbar_wait(&ctl.do_full[s1], par1, p.status, abort))) break;
+          tc_fence_after();
+          issue_dP(s1);
+          mma_commit(&ctl.dp_full);
+          mma_commit(&ctl.do_empty[s1]);  // dV(i+1) and dP(i+1), the readers of dO(i+1), issued
+        }
+      }
+      mma_commit(&ctl.kv_done);
+      mma_commit(&ctl.drain);
+      mbar_wait(&ctl.drain, 0, p.status, nullptr);
+    }
+  } else {
+    // ---------------- softmax-backward warpgroups, dQ read-out, dK/dV epilogue ----------------
+    const int wg = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;  // TMEM lane: the key row (S^T, dP^T, dV, dK), or the
+                                           // head-dim index (the dQ^T partial)
+    const int key = kt * BN + r;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const float2 sl2 = make_float2(p.sl2, p.sl2);
+    const float2 neg_log2e = make_float2(-kLog2e, -kLog2e);
+    const float2 minus1 = make_float2(-1.f, -1.f);
+    uint8_t* dsrow = smem + kDsOff + r * 128;
+    // The dQ^T partial of tile j: lane = head-dim index r, columns = the tile's queries; this
+    // warpgroup takes its 64 columns, releases them as soon as they are in registers (dP of
+    // the next tile waits for that), then adds them into the fp32 accumulator.
+    auto read_out_dq = [&](int j) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctl.dq_full, j & 1, p.status, abort))) return false;
+      tc_fence_after();
+      float v[64];
+      tmem_ld32x2(tmem + lane_off + kColDP + wg * 64, tmem + lane_off + kColDP + wg * 64 + 32,
+                  *reinterpret_cast<float(*)[32]>(&v[0]), *reinterpret_cast<float(*)[32]>(&v[32]));
+      tc_fence_before();
+      mbar_arrive(&ctl.dq_empty);
+      const int qh = (q_first + j) * BQ + wg * 64;  // first query of this half, within the head
+      const int nvalid = p.Nq - qh;
+      float* dst = p.dQacc + (size_t)(qrow_base + qh) * D + r;
+      // The bound test stays out of the reduction loop (a predicate inside it serialises the
+      // reductions); both loops unroll fully so v stays in registers.
+      if (!kTail || 64 <= nvalid) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) atomicAdd(dst + (size_t)c * D, v[c]);
+      } else {  // the last, partial tile of a head
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < nvalid) atomicAdd(dst + (size_t)c * D, v[c]);
+      }
+      return true;
+    };
+    bool ok = true;
+    for (int it = 0; ok && it < nq; ++it) {
+      const float* vec = reinterpret_cast<const float*>(smem + kVecOff + (it % kStages) * kVecBytes);
+      const int q0 = (q_first + it) * BQ;
+      // some key of the tile exceeds the limit of some query of the tile
+      const bool diag = p.causal && q0 + p.offset < kt * BN + BN - 1;
+      // ---- phase A: P^T = exp2(S^T * scale * log2e - LSE * log2e), over S^T in TMEM
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full, it & 1, p.status, abort));
+      if (!ok) break;
+      tc_fence_after();
+      float pr[64];  // this row's P for the warpgroup's 64 queries, kept for phase B
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = wg * 64 + ch * 32;  // first query column of this chunk
+        float sv[32];
+        tmem_ld32(tmem + lane_off + kColS + c0, sv);
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int c = c0 + 2 * u;
+          const float2 lse = *reinterpret_cast<const float2*>(vec + c);
+          const float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, fmul2(lse, neg_log2e));
+          float2 pv = make_float2(ex2(x.x), ex2(x.y));
+          if (diag) {
+            if (key > q0 + c + p.offset) pv.x = 0.f;
+            if (key > q0 + c + 1 + p.offset) pv.y = 0.f;
+          }
+          pr[ch * 32 + 2 * u] = pv.x;
+          pr[ch * 32 + 2 * u + 1] = pv.y;
+          pk[u] = pack_bf16(pv.x, pv.y);
+        }
+        tmem_st16(tmem + lane_off + kColS + wg * 64 + ch * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&ctl.p_done);
+      // ---- the previous tile's dQ^T partial, while dK/dQ of that tile and dV of this one run
+      if (it > 0 && !(ok = read_out_dq(it - 1))) break;
+      // ---- phase B: dS^T = P^T * (dP^T - D), to shared memory only
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dp_full, it & 1, p.status, abort));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = wg * 64 + ch * 32;
+        float dp[32];
+        tmem_ld32(tmem + lane_off + kColDP + c0, dp);
+        uint32_t dk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const float2 dd =
+              ffma2(*reinterpret_cast<const float2*>(vec + BQ + c0 + 2 * u), minus1, make_float2(dp[2 * u], dp[2 * u + 1]));
+          const float2 ds = fmul2(make_float2(pr[ch * 32 + 2 * u], pr[ch * 32 + 2 * u + 1]), dd);
+          dk[u] = pack_bf16(ds.x, ds.y);
+        }
+        // dS^T row r, query columns c0..c0+31: four 16-byte chunks of a 128-byte swizzled
+        // row (box c0 / 64, chunk (c0 % 64) / 8 + u, XOR (r % 8))
+        uint8_t* atom = dsrow + (c0 / 64) * kBox;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = ((c0 % 64) / 8 + u) ^ (r & 7);
+          *reinterpret_cast<uint4*>(atom + chunk * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&ctl.ds_done);
+    }
+    if (ok) ok = read_out_dq(nq - 1);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.kv_done, 0, p.status, abort));
+    if (ok) {
+      // dV and dK of key row r; warpgroup wg writes columns wg*64 .. wg*64 + 63
+      tc_fence_after();
+      const size_t row = (size_t)krow_base + kt * BN + r;
+      const bool in = !kTail || kt * BN + r < p.Nk;  // key rows past the end are not stored
+#pragma unroll 1
+      for (int c0 = wg * 64; c0 < wg * 64 + 64; c0 += 32) {
+        float v[32];
+        uint4 w[4];
+        uint32_t* wu = reinterpret_cast<uint32_t*>(w);
+        tmem_ld32(tmem + lane_off + kColDV + c0, v);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
+        uint4* dv = reinterpret_cast<uint4*>(p.dV + row * D + c0);
+        if (in) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) dv[u] = w[u];
+        }
+        tmem_ld32(tmem + lane_off + kColDK + c0, v);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u] * p.scale, v[2 * u + 1] * p.scale);
+        uint4* dk = reinterpret_cast<uint4*>(p.dK + row * D + c0);
+        if (in) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) dk[u] = w[u];
+        }
+      }
+    }
+  }
+
+  // The producer and MMA roles run on single lanes: they rejoin the rest of their warps
+  // first, so that the barrier below (which counts whole warps) holds until every role is done.
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t tc_bwd_wide(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                        const float* Dv, void* dK, void* dV, float* dQacc, const Shape& s, float scale, bool causal,
+                        int* status, cudaStream_t st) {
+  if (s.d != D) return cudaErrorInvalidValue;
+  CUtensorMap mq, mk, mv, mdo;
+  const int64_t heads = s.heads();
+  if (!make_map_bf16_3d(&mq, Q, heads, s.N, D, BQ) || !make_map_bf16_3d(&mk, K, heads, s.keys(), D, BN) ||
+      !make_map_bf16_3d(&mv, V, heads, s.keys(), D, BN) || !make_map_bf16_3d(&mdo, dO, heads, s.N, D, BQ))
+    return cudaErrorInvalidValue;
+  static bool attr = [] {
+    return cudaFuncSetAttribute(fa_bwd_wide_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBytes) == cudaSuccess &&
+           cudaFuncSetAttribute(fa_bwd_wide_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ==
+               cudaSuccess;
+  }();
+  if (!attr) return cudaErrorInvalidConfiguration;
+  WideParams p;
+  p.LSE = LSE;
+  p.Dvec = Dv;
+  p.dQacc = dQacc;
+  p.dK = static_cast<__nv_bfloat16*>(dK);
+  p.dV = static_cast<__nv_bfloat16*>(dV);
+  p.status = status;
+  p.Nq = s.N;
+  p.Nk = s.keys();
+  p.heads = (int)heads;
+  p.kvtiles = (s.keys() + BN - 1) / BN;
+  p.qtiles = (s.N + BQ - 1) / BQ;
+  p.causal = causal ? 1 : 0;
+  p.offset = causal ? s.keys() - s.N : 0;
+  p.scale = scale;
+  p.sl2 = scale * kLog2e;
+  const int64_t grid = (int64_t)p.kvtiles * p.heads;
+  if (s.N % BQ != 0 || s.keys() % BN != 0)
+    fa_bwd_wide_kernel<true><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, p);
+  else
+    fa_bwd_wide_kernel<false><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa
