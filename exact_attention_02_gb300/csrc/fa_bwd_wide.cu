@@ -369,29 +369,42 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const float2 minus1 = make_float2(-1.f, -1.f);
     uint8_t* dsrow = smem + kDsOff + r * 128;
     // The dQ^T partial of tile j: lane = head-dim index r, columns = the tile's queries; this
-    // warpgroup takes its 64 columns, releases them as soon as they are in registers (dP of
-    // the next tile waits for that), then adds them into the fp32 accumulator.
+    // warpgroup takes its 64 columns and releases them as soon as they are in registers (dP of
+    // the next tile waits for that). It adds the first 32 into the fp32 accumulator at once and
+    // holds the other 32 until phase B of the next tile is done: spread out this way, the
+    // reductions slow the tensor core's operand reads less than in one burst of 64.
+    float held[32];
+    float* held_dst = nullptr;
+    int held_valid = 0;
+    // red.add of 32 columns (queries) of one head-dim row; the bound test stays out of the
+    // reduction loop (a predicate inside it serialises the reductions), and both loops unroll
+    // fully so the values stay in registers.
+    auto add32 = [&](float* dst, const float* v, int nvalid) {
+      if (!kTail || 32 <= nvalid) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) atomicAdd(dst + (size_t)c * D, v[c]);
+      } else {  // the last, partial tile of a head
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c < nvalid) atomicAdd(dst + (size_t)c * D, v[c]);
+      }
+    };
+    auto flush_held = [&]() {
+      if (held_dst) add32(held_dst, held, held_valid);
+      held_dst = nullptr;
+    };
     auto read_out_dq = [&](int j) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(&ctl.dq_full, j & 1, p.status, abort))) return false;
       tc_fence_after();
-      float v[64];
-      tmem_ld32x2(tmem + lane_off + kColDP + wg * 64, tmem + lane_off + kColDP + wg * 64 + 32,
-                  *reinterpret_cast<float(*)[32]>(&v[0]), *reinterpret_cast<float(*)[32]>(&v[32]));
+      float v[32];
+      tmem_ld32x2(tmem + lane_off + kColDP + wg * 64, tmem + lane_off + kColDP + wg * 64 + 32, v, held);
       tc_fence_before();
       mbar_arrive(&ctl.dq_empty);
       const int qh = (q_first + j) * BQ + wg * 64;  // first query of this half, within the head
-      const int nvalid = p.Nq - qh;
       float* dst = p.dQacc + (size_t)(qrow_base + qh) * D + r;
-      // The bound test stays out of the reduction loop (a predicate inside it serialises the
-      // reductions); both loops unroll fully so v stays in registers.
-      if (!kTail || 64 <= nvalid) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) atomicAdd(dst + (size_t)c * D, v[c]);
-      } else {  // the last, partial tile of a head
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < nvalid) atomicAdd(dst + (size_t)c * D, v[c]);
-      }
+      add32(dst, v, p.Nq - qh);
+      held_dst = dst + (size_t)32 * D;
+      held_valid = p.Nq - qh - 32;
       return true;
     };
     bool ok = true;
@@ -461,8 +474,10 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&ctl.ds_done);
+      flush_held();
     }
     if (ok) ok = read_out_dq(nq - 1);
+    if (ok) flush_held();
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.kv_done, 0, p.status, abort));
     if (ok) {
       // dV and dK of key row r; warpgroup wg writes columns wg*64 .. wg*64 + 63
