@@ -371,8 +371,8 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // The dQ^T partial of tile j: lane = head-dim index r, columns = the tile's queries; this
     // warpgroup takes its 64 columns and releases them as soon as they are in registers (dP of
     // the next tile waits for that). It adds the first 32 into the fp32 accumulator at once and
-    // holds the other 32 until phase B of the next tile is done: spread out this way, the
-    // reductions slow the tensor core's operand reads less than in one burst of 64.
+    // holds the other 32 for phase B of the next tile (16 after each of its two chunks): spread
+    // out this way, the reductions slow the tensor core's operand reads less than in one burst.
     float held[32];
     float* held_dst = nullptr;
     int held_valid = 0;
@@ -389,9 +389,20 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           if (c < nvalid) atomicAdd(dst + (size_t)c * D, v[c]);
       }
     };
-    auto flush_held = [&]() {
-      if (held_dst) add32(held_dst, held, held_valid);
-      held_dst = nullptr;
+    // red.add of 16 of the held columns (part 0: columns 0-15, part 1: 16-31)
+    auto flush_held = [&](int part) {
+      if (!held_dst) return;
+      float* dst = held_dst + (size_t)(16 * part) * D;
+      const int nvalid = held_valid - 16 * part;
+      if (!kTail || 16 <= nvalid) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) atomicAdd(dst + (size_t)c * D, held[16 * part + c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (c < nvalid) atomicAdd(dst + (size_t)c * D, held[16 * part + c]);
+      }
+      if (part == 1) held_dst = nullptr;
     };
     auto read_out_dq = [&](int j) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(&ctl.dq_full, j & 1, p.status, abort))) return false;
@@ -470,14 +481,18 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           const int chunk = ((c0 % 64) / 8 + u) ^ (r & 7);
           *reinterpret_cast<uint4*>(atom + chunk * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
+        if (ch == 0) flush_held(0);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&ctl.ds_done);
-      flush_held();
+      flush_held(1);
     }
     if (ok) ok = read_out_dq(nq - 1);
-    if (ok) flush_held();
+    if (ok) {
+      flush_held(0);
+      flush_held(1);
+    }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.kv_done, 0, p.status, abort));
     if (ok) {
       // dV and dK of key row r; warpgroup wg writes columns wg*64 .. wg*64 + 63
