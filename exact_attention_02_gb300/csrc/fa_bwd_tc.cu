@@ -636,7 +636,7 @@ struct DropArg {
   uint32_t t = 0;
 };
 
-// The 64-query-tile kernel: d = 64, and every call with a mask or dropout.
+// The 64-query-tile kernel: every call with a mask or dropout.
 template <int D, int kVar>
 cudaError_t launch_narrow(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                           const float* Dv, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
@@ -700,8 +700,8 @@ cudaError_t launch(const void* Q, const void* K, const void* V, const void* dO, 
                    const float* Dv, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
                    float scale, bool causal, const MaskArg& mask, const DropArg& drop, int* status,
                    cudaStream_t st) {
-  if constexpr (D == 128 && kVar == 0) {
-    // d = 128 without a mask or dropout: the 128-query-tile kernel (fa_bwd_wide.cu)
+  if constexpr (kVar == 0) {
+    // no mask or dropout: the 128-query-tile kernel (fa_bwd_wide.cu)
     cudaError_t e = cudaMemsetAsync(dQacc, 0, (size_t)s.elems() * sizeof(float), st);
     if (e != cudaSuccess) return e;
     if ((e = tc_bwd_wide(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, status, st)) != cudaSuccess) return e;

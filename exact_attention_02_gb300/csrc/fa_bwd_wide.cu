@@ -1,4 +1,4 @@
-// Attention backward for head dimension 128 on 128-query tiles (bf16 in, fp32 accumulate);
+// Attention backward on 128-query tiles, head dimension 64 or 128 (bf16 in, fp32 accumulate);
 // what it computes is fa_bwd in include/fa.h, for the calls without a mask or dropout.
 //
 // Method ("flash-attention-backpropagation", 反向总览 / Softmax梯度 / QKV梯度; the single
@@ -51,7 +51,6 @@ namespace {
 
 using namespace ptx;
 
-constexpr int D = 128;   // head dimension
 constexpr int BN = 128;  // keys per CTA
 constexpr int BQ = 128;  // queries per tile
 constexpr int kThreads = 320;
@@ -60,16 +59,9 @@ constexpr int kMmaWarp = 9;
 constexpr int kStages = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Shared memory (1024-byte aligned base; control block last).
-constexpr int kBox = 128 * 128;       // one [128 rows x 64 columns] bf16 box, 128-byte swizzle
-constexpr int kTile = 2 * kBox;       // a [128 rows x 128 columns] tile: two boxes of 64 columns
-constexpr int kKOff = 0;
-constexpr int kVOff = kKOff + kTile;
-constexpr int kStageOff = kVOff + kTile;  // stage s: Q_i at + s * 2 * kTile, dO_i right after it
-constexpr int kDsOff = kStageOff + kStages * 2 * kTile;
-constexpr int kVecOff = kDsOff + kTile;   // LSE_i then D_i of each stage
+constexpr int kBox = 128 * 128;  // one [128 rows x 64 columns] bf16 box, 128-byte swizzle
 constexpr int kVecBytes = 2 * BQ * 4;
-constexpr int kCtlOff = kVecOff + kStages * kVecBytes;
+constexpr uint32_t kTmemCols = 512;
 
 struct WideCtl {
   uint64_t kv_full, q_full[kStages], do_full[kStages], q_empty[kStages], do_empty[kStages];
@@ -77,15 +69,32 @@ struct WideCtl {
   uint32_t tmem_base;
   int abort;
 };
-constexpr int kSmemBytes = kCtlOff + (int)sizeof(WideCtl);
-static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
 
-// TMEM columns.
-constexpr uint32_t kColDV = 0;
-constexpr uint32_t kColDK = 128;
-constexpr uint32_t kColS = 256;   // S^T, then P^T (bf16 pairs) in its first half of each 64
-constexpr uint32_t kColDP = 384;  // dP^T, then the dQ^T partial
-constexpr uint32_t kTmemCols = 512;
+// Sizes and places for head dimension D (64 or 128).
+template <int D>
+struct WideCfg {
+  static constexpr int kBoxes = D / 64;         // 64-column boxes per row
+  static constexpr int kRowTile = 128 * D * 2;  // a [128 rows x D] bf16 tile: K_j, V_j, Q_i or dO_i
+  // Shared memory (1024-byte aligned base; control block last). V follows K: at d = 64 the
+  // M = 128 dQ^T product reads V's rows as the second 64-row atom of K^T, and those result
+  // rows land in TMEM lanes 64-127, which nobody reads.
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kRowTile;
+  static constexpr int kStageOff = kVOff + kRowTile;  // stage s: Q_i at + s * 2 * kRowTile, dO_i after it
+  static constexpr int kDsOff = kStageOff + kStages * 2 * kRowTile;
+  static constexpr int kVecOff = kDsOff + 2 * kBox;   // dS^T is [128 keys x 128 queries]; then LSE_i, D_i
+  static constexpr int kCtlOff = kVecOff + kStages * kVecBytes;
+  static constexpr int kSmemBytes = kCtlOff + (int)sizeof(WideCtl);
+  static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
+  static_assert(D == 128 || kVOff == kKOff + kBox, "V follows K");
+  // TMEM columns: dV | dK | S^T (then P^T, bf16 pairs, in the first half of each 64) |
+  // dP^T (then the dQ^T partial)
+  static constexpr uint32_t kColDV = 0;
+  static constexpr uint32_t kColDK = D;
+  static constexpr uint32_t kColS = 2 * D;
+  static constexpr uint32_t kColDP = 2 * D + 128;
+  static_assert(kColDP + 128 <= kTmemCols, "TMEM budget");
+};
 
 struct WideParams {
   const float* LSE;
@@ -119,11 +128,13 @@ __device__ __forceinline__ uint32_t packed_col(uint32_t base, int k) { return ba
 // 10 warps put at most 3 warps on each of the SM's four sub-partitions (16 K registers each),
 // which allows 168 registers per thread: a softmax thread holds its 64 weights from phase A
 // to phase B and, between the two, a 64-column row of the dQ partial.
-template <bool kTail>
+template <int D, bool kTail>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                    const WideParams p) {
+  using C = WideCfg<D>;
+  constexpr uint32_t kColDV = C::kColDV, kColDK = C::kColDK, kColS = C::kColS, kColDP = C::kColDP;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // The swizzled operand layout needs a 1024-byte aligned base; the runtime provides it for
@@ -132,7 +143,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     if (threadIdx.x == 0 && p.status) atomicExch(p.status, 3 /* FA_ERR_CUDA */);
     return;
   }
-  WideCtl& ctl = *reinterpret_cast<WideCtl*>(smem + kCtlOff);
+  WideCtl& ctl = *reinterpret_cast<WideCtl*>(smem + C::kCtlOff);
 
   int kt, head;
   if (p.causal) {  // key tiles near the start see the most queries: launch them first
@@ -194,10 +205,10 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
-      mbar_expect_tx(&ctl.kv_full, 2 * kTile);
-      for (int b = 0; b < 2; ++b) {
-        tma_load_3d(smem + kKOff + b * kBox, &tmK, &ctl.kv_full, b * 64, kt * BN, head);
-        tma_load_3d(smem + kVOff + b * kBox, &tmV, &ctl.kv_full, b * 64, kt * BN, head);
+      mbar_expect_tx(&ctl.kv_full, 2 * C::kRowTile);
+      for (int b = 0; b < C::kBoxes; ++b) {
+        tma_load_3d(smem + C::kKOff + b * kBox, &tmK, &ctl.kv_full, b * 64, kt * BN, head);
+        tma_load_3d(smem + C::kVOff + b * kBox, &tmV, &ctl.kv_full, b * 64, kt * BN, head);
       }
     }
     int last_q[kStages] = {-1, -1}, last_do[kStages] = {-1, -1};
@@ -214,8 +225,8 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       if (!all_bulk) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       const int q0 = (q_first + it) * BQ;  // first query of the tile, within the head
-      uint8_t* st = smem + kStageOff + s * 2 * kTile;
-      float* vec = reinterpret_cast<float*>(smem + kVecOff + s * kVecBytes);
+      uint8_t* st = smem + C::kStageOff + s * 2 * C::kRowTile;
+      float* vec = reinterpret_cast<float*>(smem + C::kVecOff + s * kVecBytes);
       const bool bulk = !kTail || (q0 + BQ <= p.Nq && (p.Nq % 4) == 0);
       if (!bulk) {
         for (int c = lane; c < BQ; c += 32) {
@@ -227,8 +238,8 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
       if (lane == 0) {
         if (it > 0 || !skip_first) {
-          mbar_expect_tx(&ctl.q_full[s], kTile + (bulk ? kVecBytes : 0));
-          for (int b = 0; b < 2; ++b) tma_load_3d(st + b * kBox, &tmQ, &ctl.q_full[s], b * 64, q0, head);
+          mbar_expect_tx(&ctl.q_full[s], C::kRowTile + (bulk ? kVecBytes : 0));
+          for (int b = 0; b < C::kBoxes; ++b) tma_load_3d(st + b * kBox, &tmQ, &ctl.q_full[s], b * 64, q0, head);
           if (bulk) {
             bulk_load(vec, p.LSE + qrow_base + q0, BQ * 4, &ctl.q_full[s]);
             bulk_load(vec + BQ, p.Dvec + qrow_base + q0, BQ * 4, &ctl.q_full[s]);
@@ -238,8 +249,9 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         // dO_i's slot frees once dV of the tile two back has run (earlier than Q's).
         if (it >= kStages && !mbar_wait(&ctl.do_empty[s], par, p.status, abort)) ok = false;
         if (ok) {
-          mbar_expect_tx(&ctl.do_full[s], kTile);
-          for (int b = 0; b < 2; ++b) tma_load_3d(st + kTile + b * kBox, &tmdO, &ctl.do_full[s], b * 64, q0, head);
+          mbar_expect_tx(&ctl.do_full[s], C::kRowTile);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(st + C::kRowTile + b * kBox, &tmdO, &ctl.do_full[s], b * 64, q0, head);
           last_do[s] = it;
         }
       }
@@ -257,17 +269,19 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     if (lane == 0) {
       constexpr uint32_t idSP = idesc_bf16(BN, BQ, false, false);  // S^T, dP^T
       constexpr uint32_t idKV = idesc_bf16(BN, D, false, true);    // dV, dK (B MN-major)
-      constexpr uint32_t idQ = idesc_bf16(D, BQ, true, true);      // dQ^T (A and B MN-major)
-      const uint32_t aStage = smem_u32(smem + kStageOff);
+      constexpr uint32_t idQ = idesc_bf16(128, BQ, true, true);    // dQ^T (A and B MN-major), M = 128
+      const uint32_t aStage = smem_u32(smem + C::kStageOff);
       // Base descriptors; each MMA below only advances the start address.
-      const uint64_t dKk = sdesc_sw128(smem_u32(smem + kKOff), 16, 1024);     // K_j, K-major
-      const uint64_t dKmn = sdesc_sw128(smem_u32(smem + kKOff), kBox, 1024);  // K_j^T, MN-major
-      const uint64_t dVk = sdesc_sw128(smem_u32(smem + kVOff), 16, 1024);
-      const uint64_t dSk = sdesc_sw128(smem_u32(smem + kDsOff), 16, 1024);    // dS^T as A, K-major
-      const uint64_t dSmn = sdesc_sw128(smem_u32(smem + kDsOff), kBox, 1024); // dS^T as B, MN-major
-      auto stage_k = [&](int s, bool dO) { return sdesc_sw128(aStage + s * 2 * kTile + (dO ? kTile : 0), 16, 1024); };
+      const uint64_t dKk = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);     // K_j, K-major
+      const uint64_t dKmn = sdesc_sw128(smem_u32(smem + C::kKOff), kBox, 1024);  // K_j^T, MN-major
+      const uint64_t dVk = sdesc_sw128(smem_u32(smem + C::kVOff), 16, 1024);
+      const uint64_t dSk = sdesc_sw128(smem_u32(smem + C::kDsOff), 16, 1024);    // dS^T as A, K-major
+      const uint64_t dSmn = sdesc_sw128(smem_u32(smem + C::kDsOff), kBox, 1024); // dS^T as B, MN-major
+      auto stage_k = [&](int s, bool dO) {
+        return sdesc_sw128(aStage + s * 2 * C::kRowTile + (dO ? C::kRowTile : 0), 16, 1024);
+      };
       auto stage_mn = [&](int s, bool dO) {
-        return sdesc_sw128(aStage + s * 2 * kTile + (dO ? kTile : 0), kBox, 1024);
+        return sdesc_sw128(aStage + s * 2 * C::kRowTile + (dO ? C::kRowTile : 0), kBox, 1024);
       };
       // K = d: 16 columns (32 bytes) per step inside a box, the next box after 4 steps
       auto issue_S = [&](int s) {
@@ -367,7 +381,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const float2 sl2 = make_float2(p.sl2, p.sl2);
     const float2 neg_log2e = make_float2(-kLog2e, -kLog2e);
     const float2 minus1 = make_float2(-1.f, -1.f);
-    uint8_t* dsrow = smem + kDsOff + r * 128;
+    uint8_t* dsrow = smem + C::kDsOff + r * 128;
     // The dQ^T partial of tile j: lane = head-dim index r, columns = the tile's queries; this
     // warpgroup takes its 64 columns and releases them as soon as they are in registers (dP of
     // the next tile waits for that). It adds the first 32 into the fp32 accumulator at once and
@@ -404,6 +418,9 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
       if (part == 1) held_dst = nullptr;
     };
+    // At d = 64 only TMEM lanes 0-63 hold head-dim rows: the warps of lanes 64-127 load their
+    // (unused) lanes too, but add nothing (a test that is uniform over each warp).
+    const bool dq_rows = (warp & 3) * 32 < D;
     auto read_out_dq = [&](int j) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(&ctl.dq_full, j & 1, p.status, abort))) return false;
       tc_fence_after();
@@ -411,6 +428,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       tmem_ld32x2(tmem + lane_off + kColDP + wg * 64, tmem + lane_off + kColDP + wg * 64 + 32, v, held);
       tc_fence_before();
       mbar_arrive(&ctl.dq_empty);
+      if (!dq_rows) return true;
       const int qh = (q_first + j) * BQ + wg * 64;  // first query of this half, within the head
       float* dst = p.dQacc + (size_t)(qrow_base + qh) * D + r;
       add32(dst, v, p.Nq - qh);
@@ -420,7 +438,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     };
     bool ok = true;
     for (int it = 0; ok && it < nq; ++it) {
-      const float* vec = reinterpret_cast<const float*>(smem + kVecOff + (it % kStages) * kVecBytes);
+      const float* vec = reinterpret_cast<const float*>(smem + C::kVecOff + (it % kStages) * kVecBytes);
       const int q0 = (q_first + it) * BQ;
       // some key of the tile exceeds the limit of some query of the tile
       const bool diag = p.causal && q0 + p.offset < kt * BN + BN - 1;
@@ -495,12 +513,12 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.kv_done, 0, p.status, abort));
     if (ok) {
-      // dV and dK of key row r; warpgroup wg writes columns wg*64 .. wg*64 + 63
+      // dV and dK of key row r; warpgroup wg writes columns wg*D/2 .. wg*D/2 + D/2 - 1
       tc_fence_after();
       const size_t row = (size_t)krow_base + kt * BN + r;
       const bool in = !kTail || kt * BN + r < p.Nk;  // key rows past the end are not stored
 #pragma unroll 1
-      for (int c0 = wg * 64; c0 < wg * 64 + 64; c0 += 32) {
+      for (int c0 = wg * (D / 2); c0 < wg * (D / 2) + D / 2; c0 += 32) {
         float v[32];
         uint4 w[4];
         uint32_t* wu = reinterpret_cast<uint32_t*>(w);
@@ -535,22 +553,21 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   }
 }
 
-}  // namespace
-
-cudaError_t tc_bwd_wide(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+template <int D>
+cudaError_t launch_wide(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                         const float* Dv, void* dK, void* dV, float* dQacc, const Shape& s, float scale, bool causal,
                         int* status, cudaStream_t st) {
-  if (s.d != D) return cudaErrorInvalidValue;
+  using C = WideCfg<D>;
   CUtensorMap mq, mk, mv, mdo;
   const int64_t heads = s.heads();
   if (!make_map_bf16_3d(&mq, Q, heads, s.N, D, BQ) || !make_map_bf16_3d(&mk, K, heads, s.keys(), D, BN) ||
       !make_map_bf16_3d(&mv, V, heads, s.keys(), D, BN) || !make_map_bf16_3d(&mdo, dO, heads, s.N, D, BQ))
     return cudaErrorInvalidValue;
   static bool attr = [] {
-    return cudaFuncSetAttribute(fa_bwd_wide_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmemBytes) == cudaSuccess &&
-           cudaFuncSetAttribute(fa_bwd_wide_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ==
-               cudaSuccess;
+    return cudaFuncSetAttribute(fa_bwd_wide_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmemBytes) == cudaSuccess &&
+           cudaFuncSetAttribute(fa_bwd_wide_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmemBytes) == cudaSuccess;
   }();
   if (!attr) return cudaErrorInvalidConfiguration;
   WideParams p;
@@ -571,10 +588,20 @@ cudaError_t tc_bwd_wide(const void* Q, const void* K, const void* V, const void*
   p.sl2 = scale * kLog2e;
   const int64_t grid = (int64_t)p.kvtiles * p.heads;
   if (s.N % BQ != 0 || s.keys() % BN != 0)
-    fa_bwd_wide_kernel<true><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, p);
+    fa_bwd_wide_kernel<D, true><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
   else
-    fa_bwd_wide_kernel<false><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, mdo, p);
+    fa_bwd_wide_kernel<D, false><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_bwd_wide(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                        const float* Dv, void* dK, void* dV, float* dQacc, const Shape& s, float scale, bool causal,
+                        int* status, cudaStream_t st) {
+  if (s.d == 64) return launch_wide<64>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, status, st);
+  if (s.d == 128) return launch_wide<128>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, status, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

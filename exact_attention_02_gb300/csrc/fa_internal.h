@@ -85,9 +85,9 @@ cudaError_t tc_bwd(const void* Q, const void* K, const void* V, const void* dO, 
                    const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st);
 
-// The backward kernel alone (no zeroing, no convert) for d = 128 without a mask or dropout,
-// on 128-query tiles (fa_bwd_wide.cu): dQacc must be zero on entry and receives the
-// unscaled fp32 dQ sums.
+// The backward kernel alone (no zeroing, no convert) without a mask or dropout, on
+// 128-query tiles (fa_bwd_wide.cu; d = 64 or 128): dQacc must be zero on entry and receives
+// the unscaled fp32 dQ sums.
 cudaError_t tc_bwd_wide(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                         const float* Dv, void* dK, void* dV, float* dQacc, const Shape& s, float scale, bool causal,
                         int* status, cudaStream_t st);
