@@ -229,7 +229,8 @@ def recorded_traffic(kernel, w):
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f).get(kernel)
+            recs = json.load(f)
+        rec = recs.get(f"{kernel}@{w.name}") or recs.get(kernel)  # a record for this workload first
         if not rec or rec["workload"] != w.name:
             return None
         h = hashlib.sha256()
