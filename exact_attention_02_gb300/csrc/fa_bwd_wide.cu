@@ -1,5 +1,6 @@
 // Attention backward on 128-query tiles, head dimension 64 or 128 (bf16 in, fp32 accumulate);
-// what it computes is fa_bwd in include/fa.h, for the calls without a mask or dropout.
+// what it computes is fa_bwd in include/fa.h, and fa_bwd_masked, fa_bwd_bitmask and
+// fa_bwd_dropout with their mask or dropout (the kVar instances).
 //
 // Method ("flash-attention-backpropagation", 反向总览 / Softmax梯度 / QKV梯度; the single
 // recompute per tile of "FlashAttention 反向传播" 踩坑二): one CTA owns a 128-key tile of
@@ -36,13 +37,19 @@
 // producer; 9 MMA issuer. Shared memory: K, V (32 KB each), two Q/dO stages (64 KB each),
 // dS^T (32 KB) and LSE/D per stage.
 //
-// Query and key lengths as in fa_bwd_tc.cu: Nq query rows against Nk key rows per head,
+// Masks and dropout (kVar, "知识点13" §7: both are fused into the softmax step): the additive
+// mask adds M log2(e) to each exponent; the boolean mask (packed bits, as the forward reads
+// them) and dropout zero P for hidden or dropped keys, so their dS is 0 as well; dV takes only
+// the kept weights, scaled by 256 / (256 - t) in its epilogue, and a dropped key's dP is 0.
+//
+// Query and key lengths: Nq query rows against Nk key rows per head,
 // causal bottom-right aligned (query i hides keys j > i + Nk - Nq); rows past the end of a
 // head arrive as zeros from the tensor maps, queries past the end get LSE = +inf (P = 0),
 // and rows past the end are neither accumulated nor stored.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
+#include "philox.cuh"
 #include "sm100_ptx.cuh"
 #include "tma_host.h"
 
@@ -113,6 +120,36 @@ struct WideParams {
   float sl2;   // scale * log2(e)
 };
 
+// The arguments of the mask and dropout instances, a kernel argument of their own: with them in
+// WideParams the plain instance measured 3% slower, same source and registers otherwise.
+struct VarParams {
+  // additive mask (kVar == 1): element (b, h, i, j) at mask[b*mask_sb + h*mask_sh + i*mask_srow + j]
+  const __nv_bfloat16* mask;
+  // boolean mask (kVar == 3): visibility bits, word (b, h, i, j / 32) at
+  // bits[b*mask_sb + h*mask_sh + i*mask_srow + j / 32] (the same strides, in 32-bit words)
+  const uint32_t* bits;
+  int64_t mask_sb, mask_sh, mask_srow;
+  int H;
+  // dropout (kVar == 2): Philox key, keep threshold (in all four bytes) and a kept weight's scale
+  uint32_t seed_lo, seed_hi, drop_tt;
+  float drop_scale;
+};
+
+// Transpose of a 32 x 32 bit matrix held one row per lane: on return lane T holds bit c =
+// bit T of lane c's row. Five butterfly stages; the stage of width s swaps, between lanes l
+// and l ^ s, the s-bit groups whose position differs from the lane in bit s.
+__device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
+  constexpr uint32_t kLow[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const int s = 16 >> k;
+    const uint32_t m = kLow[k];  // bit positions p with (p & s) == 0
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, s);
+    x = (lane & s) ? ((x & ~m) | ((y & ~m) >> s)) : ((x & m) | ((y & m) << s));
+  }
+  return x;
+}
+
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -128,12 +165,16 @@ __device__ __forceinline__ uint32_t packed_col(uint32_t base, int k) { return ba
 // 10 warps put at most 3 warps on each of the SM's four sub-partitions (16 K registers each),
 // which allows 168 registers per thread: a softmax thread holds its 64 weights from phase A
 // to phase B and, between the two, a 64-column row of the dQ partial.
-template <int D, bool kTail>
+// kVar: 0 plain, 1 additive mask, 2 dropout, 3 boolean mask (packed bits).
+template <int D, bool kTail, int kVar>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                   const WideParams p) {
+                   const WideParams p, const VarParams pv) {
   using C = WideCfg<D>;
+  constexpr bool kMask = kVar == 1;
+  constexpr bool kDrop = kVar == 2;
+  constexpr bool kBits = kVar == 3;
   constexpr uint32_t kColDV = C::kColDV, kColDK = C::kColDK, kColS = C::kColS, kColDP = C::kColDP;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -436,9 +477,30 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       held_valid = p.Nq - qh - 32;
       return true;
     };
+    // kBits: the warp's 32 keys are one word of each query's row. For chunk ch, lane L reads the
+    // word of query (tile start + wg * 64 + ch * 32 + L), one tile ahead, so that the load's
+    // latency hides behind the current tile.
+    const int kword = (kt * BN + (warp & 3) * 32) >> 5;
+    const uint32_t* bcol =
+        kBits ? pv.bits + (int64_t)(head / pv.H) * pv.mask_sb + (int64_t)(head % pv.H) * pv.mask_sh + kword : nullptr;
+    auto bits_word = [&](int it, int ch) -> uint32_t {
+      const int q = (q_first + it) * BQ + wg * 64 + ch * 32 + lane;
+      return (it < nq && (!kTail || (q < p.Nq && kword * 32 < p.Nk))) ? bcol[(int64_t)q * pv.mask_srow] : 0u;
+    };
+    uint32_t bword[2] = {0u, 0u};
+    if constexpr (kBits) {
+      bword[0] = bits_word(0, 0);
+      bword[1] = bits_word(0, 1);
+    }
     bool ok = true;
     for (int it = 0; ok && it < nq; ++it) {
       const float* vec = reinterpret_cast<const float*>(smem + C::kVecOff + (it % kStages) * kVecBytes);
+      uint32_t bcur[2] = {bword[0], bword[1]};
+      if constexpr (kBits) {
+        bword[0] = bits_word(it + 1, 0);
+        bword[1] = bits_word(it + 1, 1);
+      }
+      uint32_t kbits[2] = {0u, 0u};  // kDrop: keep bits of this key against each chunk's 32 queries
       const int q0 = (q_first + it) * BQ;
       // some key of the tile exceeds the limit of some query of the tile
       const bool diag = p.causal && q0 + p.offset < kt * BN + BN - 1;
@@ -450,22 +512,76 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = wg * 64 + ch * 32;  // first query column of this chunk
+        // kMask: M(query, this key) * log2(e) for the chunk's 32 queries (across the warp each
+        // load reads 32 consecutive keys of one mask row), issued before the TMEM load
+        float mk[kMask ? 32 : 1];
+        if constexpr (kMask) {
+          const __nv_bfloat16* mcol = pv.mask + (int64_t)(head / pv.H) * pv.mask_sb + (int64_t)(head % pv.H) * pv.mask_sh + key;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int q = q0 + c0 + c;
+            mk[c] = (!kTail || (key < p.Nk && q < p.Nq)) ? __bfloat162float(mcol[(int64_t)q * pv.mask_srow]) * kLog2e : 0.f;
+          }
+        }
+        // kDrop: lane L draws the keep bits of query (chunk start + L) against the warp's 32
+        // keys (two Philox blocks of 16 keys); the transpose leaves lane T with bit c =
+        // keep(query c of the chunk, key T). kBits: the same transpose of the prefetched words.
+        if constexpr (kDrop) {
+          const uint32_t i = (uint32_t)(q0 + c0 + lane);
+          const uint32_t blk0 = (uint32_t)((kt * BN + (warp & 3) * 32) >> 4);
+          const uint32_t row = rng::keep16(blk0, i, (uint32_t)head, pv.seed_lo, pv.seed_hi, pv.drop_tt) |
+                               (rng::keep16(blk0 + 1, i, (uint32_t)head, pv.seed_lo, pv.seed_hi, pv.drop_tt) << 16);
+          kbits[ch] = transpose32(row, lane);
+        }
+        const uint32_t vbits = kBits ? transpose32(bcur[ch], lane) : 0u;
         float sv[32];
         tmem_ld32(tmem + lane_off + kColS + c0, sv);
         uint32_t pk[16];
+        if constexpr (kVar == 0) {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int c = c0 + 2 * u;
+            const float2 lse = *reinterpret_cast<const float2*>(vec + c);
+            const float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, fmul2(lse, neg_log2e));
+            float2 pv = make_float2(ex2(x.x), ex2(x.y));
+            if (diag) {
+              if (key > q0 + c + p.offset) pv.x = 0.f;
+              if (key > q0 + c + 1 + p.offset) pv.y = 0.f;
+            }
+            pr[ch * 32 + 2 * u] = pv.x;
+            pr[ch * 32 + 2 * u + 1] = pv.y;
+            pk[u] = pack_bf16(pv.x, pv.y);
+          }
+        } else {
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int c = c0 + 2 * u;
           const float2 lse = *reinterpret_cast<const float2*>(vec + c);
-          const float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, fmul2(lse, neg_log2e));
+          float2 nl = fmul2(lse, neg_log2e);
+          if constexpr (kMask || kBits) {  // a query with no visible key (LSE = -inf) has P = 0
+            if (lse.x == -INFINITY) nl.x = -INFINITY;
+            if (lse.y == -INFINITY) nl.y = -INFINITY;
+          }
+          float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, nl);
+          if constexpr (kMask) x = fadd2(x, make_float2(mk[2 * u], mk[2 * u + 1]));
           float2 pv = make_float2(ex2(x.x), ex2(x.y));
+          if constexpr (kBits) {  // a hidden key has P = 0, and so dS = 0
+            if (!((vbits >> (2 * u)) & 1u)) pv.x = 0.f;
+            if (!((vbits >> (2 * u + 1)) & 1u)) pv.y = 0.f;
+          }
           if (diag) {
             if (key > q0 + c + p.offset) pv.x = 0.f;
             if (key > q0 + c + 1 + p.offset) pv.y = 0.f;
           }
           pr[ch * 32 + 2 * u] = pv.x;
           pr[ch * 32 + 2 * u + 1] = pv.y;
-          pk[u] = pack_bf16(pv.x, pv.y);
+          if constexpr (kDrop) {  // dV takes the kept weights (scaled by c in its epilogue)
+            const uint32_t kb = kbits[ch] >> (2 * u);
+            pk[u] = pack_bf16((kb & 1u) ? pv.x : 0.f, (kb & 2u) ? pv.y : 0.f);
+          } else {
+            pk[u] = pack_bf16(pv.x, pv.y);
+          }
+        }
         }
         tmem_st16(tmem + lane_off + kColS + wg * 64 + ch * 16, pk);
       }
@@ -486,8 +602,16 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         uint32_t dk[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const float2 dd =
-              ffma2(*reinterpret_cast<const float2*>(vec + BQ + c0 + 2 * u), minus1, make_float2(dp[2 * u], dp[2 * u + 1]));
+          float2 dd;
+          if constexpr (kDrop) {  // dP of a dropped key is 0; a kept one is scaled
+            const float2 dvec = *reinterpret_cast<const float2*>(vec + BQ + c0 + 2 * u);
+            const uint32_t kb = kbits[ch] >> (2 * u);
+            dd = make_float2((kb & 1u) ? fmaf(dp[2 * u], pv.drop_scale, -dvec.x) : -dvec.x,
+                             (kb & 2u) ? fmaf(dp[2 * u + 1], pv.drop_scale, -dvec.y) : -dvec.y);
+          } else {
+            dd = ffma2(*reinterpret_cast<const float2*>(vec + BQ + c0 + 2 * u), minus1,
+                       make_float2(dp[2 * u], dp[2 * u + 1]));
+          }
           const float2 ds = fmul2(make_float2(pr[ch * 32 + 2 * u], pr[ch * 32 + 2 * u + 1]), dd);
           dk[u] = pack_bf16(ds.x, ds.y);
         }
@@ -523,8 +647,13 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         uint4 w[4];
         uint32_t* wu = reinterpret_cast<uint32_t*>(w);
         tmem_ld32(tmem + lane_off + kColDV + c0, v);
+        if constexpr (kDrop) {  // kept weights entered dV unscaled
 #pragma unroll
-        for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
+          for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u] * pv.drop_scale, v[2 * u + 1] * pv.drop_scale);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u], v[2 * u + 1]);
+        }
         uint4* dv = reinterpret_cast<uint4*>(p.dV + row * D + c0);
         if (in) {
 #pragma unroll
@@ -553,10 +682,10 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   }
 }
 
-template <int D>
+template <int D, int kVar>
 cudaError_t launch_wide(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                         const float* Dv, void* dK, void* dV, float* dQacc, const Shape& s, float scale, bool causal,
-                        int* status, cudaStream_t st) {
+                        const BwdVariant& var, int* status, cudaStream_t st) {
   using C = WideCfg<D>;
   CUtensorMap mq, mk, mv, mdo;
   const int64_t heads = s.heads();
@@ -564,9 +693,9 @@ cudaError_t launch_wide(const void* Q, const void* K, const void* V, const void*
       !make_map_bf16_3d(&mv, V, heads, s.keys(), D, BN) || !make_map_bf16_3d(&mdo, dO, heads, s.N, D, BQ))
     return cudaErrorInvalidValue;
   static bool attr = [] {
-    return cudaFuncSetAttribute(fa_bwd_wide_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(fa_bwd_wide_kernel<D, false, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes) == cudaSuccess &&
-           cudaFuncSetAttribute(fa_bwd_wide_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+           cudaFuncSetAttribute(fa_bwd_wide_kernel<D, true, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes) == cudaSuccess;
   }();
   if (!attr) return cudaErrorInvalidConfiguration;
@@ -586,21 +715,45 @@ cudaError_t launch_wide(const void* Q, const void* K, const void* V, const void*
   p.offset = causal ? s.keys() - s.N : 0;
   p.scale = scale;
   p.sl2 = scale * kLog2e;
+  VarParams pv;
+  pv.mask = static_cast<const __nv_bfloat16*>(var.mask);
+  pv.bits = static_cast<const uint32_t*>(var.mask);
+  pv.mask_sb = var.sb;
+  pv.mask_sh = var.sh;
+  pv.mask_srow = var.srow;
+  pv.H = s.H;
+  pv.seed_lo = (uint32_t)(var.seed & 0xFFFFFFFFu);
+  pv.seed_hi = (uint32_t)(var.seed >> 32);
+  pv.drop_tt = var.threshold * 0x01010101u;
+  pv.drop_scale = (float)(256.0 / (256.0 - (double)var.threshold));
   const int64_t grid = (int64_t)p.kvtiles * p.heads;
   if (s.N % BQ != 0 || s.keys() % BN != 0)
-    fa_bwd_wide_kernel<D, true><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
+    fa_bwd_wide_kernel<D, true, kVar><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p, pv);
   else
-    fa_bwd_wide_kernel<D, false><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p);
+    fa_bwd_wide_kernel<D, false, kVar><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p, pv);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_wide_var(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                            const float* Dv, void* dK, void* dV, float* dQacc, const Shape& s, float scale,
+                            bool causal, const BwdVariant& var, int* status, cudaStream_t st) {
+  switch (var.kind) {
+    case 0: return launch_wide<D, 0>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
+    case 1: return launch_wide<D, 1>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
+    case 2: return launch_wide<D, 2>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
+    case 3: return launch_wide<D, 3>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t tc_bwd_wide(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                         const float* Dv, void* dK, void* dV, float* dQacc, const Shape& s, float scale, bool causal,
-                        int* status, cudaStream_t st) {
-  if (s.d == 64) return launch_wide<64>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, status, st);
-  if (s.d == 128) return launch_wide<128>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, status, st);
+                        const BwdVariant& var, int* status, cudaStream_t st) {
+  if (s.d == 64) return launch_wide_var<64>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
+  if (s.d == 128) return launch_wide_var<128>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
   return cudaErrorInvalidValue;
 }
 

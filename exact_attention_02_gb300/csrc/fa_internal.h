@@ -85,12 +85,22 @@ cudaError_t tc_bwd(const void* Q, const void* K, const void* V, const void* dO, 
                    const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st);
 
-// The backward kernel alone (no zeroing, no convert) without a mask or dropout, on
-// 128-query tiles (fa_bwd_wide.cu; d = 64 or 128): dQacc must be zero on entry and receives
-// the unscaled fp32 dQ sums.
+// What a backward call adds to plain attention: an additive bf16 mask or a packed boolean
+// mask (pointer and strides, as for tc_fwd_masked / tc_fwd_bitmask), or dropout (Philox key
+// and keep threshold, as for tc_fwd_dropout).
+struct BwdVariant {
+  int kind = 0;  // 0 plain, 1 additive mask, 2 dropout, 3 boolean mask (packed bits)
+  const void* mask = nullptr;
+  int64_t sb = 0, sh = 0, srow = 0;
+  uint64_t seed = 0;
+  uint32_t threshold = 0;
+};
+
+// The backward kernel alone (no zeroing, no convert), on 128-query tiles (fa_bwd_wide.cu;
+// d = 64 or 128): dQacc must be zero on entry and receives the unscaled fp32 dQ sums.
 cudaError_t tc_bwd_wide(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                         const float* Dv, void* dK, void* dV, float* dQacc, const Shape& s, float scale, bool causal,
-                        int* status, cudaStream_t st);
+                        const BwdVariant& var, int* status, cudaStream_t st);
 
 // The backward with the additive mask of tc_fwd_masked.
 cudaError_t tc_bwd_masked(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
