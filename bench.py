@@ -223,6 +223,56 @@ class _Named:
         self.name = name
 
 
+L2_BYTES = 129e6  # GB300 L2 (nominal)
+
+
+def l2_plan(working_bytes):
+    """Whether timed steps flush L2 first: only when the step's data could stay resident
+    between steps (less than twice the L2); returns (flush, note for the config)."""
+    if working_bytes >= 2 * L2_BYTES:
+        return False, f"no flush: the step's tensors ({working_bytes / 1e6:.0f} MB) exceed twice the 129 MB L2"
+    return True, (f"L2 flushed before every timed step (a 256 MB write, outside the events): the step's "
+                  f"tensors ({working_bytes / 1e6:.0f} MB) are under twice the 129 MB L2")
+
+
+def clocked_loop(step, steps, soak_s, flush=None):
+    """Runs `step` for soak_s seconds untimed while the clock sampler starts, then `steps`
+    timed steps on the current stream; returns (ms per step, clock record). With `flush`, it
+    runs before every timed step and the time is the sum of the steps' own events."""
+    import torch
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < soak_s:
+        for _ in range(8):
+            step()
+        torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for e0, e1 in ev:
+        if flush is not None:
+            flush()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if flush is not None:
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+    else:
+        ms = a.elapsed_time(b) / steps
+    return ms, dict(clk, window=f"{soak_s:.1f} s of untimed steps, then the timed region")
+
+
 def recorded_traffic(kernel, w):
     """DRAM bytes per launch from profiles/traffic.json, if recorded for this workload and the
     kernel's sources are unchanged since the capture; else None."""
@@ -274,6 +324,11 @@ def run_ours(args, w):
     ws_bytes = fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d, tdt)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    esz = 2 if w.dtype == "bf16" else 4
+    # Q, K, V, O, dO, dQ, dK, dV, the fp32 dQ accumulator, LSE and D
+    working = 8 * w.B * w.H * w.N * w.d * esz + w.B * w.H * w.N * w.d * 4 + 2 * w.B * w.H * w.N * 4
+    flush_l2, l2_note = l2_plan(working)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush_l2 else None
 
     def fwd():
         fa.fa_fwd(q, k, v, w.causal, w.scale, o=o, lse=lse)
@@ -325,6 +380,8 @@ def run_ours(args, w):
     t_start.record(stream)
     for i in range(args.steps):
         e = ev[i]
+        if flush_l2:
+            flush_buf.zero_()
         e[0].record(stream)
         fwd()
         e[1].record(stream)
@@ -337,7 +394,10 @@ def run_ours(args, w):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ms = t_start.elapsed_time(t_end) / args.steps
+    if flush_l2:  # the steps' own time, without the flushes between them
+        ms = statistics.mean(e[0].elapsed_time(e[3]) for e in ev)
+    else:
+        ms = t_start.elapsed_time(t_end) / args.steps
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
@@ -396,7 +456,6 @@ def run_ours(args, w):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "path": e2e_path}
         e2e_out = out_host
 
-    esz = 2 if w.dtype == "bf16" else 4
     rows = w.B * w.H * w.N
     pre_bytes = 2 * rows * w.d * esz + rows * 4
     kern = {"fa_fwd": fwd_ms, "fa_bwd": bwd_ms, "fa_bwd_preprocess": pre_ms}
@@ -436,7 +495,7 @@ def run_ours(args, w):
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "scale": w.scale, "parallelism": f"replicas x{world} (heads independent, no collective)",
-                   "l2": "no flush: the 8 [B,H,N,d] tensors (537 MB) exceed the 129 MB L2"},
+                   "l2": l2_note},
         "fwd": {"ms": fwd_ms, "tflops": w.fwd_flop() / (fwd_ms * 1e-3) / 1e12},
         "bwd": {"ms": pre_ms + bwd_ms, "tflops": w.bwd_flop() / ((pre_ms + bwd_ms) * 1e-3) / 1e12,
                 "note": "preprocess + fa_bwd"},
@@ -506,15 +565,11 @@ def run_splitkv(args):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(args.steps):
-        step()
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.steps
-    peaks, src = load_peaks()
     nbytes = 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
+    flush_l2, l2_note = l2_plan(nbytes)
+    fbuf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush_l2 else None
+    ms, clk = clocked_loop(step, args.steps, args.soak_s, flush=fbuf.zero_ if flush_l2 else None)
+    peaks, src = load_peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
     flop = 4.0 * B * H * Nq * Nk * d
     workload = f"splitkv_b{B}h{H}_q{Nq}_k{Nk}_d{d}" + ("_causal" if c else "")
@@ -526,8 +581,9 @@ def run_splitkv(args):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload,
                    "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": bool(c),
-                   "l2": "no flush: K and V exceed the 129 MB L2" if 2 * B * H * Nk * d * 2 > 129e6 else "fits L2"},
+                   "l2": l2_note},
         "tflops": flop / (ms * 1e-3) / 1e12,
+        "clocks": clk,
         "roofline": {"kernel": kernel, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "peak_source": f"HBM copy ({src})",
                      "traffic": recorded_traffic(kernel, _Named(workload))},
@@ -562,19 +618,15 @@ def run_fp8(args):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(args.steps):
-        step()
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.steps
+    in_bytes = 3 * B * H * N * d
+    flush_l2, l2_note = l2_plan(in_bytes + B * H * N * d * 2 + B * H * N * 4)
+    fbuf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush_l2 else None
+    ms, clk = clocked_loop(step, args.steps, args.soak_s, flush=fbuf.zero_ if flush_l2 else None)
     peaks, src = load_peaks()
     flop = 4.0 * B * H * N * N * d / (2 if c else 1)
     tf = flop / (ms * 1e-3) / 1e12
     peak = 2 * peaks["bf16_tflops"]
     peak_sus = 2 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    in_bytes = 3 * B * H * N * d
     workload = f"fp8_b{B}h{H}_n{N}_d{d}" + ("_causal" if c else "")
     print(json.dumps({
         "metric": "attention fwd TFLOP/s on e4m3 inputs (fa_fwd_fp8)", "value": tf, "unit": "TFLOP/s",
@@ -582,11 +634,12 @@ def run_fp8(args):
         "data": "synthetic",
         "config": {"workload": workload, "B": B, "H": H, "N": N,
                    "d": d, "causal": bool(c),
-                   "l2": "no flush: inputs and output exceed the 129 MB L2" if in_bytes * 3 > 129e6 else "fits L2"},
+                   "l2": l2_note},
         "roofline": {"kernel": "fa_fwd_tc_kernel<128, e4m3>", "bound": "tensor", "achieved": tf, "peak": peak,
                      "unit": "TFLOP/s", "frac": tf / peak, "frac_sustained": tf / peak_sus,
                      "peak_source": f"2 x dense bf16 burst ({src}); nominal fp8/bf16 ratio",
                      "traffic": recorded_traffic("fa_fwd_fp8", _Named(workload))},
+        "clocks": clk,
         "gpu_launches": args.steps, "kernels_per_step": fa.FP8_KERNELS,
     }), flush=True)
     return 0

@@ -26,7 +26,7 @@ BF16_KERNEL_BOUND = {"fa_fwd": "tensor", "fa_bwd": "tensor", "fa_bwd_preprocess"
 # Kernels each entry point launches, in order (the dQ accumulator clear in fa_bwd is a
 # cudaMemsetAsync, not a library kernel).
 BF16_KERNELS = {"fa_fwd": ["fa_fwd_tc_kernel"], "fa_bwd_preprocess": ["preprocess_kernel"],
-                "fa_bwd": ["fa_bwd_tc_kernel", "dq_convert_kernel"]}
+                "fa_bwd": ["fa_bwd_wide_kernel", "dq_convert_kernel"]}
 SPLITKV_KERNELS = ["splitkv_tc_kernel", "splitkv_merge_kernel"]
 FP8_KERNELS = ["fa_fwd_tc_kernel"]  # the e4m3 instance of the forward kernel
 FP32_KERNELS = {"fa_fwd": ["simt_fwd_kernel"], "fa_bwd_preprocess": ["preprocess_kernel"],

@@ -17,7 +17,12 @@
 // on tile 1, and the other way round.
 //
 // TMEM (512 columns x 128 lanes): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
-// O_1 [256+d, 256+2d). P_t (bf16 pairs) overwrites the first 64 columns of S_t.
+// O_1 [256+d, 256+2d). At d = 128 P_t (bf16 pairs) overwrites the first 64 columns of S_t,
+// so S_t(j+1) waits for PV_t(j), and each Q tile's chain per K tile is softmax, then PV and
+// S on the tensor core, then softmax again. At d = 64 the 128 columns left over hold P_0
+// [384,448) and P_1 [448,512): the softmax warps release S_t as soon as they have loaded it,
+// S_t(j+1) runs while they exponentiate S_t(j), and PV_t(j) needs only finish before
+// P_t(j+1) is stored (or O_t rescaled), so the tensor core leaves the softmax's chain.
 //
 // Lazy rescale: O and l are rescaled only when the row max grows by more than 8 (log2
 // units); otherwise P uses the stale max (values <= 2^8). The result is exact because
@@ -103,6 +108,9 @@ struct FwdCfg {
   static_assert(kSmemBytes + 256 <= 227 * 1024, "shared memory per CTA");
   __device__ static constexpr uint32_t colS(int t) { return t ? 128u : 0u; }
   __device__ static constexpr uint32_t colO(int t) { return t ? 256u + D : 256u; }
+  // P in columns of its own (d = 64: 2 x (128 S + 64 O + 64 P) = 512 columns)
+  static constexpr bool kSepP = D == 64 && !F8;
+  __device__ static constexpr uint32_t colP(int t) { return kSepP ? 384u + 64u * t : colS(t); }
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -138,6 +146,7 @@ struct FwdCtl {
   uint64_t q_full;
   uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t s_free[2], pv_done[2];  // P in columns of its own: S_t loaded; PV_t(j) retired
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -208,6 +217,8 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       mbar_init(&ctl.s_full[t], 1);
       mbar_init(&ctl.p_full[t], 128);
       mbar_init(&ctl.o_full[t], 1);
+      mbar_init(&ctl.s_free[t], 128);
+      mbar_init(&ctl.pv_done[t], 1);
     }
     mbar_init(&ctl.drain, 1);
     ctl.abort = 0;
@@ -290,10 +301,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int k = 0; k < C::kPVSteps; ++k) {
           if constexpr (F8)
-            mma_ts_f8(tmem + C::colO(t), tmem + C::colS(t) + k * 8, sdesc_add(dV0, vo + k * C::kKStep * 128), idO,
+            mma_ts_f8(tmem + C::colO(t), tmem + C::colP(t) + k * 8, sdesc_add(dV0, vo + k * C::kKStep * 128), idO,
                       (acc || k > 0) ? 1u : 0u);
           else
-            mma_ts(tmem + C::colO(t), tmem + C::colS(t) + k * 8, sdesc_add(dV0, vo + k * C::kKStep * 128), idO,
+            mma_ts(tmem + C::colO(t), tmem + C::colP(t) + k * 8, sdesc_add(dV0, vo + k * C::kKStep * 128), idO,
                    (acc || k > 0) ? 1u : 0u);
         }
       };
@@ -312,8 +323,38 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
       for (int j = 0; ok && j < nkv; ++j) {
         const int s = j % C::kVStages;
-        ok = mbar_wait(&ctl.v_full[s], (j / C::kVStages) & 1, p.status, abort);
         bool k_next = false;
+        if constexpr (C::kSepP) {
+          // S_t(j+1) as soon as the softmax warps have loaded S_t(j); PV_t(j) once P_t(j) is in
+          for (int t = 0; ok && t < 2; ++t) {
+            const int nk = t ? nkv1 : nkv0;
+            if (j + 1 < nk) {
+              if (!(ok = mbar_wait(&ctl.s_free[t], j & 1, p.status, abort))) break;
+              if (!k_next) {
+                const int s2 = (j + 1) % C::kKStages;
+                if (!(ok = mbar_wait(&ctl.k_full[s2], ((j + 1) / C::kKStages) & 1, p.status, abort))) break;
+                k_next = true;
+              }
+              tc_fence_after();
+              issue_S(t, (j + 1) % C::kKStages);
+              mma_commit(&ctl.s_full[t]);
+            }
+            if (j < nk) {
+              if (t == 0 || j >= nkv0) {  // V_j lands once, before the first PV that reads it
+                if (!(ok = mbar_wait(&ctl.v_full[s], (j / C::kVStages) & 1, p.status, abort))) break;
+              }
+              if (!(ok = mbar_wait(&ctl.p_full[t], j & 1, p.status, abort))) break;
+              tc_fence_after();
+              issue_PV(t, s, j > 0);
+              mma_commit(&ctl.pv_done[t]);
+              if (j + 1 == nk) mma_commit(&ctl.o_full[t]);
+            }
+          }
+          if (k_next) mma_commit(&ctl.k_empty[(j + 1) % C::kKStages]);  // every S of K_{j+1} issued
+          mma_commit(&ctl.v_empty[s]);
+          continue;
+        }
+        ok = mbar_wait(&ctl.v_full[s], (j / C::kVStages) & 1, p.status, abort);
         for (int t = 0; ok && t < 2; ++t) {
           const int nk = t ? nkv1 : nkv0;
           if (j >= nk) continue;
@@ -349,6 +390,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::colS(t);
     const uint32_t tO = tmem + lane_off + C::colO(t);
+    const uint32_t tP = tmem + lane_off + C::colP(t);
     const float sl2 = p.sl2;
     float m = -INFINITY, l = 0.f;
     bool ok = nk > 0;
@@ -417,6 +459,10 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           }
         }
       }
+      if constexpr (C::kSepP) {  // S_t is in registers: the next S may overwrite it
+        tc_fence_before();
+        mbar_arrive(&ctl.s_free[t]);
+      }
       // kBits: keys whose bit is clear are hidden. (Skipping this for tiles whose bits are
       // all set measured 17% slower: the branch costs registers the loop needs.)
       if constexpr (kBits) {
@@ -452,6 +498,11 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       const float m_new = fmaxf(m, mx * sl2);
       const bool grow = m_new > m + C::kThreshold;
+      if (C::kSepP && j > 0) {  // PV_t(j-1) must have read P_t and added into O_t
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.pv_done[t], (j - 1) & 1, p.status, abort));
+        if (!ok) break;
+        tc_fence_after();
+      }
       if (__any_sync(0xffffffffu, grow)) {
         const float corr = grow ? ex2(m - m_new) : 1.f;
         l *= corr;
@@ -497,7 +548,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               pk[u] = pack_bf16(pr.x, pr.y);
             }
           }
-          tmem_st16(tS + 16 * q, pk);
+          tmem_st16(tP + 16 * q, pk);
         }
       } else {
 #pragma unroll
@@ -514,7 +565,7 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             rs1 = fadd2(rs1, p1);
             pk[u] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
           }
-          tmem_st16(tS + 16 * q, pk);
+          tmem_st16(tP + 16 * q, pk);
         }
       }
       l += (rs0.x + rs0.y) + (rs1.x + rs1.y);
