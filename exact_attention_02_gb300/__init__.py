@@ -94,6 +94,10 @@ def _load():
     L.fa_get_last_device_status.restype = i
     L.fa_test_inject_timeout.argtypes = [i, ctypes.c_ulonglong]
     L.fa_test_inject_timeout.restype = i
+    L.fa_set_bwd_dq_mode.argtypes = [i]
+    L.fa_set_bwd_dq_mode.restype = i
+    L.fa_get_bwd_dq_mode.argtypes = []
+    L.fa_get_bwd_dq_mode.restype = i
     _lib = L
     return L
 
@@ -433,6 +437,19 @@ def fa_fwd_bwd_host(q, k, v, do, causal: bool, scale: float | None = None, out=N
 
 def fa_get_last_device_status() -> int:
     return int(_load().fa_get_last_device_status())
+
+
+# How the bf16 backward computes dQ (``fa_set_bwd_dq_mode`` in fa.h): chosen by shape,
+# atomic fp32 partials, or the separate dQ pass.
+FA_BWD_DQ_AUTO, FA_BWD_DQ_ATOMIC, FA_BWD_DQ_SEPARATE = 0, 1, 2
+
+
+def fa_set_bwd_dq_mode(mode: int) -> None:
+    _check(_load().fa_set_bwd_dq_mode(int(mode)), "fa_set_bwd_dq_mode")
+
+
+def fa_get_bwd_dq_mode() -> int:
+    return int(_load().fa_get_bwd_dq_mode())
 
 
 # Failure-path test hook (see ``fa_test_inject_timeout`` in fa.h): which = 1 makes the

@@ -419,6 +419,14 @@ extern "C" fa_status_t fa_get_last_device_status(void) {
   return v == 0 ? FA_OK : static_cast<fa_status_t>(v);
 }
 
+extern "C" fa_status_t fa_set_bwd_dq_mode(int mode) {
+  if (mode != FA_BWD_DQ_AUTO && mode != FA_BWD_DQ_ATOMIC && mode != FA_BWD_DQ_SEPARATE) return FA_ERR_INVALID_ARG;
+  fa::set_bwd_dq_mode(mode);
+  return FA_OK;
+}
+
+extern "C" int fa_get_bwd_dq_mode(void) { return fa::bwd_dq_mode(); }
+
 extern "C" fa_status_t fa_test_inject_timeout(int which, unsigned long long wait_limit_ns) {
   if (which != 0 && which != fa::ptx::kInjectFwd && which != fa::ptx::kInjectBwd) return FA_ERR_INVALID_ARG;
   int* p = fa::device_status_ptr();

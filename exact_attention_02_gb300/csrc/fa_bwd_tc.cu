@@ -1,11 +1,17 @@
-// The backward entry functions of the tensor-core path: each zeroes the fp32 dQ accumulator,
-// runs the backward kernel (fa_bwd_wide.cu) and converts the accumulator to bf16 dQ; what
-// they compute is fa_bwd / fa_bwd_masked / fa_bwd_bitmask / fa_bwd_dropout in include/fa.h.
+// The backward entry functions of the tensor-core path; what they compute is fa_bwd /
+// fa_bwd_masked / fa_bwd_bitmask / fa_bwd_dropout in include/fa.h.
 //
-// dQ is a sum over key tiles, and every key tile is a different CTA: the kernel adds each
-// tile's fp32 partial into the accumulator, and one pass here scales it by `scale` and
-// rounds it to bf16 once ("FlashAttention 反向传播" 踩坑三: fp32 accumulators, a single cast at
-// write-back).
+// dQ is a sum over key tiles, and the 128-key-tile kernel (fa_bwd_wide.cu) gives every key
+// tile its own CTA. It computes dQ in one of two ways ("FlashAttention 反向传播" 踩坑二 weighs
+// them; both keep fp32 sums and cast to bf16 once, as its 踩坑三 asks):
+//   atomic:   each CTA adds its fp32 dQ partials into an accumulator in the workspace; the
+//             entry function zeroes it first and one pass here scales it by `scale` and
+//             rounds it to bf16 (the masked and dropout instances always take this way);
+//   separate: the 128-key-tile kernel gives dK and dV only, and a second kernel over
+//             128-query tiles (fa_bwd_dq.cu) recomputes S and dP and accumulates dQ in TMEM.
+// fa_set_bwd_dq_mode picks one; by default the atomic way runs (see separate_dq below).
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -32,6 +38,17 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
   reinterpret_cast<uint4*>(dq)[i] = w;
 }
 
+std::atomic<int> g_dq_mode{FA_BWD_DQ_AUTO};
+
+// The dQ mode for a plain backward. FA_BWD_DQ_AUTO takes the atomic way at every shape: on
+// GB300 (preprocess + backward, both modes in one process) the separate pass measured 1.682
+// against 1.323 ms at B2 H16 N8192 d128 causal, 1.080 against 0.901 ms at B16 H32 N1024
+// d128, 0.387 against 0.304 ms at B4 H16 N2048 d64, 6.136 against 4.766 ms at B1 H8 N32768
+// d128 causal and 0.226 against 0.186 ms at B4 H16 N2048 d64 causal. Dropping the dQ
+// partials saves the 128-key-tile kernel about a fifth of its time, less than the second
+// pass costs, which recomputes S and dP.
+bool separate_dq() { return g_dq_mode.load(std::memory_order_relaxed) == FA_BWD_DQ_SEPARATE; }
+
 cudaError_t run_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE, const float* Dv,
                     void* dQ, void* dK, void* dV, float* dQacc, const Shape& s, float scale, bool causal,
                     const BwdVariant& var, int* status, cudaStream_t st) {
@@ -46,9 +63,17 @@ cudaError_t run_bwd(const void* Q, const void* K, const void* V, const void* dO,
 
 }  // namespace
 
+int bwd_dq_mode() { return g_dq_mode.load(std::memory_order_relaxed); }
+void set_bwd_dq_mode(int mode) { g_dq_mode.store(mode, std::memory_order_relaxed); }
+
 cudaError_t tc_bwd(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                    const float* D, void* dQ, void* dK, void* dV, float* dQacc, const Shape& s,
                    float scale, bool causal, int* status, cudaStream_t st) {
+  if (separate_dq()) {
+    cudaError_t e = tc_bwd_wide(Q, K, V, dO, LSE, D, dK, dV, nullptr, s, scale, causal, BwdVariant{}, status, st);
+    if (e != cudaSuccess) return e;
+    return tc_bwd_dq(Q, K, V, dO, LSE, D, dQ, s, scale, causal, status, st);
+  }
   return run_bwd(Q, K, V, dO, LSE, D, dQ, dK, dV, dQacc, s, scale, causal, BwdVariant{}, status, st);
 }
 

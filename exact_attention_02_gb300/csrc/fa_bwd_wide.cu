@@ -165,8 +165,10 @@ __device__ __forceinline__ uint32_t packed_col(uint32_t base, int k) { return ba
 // 10 warps put at most 3 warps on each of the SM's four sub-partitions (16 K registers each),
 // which allows 168 registers per thread: a softmax thread holds its 64 weights from phase A
 // to phase B and, between the two, a 64-column row of the dQ partial.
-// kVar: 0 plain, 1 additive mask, 2 dropout, 3 boolean mask (packed bits).
-template <int D, bool kTail, int kVar>
+// kVar: 0 plain, 1 additive mask, 2 dropout, 3 boolean mask (packed bits). kDQ: the dQ^T
+// partials are computed and added into the accumulator; without them the kernel gives dK and
+// dV only, and the separate dQ pass (fa_bwd_dq.cu) gives dQ.
+template <int D, bool kTail, int kVar, bool kDQ>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -393,14 +395,18 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tc_fence_after();
         issue_dK(it, s);
         mma_commit(&ctl.q_empty[s]);
-        issue_dQ();
-        mma_commit(&ctl.dq_full);
+        if constexpr (kDQ) {
+          issue_dQ();
+          mma_commit(&ctl.dq_full);
+        }
         if (next) {
           if (!(ok = mbar_wait(&ctl.p_done, (it + 1) & 1, p.status, abort))) break;
           tc_fence_after();
           issue_dV(it + 1, s1);
           // dP(i+1) once the dQ warps have read the dQ^T(i) partial out of its columns
-          if (!(ok = mbar_wait(&ctl.dq_empty, it & 1, p.status, abort))) break;
+          if constexpr (kDQ) {
+            if (!(ok = mbar_wait(&ctl.dq_empty, it & 1, p.status, abort))) break;
+          }
           if (!(ok = mbar_wait(&ctl.do_full[s1], par1, p.status, abort))) break;
           tc_fence_after();
           issue_dP(s1);
@@ -589,7 +595,9 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       tc_fence_before();
       mbar_arrive(&ctl.p_done);
       // ---- the previous tile's dQ^T partial, while dK/dQ of that tile and dV of this one run
-      if (it > 0 && !(ok = read_out_dq(it - 1))) break;
+      if constexpr (kDQ) {
+        if (it > 0 && !(ok = read_out_dq(it - 1))) break;
+      }
       // ---- phase B: dS^T = P^T * (dP^T - D), to shared memory only
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dp_full, it & 1, p.status, abort));
       if (!ok) break;
@@ -630,7 +638,9 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_arrive(&ctl.ds_done);
       flush_held(1);
     }
-    if (ok) ok = read_out_dq(nq - 1);
+    if constexpr (kDQ) {
+      if (ok) ok = read_out_dq(nq - 1);
+    }
     if (ok) {
       flush_held(0);
       flush_held(1);
@@ -682,7 +692,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   }
 }
 
-template <int D, int kVar>
+template <int D, int kVar, bool kDQ>
 cudaError_t launch_wide(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                         const float* Dv, void* dK, void* dV, float* dQacc, const Shape& s, float scale, bool causal,
                         const BwdVariant& var, int* status, cudaStream_t st) {
@@ -693,9 +703,9 @@ cudaError_t launch_wide(const void* Q, const void* K, const void* V, const void*
       !make_map_bf16_3d(&mv, V, heads, s.keys(), D, BN) || !make_map_bf16_3d(&mdo, dO, heads, s.N, D, BQ))
     return cudaErrorInvalidValue;
   static bool attr = [] {
-    return cudaFuncSetAttribute(fa_bwd_wide_kernel<D, false, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                C::kSmemBytes) == cudaSuccess &&
-           cudaFuncSetAttribute(fa_bwd_wide_kernel<D, true, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(fa_bwd_wide_kernel<D, false, kVar, kDQ>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) == cudaSuccess &&
+           cudaFuncSetAttribute(fa_bwd_wide_kernel<D, true, kVar, kDQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes) == cudaSuccess;
   }();
   if (!attr) return cudaErrorInvalidConfiguration;
@@ -728,9 +738,9 @@ cudaError_t launch_wide(const void* Q, const void* K, const void* V, const void*
   pv.drop_scale = (float)(256.0 / (256.0 - (double)var.threshold));
   const int64_t grid = (int64_t)p.kvtiles * p.heads;
   if (s.N % BQ != 0 || s.keys() % BN != 0)
-    fa_bwd_wide_kernel<D, true, kVar><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p, pv);
+    fa_bwd_wide_kernel<D, true, kVar, kDQ><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p, pv);
   else
-    fa_bwd_wide_kernel<D, false, kVar><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p, pv);
+    fa_bwd_wide_kernel<D, false, kVar, kDQ><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p, pv);
   return cudaGetLastError();
 }
 
@@ -738,11 +748,15 @@ template <int D>
 cudaError_t launch_wide_var(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                             const float* Dv, void* dK, void* dV, float* dQacc, const Shape& s, float scale,
                             bool causal, const BwdVariant& var, int* status, cudaStream_t st) {
+  if (!dQacc) {  // dK and dV only: the plain instance; dQ comes from the separate pass
+    if (var.kind != 0) return cudaErrorInvalidValue;
+    return launch_wide<D, 0, false>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
+  }
   switch (var.kind) {
-    case 0: return launch_wide<D, 0>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
-    case 1: return launch_wide<D, 1>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
-    case 2: return launch_wide<D, 2>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
-    case 3: return launch_wide<D, 3>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
+    case 0: return launch_wide<D, 0, true>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
+    case 1: return launch_wide<D, 1, true>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
+    case 2: return launch_wide<D, 2, true>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
+    case 3: return launch_wide<D, 3, true>(Q, K, V, dO, LSE, Dv, dK, dV, dQacc, s, scale, causal, var, status, st);
   }
   return cudaErrorInvalidValue;
 }

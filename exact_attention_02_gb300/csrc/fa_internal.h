@@ -97,10 +97,21 @@ struct BwdVariant {
 };
 
 // The backward kernel alone (no zeroing, no convert), on 128-query tiles (fa_bwd_wide.cu;
-// d = 64 or 128): dQacc must be zero on entry and receives the unscaled fp32 dQ sums.
+// d = 64 or 128): dQacc must be zero on entry and receives the unscaled fp32 dQ sums. With
+// dQacc null (plain attention only) it computes dK and dV alone.
 cudaError_t tc_bwd_wide(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                         const float* Dv, void* dK, void* dV, float* dQacc, const Shape& s, float scale, bool causal,
                         const BwdVariant& var, int* status, cudaStream_t st);
+
+// The separate dQ pass (fa_bwd_dq.cu; d = 64 or 128, plain attention): dQ in bf16, written
+// directly, from the same inputs as tc_bwd_wide.
+cudaError_t tc_bwd_dq(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                      const float* Dv, void* dQ, const Shape& s, float scale, bool causal, int* status,
+                      cudaStream_t st);
+
+// How tc_bwd computes dQ (fa_set_bwd_dq_mode): FA_BWD_DQ_AUTO, _ATOMIC or _SEPARATE.
+int bwd_dq_mode();
+void set_bwd_dq_mode(int mode);
 
 // The backward with the additive mask of tc_fwd_masked.
 cudaError_t tc_bwd_masked(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,

@@ -104,6 +104,28 @@ FA_API fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const voi
                    void* stream);
 
 /*
+ * fa_set_bwd_dq_mode / fa_get_bwd_dq_mode — how the bf16 backward without mask or dropout
+ * (fa_bwd, fa_bwd_rect, fa_bwd_noalloc) computes dQ, the one gradient that sums over key
+ * tiles ("FlashAttention 反向传播" 踩坑二: one recompute per tile for all three gradients, or
+ * a second pass for dQ; "flash-attention-v2-sram-tiling" §7 counts the cost of split
+ * sums). Both modes keep fp32 sums and round to bf16 once (踩坑三); they agree to bf16
+ * rounding, not bit for bit.
+ *   FA_BWD_DQ_ATOMIC   (1): each 128-key tile adds its fp32 dQ partials into the workspace
+ *                           with atomic additions, then one pass scales and rounds them.
+ *   FA_BWD_DQ_SEPARATE (2): dK and dV from the key-tile kernel alone, then a kernel over
+ *                           128-query tiles recomputes S and dP and accumulates dQ on chip;
+ *                           dQ does not depend on the order of any additions.
+ *   FA_BWD_DQ_AUTO     (0, the default): the atomic mode, the faster of the two at every
+ *                           shape measured on GB300 (the separate pass costs 19-29% more).
+ * The setting is process-wide and applies to calls made after it; masked and dropout
+ * backward calls always use the atomic mode. fa_set_bwd_dq_mode returns
+ * FA_ERR_INVALID_ARG for any other value; fa_get_bwd_dq_mode returns the setting.
+ */
+typedef enum { FA_BWD_DQ_AUTO = 0, FA_BWD_DQ_ATOMIC = 1, FA_BWD_DQ_SEPARATE = 2 } fa_bwd_dq_mode_t;
+FA_API fa_status_t fa_set_bwd_dq_mode(int mode);
+FA_API int fa_get_bwd_dq_mode(void);
+
+/*
  * fa_fwd_rect / fa_bwd_rect — fa_fwd / fa_bwd with Nq query rows against Nk key/value rows
  * per head (cross-attention, or a prefill of Nq new tokens that continues a cached prefix
  * of Nk - Nq tokens: "flash-attention-v2-sram-tiling" 场景二 serves long documents against

@@ -55,14 +55,18 @@ def _parity_after(w, x, dev):
         assert np.linalg.norm(got[n] - ref[n]) / np.linalg.norm(ref[n]) <= 2e-2, n
 
 
-@pytest.mark.parametrize("which", ["fwd", "bwd"])
+@pytest.mark.parametrize("which", ["fwd", "bwd", "bwd_separate_dq"])
 def test_wait_that_runs_out_reports_timeout_and_the_context_survives(which):
+    """bwd_separate_dq: the backward in the separate dQ mode, where both of its kernels (dK/dV
+    and dQ) skip their first Q arrival in CTA 0."""
     w, x, dev = _inputs()
     q, k, v, do = dev
     o, lse = fa.fa_fwd(q, k, v, w.causal, w.scale)
     torch.cuda.synchronize()
     assert fa.fa_get_last_device_status() == fa.FA_OK  # a clean word to start from
     try:
+        if which == "bwd_separate_dq":
+            fa.fa_set_bwd_dq_mode(fa.FA_BWD_DQ_SEPARATE)
         fa.fa_test_inject_timeout(fa.FA_INJECT_FWD if which == "fwd" else fa.FA_INJECT_BWD, LIMIT_NS)
         t0 = time.perf_counter()
         if which == "fwd":
@@ -73,6 +77,7 @@ def test_wait_that_runs_out_reports_timeout_and_the_context_survives(which):
         elapsed = time.perf_counter() - t0
     finally:
         fa.fa_test_inject_timeout(fa.FA_INJECT_OFF, 0)
+        fa.fa_set_bwd_dq_mode(fa.FA_BWD_DQ_AUTO)
     # it gave up after the short limit, long before the default of 4 s
     assert elapsed < 1.0, elapsed
     assert fa.fa_get_last_device_status() == fa.FA_ERR_DEVICE_TIMEOUT
