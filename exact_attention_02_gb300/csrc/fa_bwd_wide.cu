@@ -400,15 +400,16 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           mma_commit(&ctl.dq_full);
         }
         if (next) {
+          // dV(i+1) reads P^T(i+1) from TMEM and dO(i+1) from its stage: both must be in
           if (!(ok = mbar_wait(&ctl.p_done, (it + 1) & 1, p.status, abort))) break;
-          tc_fence_after();
-          issue_dV(it + 1, s1);
-          // dP(i+1) once the dQ warps have read the dQ^T(i) partial out of its columns
-          if constexpr (kDQ) {
-            if (!(ok = mbar_wait(&ctl.dq_empty, it & 1, p.status, abort))) break;
-          }
           if (!(ok = mbar_wait(&ctl.do_full[s1], par1, p.status, abort))) break;
           tc_fence_after();
+          issue_dV(it + 1, s1);
+          // dP(i+1) once the softmax warps have read the dQ^T(i) partial out of its columns
+          if constexpr (kDQ) {
+            if (!(ok = mbar_wait(&ctl.dq_empty, it & 1, p.status, abort))) break;
+            tc_fence_after();
+          }
           issue_dP(s1);
           mma_commit(&ctl.dp_full);
           mma_commit(&ctl.do_empty[s1]);  // dV(i+1) and dP(i+1), the readers of dO(i+1), issued

@@ -178,3 +178,24 @@ def test_rect_rejects_mismatched_shapes():
         fa.fa_fwd_rect(q, k, k[:, :, :100], True)
     with pytest.raises(ValueError):
         fa.fa_fwd_rect(q, k[..., :32].contiguous(), k[..., :32].contiguous(), True)
+
+
+@pytest.mark.parametrize("case", [(1, 1, 1000, 32768, 64, True), (1, 2, 1000, 8192, 128, True),
+                                  (2, 4, 2048, 2048, 64, False), (1, 4, 4096, 4096, 128, True)],
+                         ids=lambda c: "q{}k{}d{}{}".format(*c[2:5], "c" if c[5] else ""))
+def test_dk_dv_identical_across_runs(case):
+    """dK and dV take no atomic additions: four calls on the same inputs must agree bit for bit.
+    A product that read a shared-memory stage before its copy landed would show up here as a
+    run-to-run difference (dQ sums fp32 partials atomically, so only it may differ)."""
+    B, H, Nq, Nk, d, causal = case
+    x = _inputs(B, H, Nq, Nk, d, "bf16", seed=Nq + Nk + d)
+    q, k, v, do = (_dev(x[n], "bf16") for n in ("q", "k", "v", "do"))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fa_fwd_rect(q, k, v, causal, scale)
+    D = fa.fa_bwd_preprocess(o, do)
+    first = fa.fa_bwd_rect(q, k, v, o, do, lse, causal, scale, D=D)
+    for _ in range(3):
+        again = fa.fa_bwd_rect(q, k, v, o, do, lse, causal, scale, D=D)
+        torch.cuda.synchronize()
+        assert torch.equal(first[1], again[1]) and torch.equal(first[2], again[2])
+    assert fa.fa_get_last_device_status() == fa.FA_OK
