@@ -325,30 +325,31 @@ fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const int s = j % C::kVStages;
         bool k_next = false;
         if constexpr (C::kSepP) {
-          // S_t(j+1) as soon as the softmax warps have loaded S_t(j); PV_t(j) once P_t(j) is in
+          // S_0(j+1) and S_1(j+1) as soon as each softmax warpgroup has loaded its S(j), then
+          // PV_0(j) and PV_1(j) once P(j) is in: the order in which those events come, so that
+          // neither warpgroup's next S waits for the other's softmax
           for (int t = 0; ok && t < 2; ++t) {
             const int nk = t ? nkv1 : nkv0;
-            if (j + 1 < nk) {
-              if (!(ok = mbar_wait(&ctl.s_free[t], j & 1, p.status, abort))) break;
-              if (!k_next) {
-                const int s2 = (j + 1) % C::kKStages;
-                if (!(ok = mbar_wait(&ctl.k_full[s2], ((j + 1) / C::kKStages) & 1, p.status, abort))) break;
-                k_next = true;
-              }
-              tc_fence_after();
-              issue_S(t, (j + 1) % C::kKStages);
-              mma_commit(&ctl.s_full[t]);
+            if (j + 1 >= nk) continue;
+            if (!(ok = mbar_wait(&ctl.s_free[t], j & 1, p.status, abort))) break;
+            if (!k_next) {
+              const int s2 = (j + 1) % C::kKStages;
+              if (!(ok = mbar_wait(&ctl.k_full[s2], ((j + 1) / C::kKStages) & 1, p.status, abort))) break;
+              k_next = true;
             }
-            if (j < nk) {
-              if (t == 0 || j >= nkv0) {  // V_j lands once, before the first PV that reads it
-                if (!(ok = mbar_wait(&ctl.v_full[s], (j / C::kVStages) & 1, p.status, abort))) break;
-              }
-              if (!(ok = mbar_wait(&ctl.p_full[t], j & 1, p.status, abort))) break;
-              tc_fence_after();
-              issue_PV(t, s, j > 0);
-              mma_commit(&ctl.pv_done[t]);
-              if (j + 1 == nk) mma_commit(&ctl.o_full[t]);
-            }
+            tc_fence_after();
+            issue_S(t, (j + 1) % C::kKStages);
+            mma_commit(&ctl.s_full[t]);
+          }
+          if (ok) ok = mbar_wait(&ctl.v_full[s], (j / C::kVStages) & 1, p.status, abort);
+          for (int t = 0; ok && t < 2; ++t) {
+            const int nk = t ? nkv1 : nkv0;
+            if (j >= nk) continue;
+            if (!(ok = mbar_wait(&ctl.p_full[t], j & 1, p.status, abort))) break;
+            tc_fence_after();
+            issue_PV(t, s, j > 0);
+            mma_commit(&ctl.pv_done[t]);
+            if (j + 1 == nk) mma_commit(&ctl.o_full[t]);
           }
           if (k_next) mma_commit(&ctl.k_empty[(j + 1) % C::kKStages]);  // every S of K_{j+1} issued
           mma_commit(&ctl.v_empty[s]);
