@@ -127,16 +127,17 @@ def cpu_model():
     return platform.machine() or "unknown"
 
 
-def cpu_baseline(w, x, budget_s=12.0, max_heads=8, keep=None):
-    """The oracle, as it stands, on whole heads of the workload until ~budget_s. With
-    ``keep`` (a list), each head's oracle outputs are appended to it as ((b, h), outputs)."""
+def cpu_baseline(w, x, budget_s=12.0, keep=None, keep_max=32):
+    """The oracle, as it stands, on whole heads of the workload until ~budget_s have passed
+    (every head at most once; batches taken in turn). With ``keep`` (a list), the outputs of
+    the first ``keep_max`` heads are appended to it as ((b, h), outputs)."""
     flop_head = (w.fwd_flop() + w.bwd_flop()) / (w.B * w.H)
     t0 = time.perf_counter()
     n = 0
-    while n < max_heads and (time.perf_counter() - t0) < budget_s:
-        b, h = n // w.H % w.B, n % w.H
+    while n < w.B * w.H and (n == 0 or (time.perf_counter() - t0) < budget_s):
+        b, h = n % w.B, n // w.B
         r = oracle_head_step(w, x, b, h)
-        if keep is not None:
+        if keep is not None and len(keep) < keep_max:
             keep.append(((b, h), r))
         n += 1
     dt = time.perf_counter() - t0

@@ -3,10 +3,10 @@
 The keep bits are Philox-4x32-10 on both sides (oracle/philox.py and the kernels'
 philox.cuh, written separately from the same published definition), so the dropped
 attention is the same function of the inputs, and the tolerances are those of every bf16
-test with one derived change: kept weights are multiplied by c = 256 / (256 - t), which
-scales O and every rounding error in it (the bf16 weights, the bf16 output) by c, so O's
-max-abs bound is 2e-2 * c. LSE 1e-3 and dQ/dK/dV relative Frobenius 2e-2 are unchanged
-(LSE is the undropped softmax's; the relative norms do not see the scale). Two tests read the keep
+test: O max-abs 2e-2, LSE 1e-3 (the undropped softmax's), dQ/dK/dV relative Frobenius
+2e-2. Kept weights are multiplied by c = 256 / (256 - t), which scales O and its rounding
+errors (the bf16 weights, the bf16 output) by c, up to 2 at p = 0.5; the bound on O is
+nonetheless not widened by c, and the test records how the error moves with c. Two tests read the keep
 bits of each kernel back exactly: with Q = 0 every visible weight is 1/N, and one-hot V
 (or dO) rows weighted 1 for keys (queries) below 128 and 2 above turn each output element
 into (K1 + 2 K2) c / N, from which both keep bits follow.
@@ -67,9 +67,10 @@ def test_dropout_matches_oracle(case):
             K = philox.keep_matrix(seed, b * H + h, N, N, p)
             ref = ora.head_backward(*(x[b, h].astype(np.float64) for x in (q, k, v, do)), scale, causal,
                                     keep=K, keep_scale=c)
-            # O grows by c with the kept weights, and so does its bf16 rounding: the fixed
-            # bound applies to O / c
-            assert np.abs(got["o"][b, h] - ref["o"]).max() / c <= 2e-2, (b, h)
+            # O grows by c with the kept weights, and so does its bf16 rounding; the bound
+            # stays the fixed one of every bf16 test
+            e_o = np.abs(got["o"][b, h] - ref["o"]).max()
+            assert e_o <= 2e-2, (b, h, "o", e_o, "c", c)
             assert np.abs(got["lse"][b, h] - ref["lse"]).max() <= 1e-3, (b, h)
             for n in ("dq", "dk", "dv"):
                 assert _rel(got[n][b, h], ref[n]) <= 2e-2, (b, h, n, _rel(got[n][b, h], ref[n]))
