@@ -314,6 +314,8 @@ def run_ours(args, w):
     if world > 1:
         dist.barrier()
     fa.lib()
+    fa.fa_set_bwd_dq_mode({"auto": fa.FA_BWD_DQ_AUTO, "atomic": fa.FA_BWD_DQ_ATOMIC,
+                           "separate": fa.FA_BWD_DQ_SEPARATE}[args.dq_mode])
     dev = torch.device("cuda", local)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     x = make_inputs(w)
@@ -352,7 +354,9 @@ def run_ours(args, w):
     launch_source = "CUDA activity profiler"
     if launches is None and not args.no_count:
         # the profiler saw nothing: count by the library's launch sequence instead
-        seq = fa.BF16_KERNELS if w.dtype == "bf16" else fa.FP32_KERNELS
+        seq = dict(fa.BF16_KERNELS) if w.dtype == "bf16" else fa.FP32_KERNELS
+        if w.dtype == "bf16" and args.dq_mode == "separate":
+            seq["fa_bwd"] = ["fa_bwd_wide_kernel", "fa_bwd_dq_kernel"]
         kernel_names = [k for e in ("fa_fwd", "fa_bwd_preprocess", "fa_bwd") for k in seq[e]]
         launches = len(kernel_names)
         launch_source = "library launch sequence (profiler saw no kernels); ncu launch list in profiles/ agrees"
@@ -496,7 +500,7 @@ def run_ours(args, w):
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "scale": w.scale, "parallelism": f"replicas x{world} (heads independent, no collective)",
-                   "l2": l2_note},
+                   "dq_mode": args.dq_mode, "l2": l2_note},
         "fwd": {"ms": fwd_ms, "tflops": w.fwd_flop() / (fwd_ms * 1e-3) / 1e12},
         "bwd": {"ms": pre_ms + bwd_ms, "tflops": w.bwd_flop() / ((pre_ms + bwd_ms) * 1e-3) / 1e12,
                 "note": "preprocess + fa_bwd"},
@@ -664,6 +668,8 @@ def main():
     ap.add_argument("--no-count", action="store_true", help="skip the profiler launch count")
     ap.add_argument("--soak-s", type=float, default=1.0,
                     help="extra untimed steps (seconds) run under the clock sampler before the timed region")
+    ap.add_argument("--dq-mode", choices=["auto", "atomic", "separate"], default="auto",
+                    help="how fa_bwd computes dQ (fa_set_bwd_dq_mode): by default the library's choice")
     args = ap.parse_args()
     from exact_attention_02_gb300.workloads import HEADLINE, WORKLOADS, Workload
     if args.shape:
