@@ -484,7 +484,8 @@ def run_ours(args, w):
     else:
         achieved = pre_bytes / (pre_ms * 1e-3) / 1e9
         peak, unit, peak_desc = peaks["hbm_gbs"], "GB/s", f"HBM copy ({peak_src})"
-    traffic = recorded_traffic(dominant, w)
+    # the records describe the default kernels; another dQ mode runs other kernels
+    traffic = recorded_traffic(dominant, w) if args.dq_mode == "auto" or dominant != "fa_bwd" else None
     roofline = {"kernel": dominant, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "peak_source": peak_desc, "traffic": traffic,
                 "traffic_note": "DRAM bytes per launch from profiles/traffic.json (ncu, scaled by heads)"
