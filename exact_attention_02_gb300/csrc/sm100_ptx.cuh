@@ -34,7 +34,7 @@ struct StatusBlock {
   unsigned long long limit_ns;
 };
 constexpr int kInjectFwd = 1;  // fa_fwd_tc_kernel: CTA 0 never arms its first K stage
-constexpr int kInjectBwd = 2;  // fa_bwd_tc_kernel: CTA 0 never arms its first Q/dO stage
+constexpr int kInjectBwd = 2;  // the backward kernels: CTA 0 never arms its first Q (and dO) load
 
 // The wait limit in force: the test override if one is set, else kWaitLimitNs.
 __device__ __forceinline__ uint64_t wait_limit(const int* status) {
