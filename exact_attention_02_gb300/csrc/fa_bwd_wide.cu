@@ -30,6 +30,11 @@
 //   S(i+1) | dK(i) dQ(i) | dV(i+1) | dP(i+1)
 // so phase A of tile i+1 runs beside dK(i) and dQ(i), the softmax warps read the dQ(i)
 // partial out of the dP^T columns beside dV(i+1), and phase B of tile i+1 runs beside S(i+2).
+// At d = 64 the dQ^T partial has TMEM columns of its own (dV and dK take 64 each, which
+// leaves 128 free), and the separate dQ mode has no dQ product at all: there nothing waits
+// for the dP^T columns but dP itself, and the order is
+//   S(i+1) | dK(i) dQ(i) | dP(i+1) | dV(i+1)
+// so that phase B of tile i+1, which needs only dP(i+1), runs beside dV(i+1) and S(i+2).
 //
 // CTA = 10 warps: 0-7 softmax (two warpgroups over query columns 0-63 and 64-127; a thread
 // owns one key row = TMEM lane), which also read the dQ^T partials out of TMEM (between
@@ -95,12 +100,14 @@ struct WideCfg {
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget");
   static_assert(D == 128 || kVOff == kKOff + kBox, "V follows K");
   // TMEM columns: dV | dK | S^T (then P^T, bf16 pairs, in the first half of each 64) |
-  // dP^T (then the dQ^T partial)
+  // dP^T (then, at d = 128, the dQ^T partial) | at d = 64, the dQ^T partial
   static constexpr uint32_t kColDV = 0;
   static constexpr uint32_t kColDK = D;
   static constexpr uint32_t kColS = 2 * D;
   static constexpr uint32_t kColDP = 2 * D + 128;
-  static_assert(kColDP + 128 <= kTmemCols, "TMEM budget");
+  static constexpr bool kSepDQ = kColDP + 256 <= kTmemCols;  // room for dQ^T beside dP^T
+  static constexpr uint32_t kColDQ = kSepDQ ? kColDP + 128 : kColDP;
+  static_assert(kColDQ + 128 <= kTmemCols, "TMEM budget");
 };
 
 struct WideParams {
@@ -177,7 +184,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   constexpr bool kMask = kVar == 1;
   constexpr bool kDrop = kVar == 2;
   constexpr bool kBits = kVar == 3;
-  constexpr uint32_t kColDV = C::kColDV, kColDK = C::kColDK, kColS = C::kColS, kColDP = C::kColDP;
+  constexpr uint32_t kColDV = C::kColDV, kColDK = C::kColDK, kColS = C::kColS, kColDP = C::kColDP, kColDQ = C::kColDQ;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // The swizzled operand layout needs a 1024-byte aligned base; the runtime provides it for
@@ -359,7 +366,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       auto issue_dQ = [&]() {
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          mma_ss(tmem + kColDP, sdesc_add(dKmn, k * 2048), sdesc_add(dSmn, k * 2048), idQ, k > 0);
+          mma_ss(tmem + kColDQ, sdesc_add(dKmn, k * 2048), sdesc_add(dSmn, k * 2048), idQ, k > 0);
       };
       bool ok = mbar_wait(&ctl.kv_full, 0, p.status, abort);
       // prologue: S(0), dP(0), dV(0)
@@ -390,23 +397,41 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           mma_commit(&ctl.s_full);
         }
         // dK(i) and dQ(i) read dS^T(i) from shared memory; dQ^T(i) lands in the dP^T
-        // columns, which phase B of tile i has read
+        // columns, which phase B of tile i has read, or in columns of its own, which the
+        // softmax warps have emptied of dQ^T(i-1)
         if (!(ok = mbar_wait(&ctl.ds_done, it & 1, p.status, abort))) break;
         tc_fence_after();
         issue_dK(it, s);
         mma_commit(&ctl.q_empty[s]);
         if constexpr (kDQ) {
+          if (C::kSepDQ && it > 0) {
+            if (!(ok = mbar_wait(&ctl.dq_empty, (it - 1) & 1, p.status, abort))) break;
+            tc_fence_after();
+          }
           issue_dQ();
           mma_commit(&ctl.dq_full);
         }
-        if (next) {
+        // dP(i+1) ahead of dV(i+1) where nothing else occupies the dP^T columns; with the dQ^T
+        // partial there, dP(i+1) would wait for its read-out, and dV(i+1) goes first (dP first
+        // measured 2% slower at d = 128)
+        constexpr bool kDPFirst = C::kSepDQ || !kDQ;
+        if (kDPFirst && next) {
+          if (!(ok = mbar_wait(&ctl.do_full[s1], par1, p.status, abort))) break;
+          tc_fence_after();
+          issue_dP(s1);
+          mma_commit(&ctl.dp_full);
+          if (!(ok = mbar_wait(&ctl.p_done, (it + 1) & 1, p.status, abort))) break;
+          tc_fence_after();
+          issue_dV(it + 1, s1);
+          mma_commit(&ctl.do_empty[s1]);  // dP(i+1) and dV(i+1), the readers of dO(i+1), issued
+        } else if (next) {
           // dV(i+1) reads P^T(i+1) from TMEM and dO(i+1) from its stage: both must be in
           if (!(ok = mbar_wait(&ctl.p_done, (it + 1) & 1, p.status, abort))) break;
           if (!(ok = mbar_wait(&ctl.do_full[s1], par1, p.status, abort))) break;
           tc_fence_after();
           issue_dV(it + 1, s1);
           // dP(i+1) once the softmax warps have read the dQ^T(i) partial out of its columns
-          if constexpr (kDQ) {
+          if constexpr (kDQ && !C::kSepDQ) {
             if (!(ok = mbar_wait(&ctl.dq_empty, it & 1, p.status, abort))) break;
             tc_fence_after();
           }
@@ -432,7 +457,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     uint8_t* dsrow = smem + C::kDsOff + r * 128;
     // The dQ^T partial of tile j: lane = head-dim index r, columns = the tile's queries; this
     // warpgroup takes its 64 columns and releases them as soon as they are in registers (dP of
-    // the next tile waits for that). It adds the first 32 into the fp32 accumulator at once and
+    // the next tile, or at d = 64 its dQ, waits for that). It adds the first 32 into the fp32 accumulator at once and
     // holds the other 32 for phase B of the next tile (16 after each of its two chunks): spread
     // out this way, the reductions slow the tensor core's operand reads less than in one burst.
     float held[32];
@@ -473,7 +498,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       if (!__all_sync(0xffffffffu, mbar_wait(&ctl.dq_full, j & 1, p.status, abort))) return false;
       tc_fence_after();
       float v[32];
-      tmem_ld32x2(tmem + lane_off + kColDP + wg * 64, tmem + lane_off + kColDP + wg * 64 + 32, v, held);
+      tmem_ld32x2(tmem + lane_off + kColDQ + wg * 64, tmem + lane_off + kColDQ + wg * 64 + 32, v, held);
       tc_fence_before();
       mbar_arrive(&ctl.dq_empty);
       if (!dq_rows) return true;
