@@ -41,10 +41,10 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 std::atomic<int> g_dq_mode{FA_BWD_DQ_AUTO};
 
 // The dQ mode for a plain backward. FA_BWD_DQ_AUTO takes the atomic way at every shape: on
-// GB300 (preprocess + backward, both modes in one process) the separate pass measured 1.599
-// against 1.330 ms at B2 H16 N8192 d128 causal, 1.036 against 0.898 ms at B16 H32 N1024
-// d128, 0.358 against 0.283 ms at B4 H16 N2048 d64, 5.853 against 4.832 ms at B1 H8 N32768
-// d128 causal and 0.212 against 0.176 ms at B4 H16 N2048 d64 causal. Dropping the dQ
+// GB300 (preprocess + backward, both modes in one process) the separate pass measured 1.565
+// against 1.280 ms at B2 H16 N8192 d128 causal, 0.973 against 0.837 ms at B16 H32 N1024
+// d128, 0.346 against 0.270 ms at B4 H16 N2048 d64, 5.800 against 4.697 ms at B1 H8 N32768
+// d128 causal and 0.203 against 0.165 ms at B4 H16 N2048 d64 causal. Dropping the dQ
 // partials saves the 128-key-tile kernel about a fifth of its time, less than the second
 // pass costs, which recomputes S and dP.
 bool separate_dq() { return g_dq_mode.load(std::memory_order_relaxed) == FA_BWD_DQ_SEPARATE; }

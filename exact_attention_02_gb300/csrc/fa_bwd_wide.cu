@@ -3,8 +3,8 @@
 // fa_bwd_dropout with their mask or dropout (the kVar instances).
 //
 // Method ("flash-attention-backpropagation", 反向总览 / Softmax梯度 / QKV梯度; the single
-// recompute per tile of "FlashAttention 反向传播" 踩坑二): one CTA owns a 128-key tile of
-// one head and loops over the 128-row query tiles that see it; P is rebuilt from the
+// recompute per tile of "FlashAttention 反向传播" 踩坑二): a work item is a 128-key tile of
+// one head, whose CTA loops over the 128-row query tiles that see it; P is rebuilt from the
 // forward's LSE, and each recompute of a tile feeds dV, dK and dQ.
 //
 // Keys sit on the 128 TMEM lanes, so dV and dK accumulate in TMEM:
@@ -42,6 +42,12 @@
 // producer; 9 MMA issuer. Shared memory: K, V (32 KB each), two Q/dO stages (64 KB each),
 // dS^T (32 KB) and LSE/D per stage.
 //
+// Persistent: one CTA per SM runs (key tile, head) items one after another, so that each
+// item's fixed costs overlap the previous item's end. While the softmax warps read out the
+// last dQ^T partial and store dK and dV, the producer loads the next item's first Q/dO stage
+// and (once the last products have read them) its K and V, and the tensor core computes its
+// first S^T and dP^T; only dV and dK of the new item wait for the accumulators to be read.
+//
 // Masks and dropout (kVar, "知识点13" §7: both are fused into the softmax step): the additive
 // mask adds M log2(e) to each exponent; the boolean mask (packed bits, as the forward reads
 // them) and dropout zero P for hidden or dropped keys, so their dS is 0 as well; dV takes only
@@ -77,7 +83,7 @@ constexpr uint32_t kTmemCols = 512;
 
 struct WideCtl {
   uint64_t kv_full, q_full[kStages], do_full[kStages], q_empty[kStages], do_empty[kStages];
-  uint64_t s_full, dp_full, p_done, ds_done, dq_full, dq_empty, kv_done, drain;
+  uint64_t s_full, dp_full, p_done, ds_done, dq_full, dq_empty, kv_done, acc_empty, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -195,29 +201,24 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   }
   WideCtl& ctl = *reinterpret_cast<WideCtl*>(smem + C::kCtlOff);
 
-  int kt, head;
-  if (p.causal) {  // key tiles near the start see the most queries: launch them first
-    kt = (int)(blockIdx.x / p.heads);
-    head = (int)(blockIdx.x % p.heads);
-  } else {
-    kt = (int)(blockIdx.x % p.kvtiles);
-    head = (int)(blockIdx.x / p.kvtiles);
-  }
-  const int qrow_base = head * p.Nq;
-  const int krow_base = head * p.Nk;
-  // causal: the first query tile holding a query that sees key kt * BN (query + offset >= key)
-  const int q_first = p.causal ? max(0, kt * BN - p.offset) / BQ : 0;
-  const int nq = p.qtiles - q_first;
-  if (nq <= 0) {  // no query sees these keys: dK = dV = 0
-    if (threadIdx.x < BN && kt * BN + (int)threadIdx.x < p.Nk) {
-      const size_t row = (size_t)krow_base + kt * BN + threadIdx.x;
-      uint4* dk = reinterpret_cast<uint4*>(p.dK + row * D);
-      uint4* dv = reinterpret_cast<uint4*>(p.dV + row * D);
-#pragma unroll
-      for (int u = 0; u < D / 8; ++u) dk[u] = dv[u] = make_uint4(0, 0, 0, 0);
+  // Work items are (key tile, head) pairs, w = 0 .. items-1. Causal: key tiles near the start
+  // see the most queries and come first. Each CTA (one per SM) takes the items
+  // b, 2G-1-b, 2G+b, 4G-1-b, ... (G CTAs): every round of G items runs in the other direction,
+  // so that the heavier items of one round and the lighter ones of the next land on the same SM.
+  const int items = p.kvtiles * p.heads;
+  const int G = (int)gridDim.x, b = (int)blockIdx.x;
+  auto item_of = [&](int r) { return r * G + ((r & 1) ? G - 1 - b : b); };
+  auto decode = [&](int w, int& kt, int& head) {
+    if (p.causal) {
+      kt = w / p.heads;
+      head = w % p.heads;
+    } else {
+      kt = w % p.kvtiles;
+      head = w / p.kvtiles;
     }
-    return;
-  }
+  };
+  // causal: the first query tile holding a query that sees key kt * BN (query + offset >= key)
+  auto q_first_of = [&](int kt) { return p.causal ? max(0, kt * BN - p.offset) / BQ : 0; };
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl.kv_full, 1);
@@ -234,6 +235,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     mbar_init(&ctl.dq_full, 1);
     mbar_init(&ctl.dq_empty, 256);
     mbar_init(&ctl.kv_done, 1);
+    mbar_init(&ctl.acc_empty, 256);
     mbar_init(&ctl.drain, 1);
     ctl.abort = 0;
     fence_mbar_init();
@@ -245,6 +247,8 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort = &ctl.abort;
 
+  // Every barrier of a query tile counts tiles over all items of the CTA (g below), and kv_full,
+  // kv_done and acc_empty count the CTA's items (ni).
   if (warp == kLoadWarp) {
     // Lane 0 drives the copies and barriers. LSE_i and D_i of a whole tile whose rows start
     // 16-byte aligned arrive by bulk copy with Q_i; otherwise (the last, partial tile of a
@@ -255,61 +259,88 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
-      mbar_expect_tx(&ctl.kv_full, 2 * C::kRowTile);
-      for (int b = 0; b < C::kBoxes; ++b) {
-        tma_load_3d(smem + C::kKOff + b * kBox, &tmK, &ctl.kv_full, b * 64, kt * BN, head);
-        tma_load_3d(smem + C::kVOff + b * kBox, &tmV, &ctl.kv_full, b * 64, kt * BN, head);
-      }
     }
-    int last_q[kStages] = {-1, -1}, last_do[kStages] = {-1, -1};
+    int last_q[kStages] = {-1, -1}, last_do[kStages] = {-1, -1}, last_kv = -1;
     // Test hook of the failure path: never arm the first Q stage, so the MMA thread's wait
     // for it runs out (see StatusBlock); off unless a test sets it.
     const bool skip_first = injected(p.status, kInjectBwd);
     const bool all_bulk = !kTail || ((p.Nq % BQ) == 0 && (p.Nq % 4) == 0);
-    for (int it = 0; it < nq && (lane == 0 || !all_bulk); ++it) {
-      const int s = it % kStages;
-      const uint32_t par = ((it / kStages) - 1) & 1;
-      // Q_i's slot (and its LSE/D) frees once dK of the tile two back has run.
-      bool ok = true;
-      if (lane == 0 && it >= kStages) ok = mbar_wait(&ctl.q_empty[s], par, p.status, abort);
-      if (!all_bulk) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      const int q0 = (q_first + it) * BQ;  // first query of the tile, within the head
-      uint8_t* st = smem + C::kStageOff + s * 2 * C::kRowTile;
-      float* vec = reinterpret_cast<float*>(smem + C::kVecOff + s * kVecBytes);
-      const bool bulk = !kTail || (q0 + BQ <= p.Nq && (p.Nq % 4) == 0);
-      if (!bulk) {
-        for (int c = lane; c < BQ; c += 32) {
-          const bool in = q0 + c < p.Nq;
-          vec[c] = in ? p.LSE[qrow_base + q0 + c] : INFINITY;
-          vec[BQ + c] = in ? p.Dvec[qrow_base + q0 + c] : 0.f;
-        }
-        __syncwarp();
-      }
-      if (lane == 0) {
-        if (it > 0 || !skip_first) {
-          mbar_expect_tx(&ctl.q_full[s], C::kRowTile + (bulk ? kVecBytes : 0));
-          for (int b = 0; b < C::kBoxes; ++b) tma_load_3d(st + b * kBox, &tmQ, &ctl.q_full[s], b * 64, q0, head);
-          if (bulk) {
-            bulk_load(vec, p.LSE + qrow_base + q0, BQ * 4, &ctl.q_full[s]);
-            bulk_load(vec + BQ, p.Dvec + qrow_base + q0, BQ * 4, &ctl.q_full[s]);
+    bool ok = true;
+    int g = 0, ni = 0;
+    for (int r = 0; ok && (lane == 0 || !all_bulk); ++r) {
+      const int w = item_of(r);
+      if (w >= items) break;
+      int kt, head;
+      decode(w, kt, head);
+      const int q_first = q_first_of(kt);
+      const int nq = p.qtiles - q_first;
+      if (nq <= 0) continue;
+      const int qrow_base = head * p.Nq;
+      // K_j and V_j once the products of the previous item that read them have run; after the
+      // first item, behind this item's first Q/dO stage, whose slot frees earlier
+      auto load_kv = [&]() {
+        if (lane == 0) {
+          if (ni > 0 && !mbar_wait(&ctl.kv_done, (ni - 1) & 1, p.status, abort)) {
+            ok = false;
+          } else {
+            mbar_expect_tx(&ctl.kv_full, 2 * C::kRowTile);
+            for (int bx = 0; bx < C::kBoxes; ++bx) {
+              tma_load_3d(smem + C::kKOff + bx * kBox, &tmK, &ctl.kv_full, bx * 64, kt * BN, head);
+              tma_load_3d(smem + C::kVOff + bx * kBox, &tmV, &ctl.kv_full, bx * 64, kt * BN, head);
+            }
+            last_kv = ni;
           }
-          last_q[s] = it;
         }
-        // dO_i's slot frees once dV of the tile two back has run (earlier than Q's).
-        if (it >= kStages && !mbar_wait(&ctl.do_empty[s], par, p.status, abort)) ok = false;
-        if (ok) {
-          mbar_expect_tx(&ctl.do_full[s], C::kRowTile);
-          for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(st + C::kRowTile + b * kBox, &tmdO, &ctl.do_full[s], b * 64, q0, head);
-          last_do[s] = it;
+        if (!all_bulk) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      };
+      if (ni == 0) load_kv();
+      for (int it = 0; ok && it < nq; ++it) {
+        const int gi = g + it;
+        const int s = gi % kStages;
+        const uint32_t par = ((gi / kStages) - 1) & 1;
+        // Q_i's slot (and its LSE/D) frees once dK of the tile two back has run.
+        if (lane == 0 && gi >= kStages) ok = mbar_wait(&ctl.q_empty[s], par, p.status, abort);
+        if (!all_bulk) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const int q0 = (q_first + it) * BQ;  // first query of the tile, within the head
+        uint8_t* st = smem + C::kStageOff + s * 2 * C::kRowTile;
+        float* vec = reinterpret_cast<float*>(smem + C::kVecOff + s * kVecBytes);
+        const bool bulk = !kTail || (q0 + BQ <= p.Nq && (p.Nq % 4) == 0);
+        if (!bulk) {
+          for (int c = lane; c < BQ; c += 32) {
+            const bool in = q0 + c < p.Nq;
+            vec[c] = in ? p.LSE[qrow_base + q0 + c] : INFINITY;
+            vec[BQ + c] = in ? p.Dvec[qrow_base + q0 + c] : 0.f;
+          }
+          __syncwarp();
         }
+        if (lane == 0) {
+          if (gi > 0 || !skip_first) {
+            mbar_expect_tx(&ctl.q_full[s], C::kRowTile + (bulk ? kVecBytes : 0));
+            for (int bx = 0; bx < C::kBoxes; ++bx) tma_load_3d(st + bx * kBox, &tmQ, &ctl.q_full[s], bx * 64, q0, head);
+            if (bulk) {
+              bulk_load(vec, p.LSE + qrow_base + q0, BQ * 4, &ctl.q_full[s]);
+              bulk_load(vec + BQ, p.Dvec + qrow_base + q0, BQ * 4, &ctl.q_full[s]);
+            }
+            last_q[s] = gi;
+          }
+          // dO_i's slot frees once dV of the tile two back has run (earlier than Q's).
+          if (gi >= kStages && !mbar_wait(&ctl.do_empty[s], par, p.status, abort)) ok = false;
+          if (ok) {
+            mbar_expect_tx(&ctl.do_full[s], C::kRowTile);
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              tma_load_3d(st + C::kRowTile + bx * kBox, &tmdO, &ctl.do_full[s], bx * 64, q0, head);
+            last_do[s] = gi;
+          }
+        }
+        if (!all_bulk) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (ok && it == 0 && ni > 0) load_kv();
       }
-      if (!all_bulk) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
+      g += nq;
+      ++ni;
     }
     if (lane == 0) {  // every issued copy must land before the CTA may exit
-      mbar_wait(&ctl.kv_full, 0, p.status, nullptr);
+      if (last_kv >= 0) mbar_wait(&ctl.kv_full, last_kv & 1, p.status, nullptr);
       for (int s = 0; s < kStages; ++s) {
         if (last_q[s] >= 0) mbar_wait(&ctl.q_full[s], (last_q[s] / kStages) & 1, p.status, nullptr);
         if (last_do[s] >= 0) mbar_wait(&ctl.do_full[s], (last_do[s] / kStages) & 1, p.status, nullptr);
@@ -349,18 +380,18 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                  sdesc_add(od, (k / 4) * kBox + (k % 4) * 32), idSP, k > 0);
       };
       // K = queries: 16 rows (2048 bytes) of the MN-major dO_i / Q_i per step
-      auto issue_dV = [&](int it, int s) {
+      auto issue_dV = [&](bool first, int s) {
         const uint64_t bd = stage_mn(s, true);
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
-          mma_ts(tmem + kColDV, packed_col(tmem + kColS, k), sdesc_add(bd, k * 2048), idKV, (it > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tmem + kColDV, packed_col(tmem + kColS, k), sdesc_add(bd, k * 2048), idKV, (!first || k > 0) ? 1u : 0u);
       };
-      auto issue_dK = [&](int it, int s) {
+      auto issue_dK = [&](bool first, int s) {
         const uint64_t bd = stage_mn(s, false);
 #pragma unroll
         for (int k = 0; k < BQ / 16; ++k)
           mma_ss(tmem + kColDK, sdesc_add(dSk, (k / 4) * kBox + (k % 4) * 32), sdesc_add(bd, k * 2048), idKV,
-                 (it > 0 || k > 0) ? 1u : 0u);
+                 (!first || k > 0) ? 1u : 0u);
       };
       // K = keys: 16 rows (2048 bytes) of K_j and of dS^T per step
       auto issue_dQ = [&]() {
@@ -368,79 +399,97 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         for (int k = 0; k < BN / 16; ++k)
           mma_ss(tmem + kColDQ, sdesc_add(dKmn, k * 2048), sdesc_add(dSmn, k * 2048), idQ, k > 0);
       };
-      bool ok = mbar_wait(&ctl.kv_full, 0, p.status, abort);
-      // prologue: S(0), dP(0), dV(0)
-      if (ok && (ok = mbar_wait(&ctl.q_full[0], 0, p.status, abort))) {
+      bool ok = true;
+      int g = 0, ni = 0;
+      for (int r = 0; ok; ++r) {
+        const int w = item_of(r);
+        if (w >= items) break;
+        int kt, head;
+        decode(w, kt, head);
+        const int nq = p.qtiles - q_first_of(kt);
+        if (nq <= 0) continue;
+        // prologue: S(0), dP(0), dV(0) of the item
+        const int s0 = g % kStages;
+        const uint32_t par0 = (g / kStages) & 1;
+        if (!(ok = mbar_wait(&ctl.kv_full, ni & 1, p.status, abort))) break;
+        if (!(ok = mbar_wait(&ctl.q_full[s0], par0, p.status, abort))) break;
         tc_fence_after();
-        issue_S(0);
+        issue_S(s0);
         mma_commit(&ctl.s_full);
-      }
-      if (ok && (ok = mbar_wait(&ctl.do_full[0], 0, p.status, abort))) {
+        if (!(ok = mbar_wait(&ctl.do_full[s0], par0, p.status, abort))) break;
+        if constexpr (kDQ && !C::kSepDQ) {  // the previous item's last dQ^T partial is out of the dP^T columns
+          if (g > 0 && !(ok = mbar_wait(&ctl.dq_empty, (g - 1) & 1, p.status, abort))) break;
+        }
         tc_fence_after();
-        issue_dP(0);
+        issue_dP(s0);
         mma_commit(&ctl.dp_full);
-      }
-      if (ok && (ok = mbar_wait(&ctl.p_done, 0, p.status, abort))) {
+        if (!(ok = mbar_wait(&ctl.p_done, g & 1, p.status, abort))) break;
+        // dV and dK of the previous item have been read out of TMEM
+        if (ni > 0 && !(ok = mbar_wait(&ctl.acc_empty, (ni - 1) & 1, p.status, abort))) break;
         tc_fence_after();
-        issue_dV(0, 0);
-        mma_commit(&ctl.do_empty[0]);  // dP(0) and dV(0), the readers of dO(0), issued
-      }
-      for (int it = 0; ok && it < nq; ++it) {
-        const int s = it % kStages, s1 = (it + 1) % kStages;
-        const bool next = it + 1 < nq;
-        const uint32_t par1 = ((it + 1) / kStages) & 1;
-        // S(i+1) over the S^T columns: P^T(i) was read by dV(i), issued before
-        if (next) {
-          if (!(ok = mbar_wait(&ctl.q_full[s1], par1, p.status, abort))) break;
-          tc_fence_after();
-          issue_S(s1);
-          mma_commit(&ctl.s_full);
-        }
-        // dK(i) and dQ(i) read dS^T(i) from shared memory; dQ^T(i) lands in the dP^T
-        // columns, which phase B of tile i has read, or in columns of its own, which the
-        // softmax warps have emptied of dQ^T(i-1)
-        if (!(ok = mbar_wait(&ctl.ds_done, it & 1, p.status, abort))) break;
-        tc_fence_after();
-        issue_dK(it, s);
-        mma_commit(&ctl.q_empty[s]);
-        if constexpr (kDQ) {
-          if (C::kSepDQ && it > 0) {
-            if (!(ok = mbar_wait(&ctl.dq_empty, (it - 1) & 1, p.status, abort))) break;
+        issue_dV(true, s0);
+        mma_commit(&ctl.do_empty[s0]);  // dP(0) and dV(0), the readers of dO(0), issued
+        for (int it = 0; ok && it < nq; ++it) {
+          const int gi = g + it;
+          const int s = gi % kStages, s1 = (gi + 1) % kStages;
+          const bool next = it + 1 < nq;
+          const uint32_t par1 = ((gi + 1) / kStages) & 1;
+          // S(i+1) over the S^T columns: P^T(i) was read by dV(i), issued before
+          if (next) {
+            if (!(ok = mbar_wait(&ctl.q_full[s1], par1, p.status, abort))) break;
             tc_fence_after();
+            issue_S(s1);
+            mma_commit(&ctl.s_full);
           }
-          issue_dQ();
-          mma_commit(&ctl.dq_full);
-        }
-        // dP(i+1) ahead of dV(i+1) where nothing else occupies the dP^T columns; with the dQ^T
-        // partial there, dP(i+1) would wait for its read-out, and dV(i+1) goes first (dP first
-        // measured 2% slower at d = 128)
-        constexpr bool kDPFirst = C::kSepDQ || !kDQ;
-        if (kDPFirst && next) {
-          if (!(ok = mbar_wait(&ctl.do_full[s1], par1, p.status, abort))) break;
+          // dK(i) and dQ(i) read dS^T(i) from shared memory; dQ^T(i) lands in the dP^T
+          // columns, which phase B of tile i has read, or in columns of its own, which the
+          // softmax warps have emptied of the previous partial
+          if (!(ok = mbar_wait(&ctl.ds_done, gi & 1, p.status, abort))) break;
           tc_fence_after();
-          issue_dP(s1);
-          mma_commit(&ctl.dp_full);
-          if (!(ok = mbar_wait(&ctl.p_done, (it + 1) & 1, p.status, abort))) break;
-          tc_fence_after();
-          issue_dV(it + 1, s1);
-          mma_commit(&ctl.do_empty[s1]);  // dP(i+1) and dV(i+1), the readers of dO(i+1), issued
-        } else if (next) {
-          // dV(i+1) reads P^T(i+1) from TMEM and dO(i+1) from its stage: both must be in
-          if (!(ok = mbar_wait(&ctl.p_done, (it + 1) & 1, p.status, abort))) break;
-          if (!(ok = mbar_wait(&ctl.do_full[s1], par1, p.status, abort))) break;
-          tc_fence_after();
-          issue_dV(it + 1, s1);
-          // dP(i+1) once the softmax warps have read the dQ^T(i) partial out of its columns
-          if constexpr (kDQ && !C::kSepDQ) {
-            if (!(ok = mbar_wait(&ctl.dq_empty, it & 1, p.status, abort))) break;
+          issue_dK(it == 0, s);
+          mma_commit(&ctl.q_empty[s]);
+          if constexpr (kDQ) {
+            if (C::kSepDQ && gi > 0) {
+              if (!(ok = mbar_wait(&ctl.dq_empty, (gi - 1) & 1, p.status, abort))) break;
+              tc_fence_after();
+            }
+            issue_dQ();
+            mma_commit(&ctl.dq_full);
+          }
+          // dP(i+1) ahead of dV(i+1) where nothing else occupies the dP^T columns; with the dQ^T
+          // partial there, dP(i+1) would wait for its read-out, and dV(i+1) goes first (dP first
+          // measured 2% slower at d = 128)
+          constexpr bool kDPFirst = C::kSepDQ || !kDQ;
+          if (kDPFirst && next) {
+            if (!(ok = mbar_wait(&ctl.do_full[s1], par1, p.status, abort))) break;
             tc_fence_after();
+            issue_dP(s1);
+            mma_commit(&ctl.dp_full);
+            if (!(ok = mbar_wait(&ctl.p_done, (gi + 1) & 1, p.status, abort))) break;
+            tc_fence_after();
+            issue_dV(false, s1);
+            mma_commit(&ctl.do_empty[s1]);  // dP(i+1) and dV(i+1), the readers of dO(i+1), issued
+          } else if (next) {
+            // dV(i+1) reads P^T(i+1) from TMEM and dO(i+1) from its stage: both must be in
+            if (!(ok = mbar_wait(&ctl.p_done, (gi + 1) & 1, p.status, abort))) break;
+            if (!(ok = mbar_wait(&ctl.do_full[s1], par1, p.status, abort))) break;
+            tc_fence_after();
+            issue_dV(false, s1);
+            // dP(i+1) once the softmax warps have read the dQ^T(i) partial out of its columns
+            if constexpr (kDQ && !C::kSepDQ) {
+              if (!(ok = mbar_wait(&ctl.dq_empty, gi & 1, p.status, abort))) break;
+              tc_fence_after();
+            }
+            issue_dP(s1);
+            mma_commit(&ctl.dp_full);
+            mma_commit(&ctl.do_empty[s1]);  // dV(i+1) and dP(i+1), the readers of dO(i+1), issued
           }
-          issue_dP(s1);
-          mma_commit(&ctl.dp_full);
-          mma_commit(&ctl.do_empty[s1]);  // dV(i+1) and dP(i+1), the readers of dO(i+1), issued
         }
+        if (!ok) break;
+        mma_commit(&ctl.kv_done);  // every product of the item: K_j, V_j and dV, dK are free to read
+        g += nq;
+        ++ni;
       }
-      mma_commit(&ctl.kv_done);
       mma_commit(&ctl.drain);
       mbar_wait(&ctl.drain, 0, p.status, nullptr);
     }
@@ -449,7 +498,6 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int wg = warp >> 2;
     const int r = (warp & 3) * 32 + lane;  // TMEM lane: the key row (S^T, dP^T, dV, dK), or the
                                            // head-dim index (the dQ^T partial)
-    const int key = kt * BN + r;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float2 sl2 = make_float2(p.sl2, p.sl2);
     const float2 neg_log2e = make_float2(-kLog2e, -kLog2e);
@@ -457,9 +505,10 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     uint8_t* dsrow = smem + C::kDsOff + r * 128;
     // The dQ^T partial of tile j: lane = head-dim index r, columns = the tile's queries; this
     // warpgroup takes its 64 columns and releases them as soon as they are in registers (dP of
-    // the next tile, or at d = 64 its dQ, waits for that). It adds the first 32 into the fp32 accumulator at once and
-    // holds the other 32 for phase B of the next tile (16 after each of its two chunks): spread
-    // out this way, the reductions slow the tensor core's operand reads less than in one burst.
+    // the next tile, or at d = 64 its dQ, waits for that). It adds the first 32 into the fp32
+    // accumulator at once and holds the other 32 for phase B of the next tile (16 after each of
+    // its two chunks): spread out this way, the reductions slow the tensor core's operand reads
+    // less than in one burst.
     float held[32];
     float* held_dst = nullptr;
     int held_valid = 0;
@@ -494,8 +543,10 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // At d = 64 only TMEM lanes 0-63 hold head-dim rows: the warps of lanes 64-127 load their
     // (unused) lanes too, but add nothing (a test that is uniform over each warp).
     const bool dq_rows = (warp & 3) * 32 < D;
-    auto read_out_dq = [&](int j) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(&ctl.dq_full, j & 1, p.status, abort))) return false;
+    int q_first = 0, qrow_base = 0;
+    // partial j of the current item, the CTA's tile gj
+    auto read_out_dq = [&](int j, int gj) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctl.dq_full, gj & 1, p.status, abort))) return false;
       tc_fence_after();
       float v[32];
       tmem_ld32x2(tmem + lane_off + kColDQ + wg * 64, tmem + lane_off + kColDQ + wg * 64 + 32, v, held);
@@ -509,170 +560,192 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       held_valid = p.Nq - qh - 32;
       return true;
     };
-    // kBits: the warp's 32 keys are one word of each query's row. For chunk ch, lane L reads the
-    // word of query (tile start + wg * 64 + ch * 32 + L), one tile ahead, so that the load's
-    // latency hides behind the current tile.
-    const int kword = (kt * BN + (warp & 3) * 32) >> 5;
-    const uint32_t* bcol =
-        kBits ? pv.bits + (int64_t)(head / pv.H) * pv.mask_sb + (int64_t)(head % pv.H) * pv.mask_sh + kword : nullptr;
-    auto bits_word = [&](int it, int ch) -> uint32_t {
-      const int q = (q_first + it) * BQ + wg * 64 + ch * 32 + lane;
-      return (it < nq && (!kTail || (q < p.Nq && kword * 32 < p.Nk))) ? bcol[(int64_t)q * pv.mask_srow] : 0u;
-    };
-    uint32_t bword[2] = {0u, 0u};
-    if constexpr (kBits) {
-      bword[0] = bits_word(0, 0);
-      bword[1] = bits_word(0, 1);
-    }
     bool ok = true;
-    for (int it = 0; ok && it < nq; ++it) {
-      const float* vec = reinterpret_cast<const float*>(smem + C::kVecOff + (it % kStages) * kVecBytes);
-      uint32_t bcur[2] = {bword[0], bword[1]};
-      if constexpr (kBits) {
-        bword[0] = bits_word(it + 1, 0);
-        bword[1] = bits_word(it + 1, 1);
+    int g = 0, ni = 0;
+    for (int rr = 0; ok; ++rr) {
+      const int w = item_of(rr);
+      if (w >= items) break;
+      int kt, head;
+      decode(w, kt, head);
+      q_first = q_first_of(kt);
+      const int nq = p.qtiles - q_first;
+      qrow_base = head * p.Nq;
+      const int krow_base = head * p.Nk;
+      if (nq <= 0) {  // no query sees these keys: dK = dV = 0
+        if (threadIdx.x < BN && kt * BN + (int)threadIdx.x < p.Nk) {
+          const size_t row = (size_t)krow_base + kt * BN + threadIdx.x;
+          uint4* dk = reinterpret_cast<uint4*>(p.dK + row * D);
+          uint4* dv = reinterpret_cast<uint4*>(p.dV + row * D);
+#pragma unroll
+          for (int u = 0; u < D / 8; ++u) dk[u] = dv[u] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
       }
-      uint32_t kbits[2] = {0u, 0u};  // kDrop: keep bits of this key against each chunk's 32 queries
-      const int q0 = (q_first + it) * BQ;
-      // some key of the tile exceeds the limit of some query of the tile
-      const bool diag = p.causal && q0 + p.offset < kt * BN + BN - 1;
-      // ---- phase A: P^T = exp2(S^T * scale * log2e - LSE * log2e), over S^T in TMEM
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full, it & 1, p.status, abort));
-      if (!ok) break;
-      tc_fence_after();
-      float pr[64];  // this row's P for the warpgroup's 64 queries, kept for phase B
+      const int key = kt * BN + r;
+      // kBits: the warp's 32 keys are one word of each query's row. For chunk ch, lane L reads the
+      // word of query (tile start + wg * 64 + ch * 32 + L), one tile ahead, so that the load's
+      // latency hides behind the current tile.
+      const int kword = (kt * BN + (warp & 3) * 32) >> 5;
+      const uint32_t* bcol =
+          kBits ? pv.bits + (int64_t)(head / pv.H) * pv.mask_sb + (int64_t)(head % pv.H) * pv.mask_sh + kword : nullptr;
+      auto bits_word = [&](int it, int ch) -> uint32_t {
+        const int q = (q_first + it) * BQ + wg * 64 + ch * 32 + lane;
+        return (it < nq && (!kTail || (q < p.Nq && kword * 32 < p.Nk))) ? bcol[(int64_t)q * pv.mask_srow] : 0u;
+      };
+      uint32_t bword[2] = {0u, 0u};
+      if constexpr (kBits) {
+        bword[0] = bits_word(0, 0);
+        bword[1] = bits_word(0, 1);
+      }
+      for (int it = 0; ok && it < nq; ++it) {
+        const int gi = g + it;
+        const float* vec = reinterpret_cast<const float*>(smem + C::kVecOff + (gi % kStages) * kVecBytes);
+        uint32_t bcur[2] = {bword[0], bword[1]};
+        if constexpr (kBits) {
+          bword[0] = bits_word(it + 1, 0);
+          bword[1] = bits_word(it + 1, 1);
+        }
+        uint32_t kbits[2] = {0u, 0u};  // kDrop: keep bits of this key against each chunk's 32 queries
+        const int q0 = (q_first + it) * BQ;
+        // some key of the tile exceeds the limit of some query of the tile
+        const bool diag = p.causal && q0 + p.offset < kt * BN + BN - 1;
+        // ---- phase A: P^T = exp2(S^T * scale * log2e - LSE * log2e), over S^T in TMEM
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.s_full, gi & 1, p.status, abort));
+        if (!ok) break;
+        tc_fence_after();
+        float pr[64];  // this row's P for the warpgroup's 64 queries, kept for phase B
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int c0 = wg * 64 + ch * 32;  // first query column of this chunk
-        // kMask: M(query, this key) * log2(e) for the chunk's 32 queries (across the warp each
-        // load reads 32 consecutive keys of one mask row), issued before the TMEM load
-        float mk[kMask ? 32 : 1];
-        if constexpr (kMask) {
-          const __nv_bfloat16* mcol = pv.mask + (int64_t)(head / pv.H) * pv.mask_sb + (int64_t)(head % pv.H) * pv.mask_sh + key;
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = wg * 64 + ch * 32;  // first query column of this chunk
+          // kMask: M(query, this key) * log2(e) for the chunk's 32 queries (across the warp each
+          // load reads 32 consecutive keys of one mask row), issued before the TMEM load
+          float mk[kMask ? 32 : 1];
+          if constexpr (kMask) {
+            const __nv_bfloat16* mcol = pv.mask + (int64_t)(head / pv.H) * pv.mask_sb + (int64_t)(head % pv.H) * pv.mask_sh + key;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int q = q0 + c0 + c;
-            mk[c] = (!kTail || (key < p.Nk && q < p.Nq)) ? __bfloat162float(mcol[(int64_t)q * pv.mask_srow]) * kLog2e : 0.f;
+            for (int c = 0; c < 32; ++c) {
+              const int q = q0 + c0 + c;
+              mk[c] = (!kTail || (key < p.Nk && q < p.Nq)) ? __bfloat162float(mcol[(int64_t)q * pv.mask_srow]) * kLog2e : 0.f;
+            }
           }
-        }
-        // kDrop: lane L draws the keep bits of query (chunk start + L) against the warp's 32
-        // keys (two Philox blocks of 16 keys); the transpose leaves lane T with bit c =
-        // keep(query c of the chunk, key T). kBits: the same transpose of the prefetched words.
-        if constexpr (kDrop) {
-          const uint32_t i = (uint32_t)(q0 + c0 + lane);
-          const uint32_t blk0 = (uint32_t)((kt * BN + (warp & 3) * 32) >> 4);
-          const uint32_t row = rng::keep16(blk0, i, (uint32_t)head, pv.seed_lo, pv.seed_hi, pv.drop_tt) |
-                               (rng::keep16(blk0 + 1, i, (uint32_t)head, pv.seed_lo, pv.seed_hi, pv.drop_tt) << 16);
-          kbits[ch] = transpose32(row, lane);
-        }
-        const uint32_t vbits = kBits ? transpose32(bcur[ch], lane) : 0u;
-        float sv[32];
-        tmem_ld32(tmem + lane_off + kColS + c0, sv);
-        uint32_t pk[16];
-        if constexpr (kVar == 0) {
+          // kDrop: lane L draws the keep bits of query (chunk start + L) against the warp's 32
+          // keys (two Philox blocks of 16 keys); the transpose leaves lane T with bit c =
+          // keep(query c of the chunk, key T). kBits: the same transpose of the prefetched words.
+          if constexpr (kDrop) {
+            const uint32_t i = (uint32_t)(q0 + c0 + lane);
+            const uint32_t blk0 = (uint32_t)((kt * BN + (warp & 3) * 32) >> 4);
+            const uint32_t row = rng::keep16(blk0, i, (uint32_t)head, pv.seed_lo, pv.seed_hi, pv.drop_tt) |
+                                 (rng::keep16(blk0 + 1, i, (uint32_t)head, pv.seed_lo, pv.seed_hi, pv.drop_tt) << 16);
+            kbits[ch] = transpose32(row, lane);
+          }
+          const uint32_t vbits = kBits ? transpose32(bcur[ch], lane) : 0u;
+          float sv[32];
+          tmem_ld32(tmem + lane_off + kColS + c0, sv);
+          uint32_t pk[16];
+          if constexpr (kVar == 0) {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int c = c0 + 2 * u;
+              const float2 lse = *reinterpret_cast<const float2*>(vec + c);
+              const float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, fmul2(lse, neg_log2e));
+              float2 pv = make_float2(ex2(x.x), ex2(x.y));
+              if (diag) {
+                if (key > q0 + c + p.offset) pv.x = 0.f;
+                if (key > q0 + c + 1 + p.offset) pv.y = 0.f;
+              }
+              pr[ch * 32 + 2 * u] = pv.x;
+              pr[ch * 32 + 2 * u + 1] = pv.y;
+              pk[u] = pack_bf16(pv.x, pv.y);
+            }
+          } else {
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
             const int c = c0 + 2 * u;
             const float2 lse = *reinterpret_cast<const float2*>(vec + c);
-            const float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, fmul2(lse, neg_log2e));
+            float2 nl = fmul2(lse, neg_log2e);
+            if constexpr (kMask || kBits) {  // a query with no visible key (LSE = -inf) has P = 0
+              if (lse.x == -INFINITY) nl.x = -INFINITY;
+              if (lse.y == -INFINITY) nl.y = -INFINITY;
+            }
+            float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, nl);
+            if constexpr (kMask) x = fadd2(x, make_float2(mk[2 * u], mk[2 * u + 1]));
             float2 pv = make_float2(ex2(x.x), ex2(x.y));
+            if constexpr (kBits) {  // a hidden key has P = 0, and so dS = 0
+              if (!((vbits >> (2 * u)) & 1u)) pv.x = 0.f;
+              if (!((vbits >> (2 * u + 1)) & 1u)) pv.y = 0.f;
+            }
             if (diag) {
               if (key > q0 + c + p.offset) pv.x = 0.f;
               if (key > q0 + c + 1 + p.offset) pv.y = 0.f;
             }
             pr[ch * 32 + 2 * u] = pv.x;
             pr[ch * 32 + 2 * u + 1] = pv.y;
-            pk[u] = pack_bf16(pv.x, pv.y);
+            if constexpr (kDrop) {  // dV takes the kept weights (scaled by c in its epilogue)
+              const uint32_t kb = kbits[ch] >> (2 * u);
+              pk[u] = pack_bf16((kb & 1u) ? pv.x : 0.f, (kb & 2u) ? pv.y : 0.f);
+            } else {
+              pk[u] = pack_bf16(pv.x, pv.y);
+            }
           }
-        } else {
+          }
+          tmem_st16(tmem + lane_off + kColS + wg * 64 + ch * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&ctl.p_done);
+        // ---- the previous tile's dQ^T partial, while dK/dQ of that tile and dV of this one run
+        if constexpr (kDQ) {
+          if (it > 0 && !(ok = read_out_dq(it - 1, gi - 1))) break;
+        }
+        // ---- phase B: dS^T = P^T * (dP^T - D), to shared memory only
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dp_full, gi & 1, p.status, abort));
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int c = c0 + 2 * u;
-          const float2 lse = *reinterpret_cast<const float2*>(vec + c);
-          float2 nl = fmul2(lse, neg_log2e);
-          if constexpr (kMask || kBits) {  // a query with no visible key (LSE = -inf) has P = 0
-            if (lse.x == -INFINITY) nl.x = -INFINITY;
-            if (lse.y == -INFINITY) nl.y = -INFINITY;
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = wg * 64 + ch * 32;
+          float dp[32];
+          tmem_ld32(tmem + lane_off + kColDP + c0, dp);
+          uint32_t dk[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            float2 dd;
+            if constexpr (kDrop) {  // dP of a dropped key is 0; a kept one is scaled
+              const float2 dvec = *reinterpret_cast<const float2*>(vec + BQ + c0 + 2 * u);
+              const uint32_t kb = kbits[ch] >> (2 * u);
+              dd = make_float2((kb & 1u) ? fmaf(dp[2 * u], pv.drop_scale, -dvec.x) : -dvec.x,
+                               (kb & 2u) ? fmaf(dp[2 * u + 1], pv.drop_scale, -dvec.y) : -dvec.y);
+            } else {
+              dd = ffma2(*reinterpret_cast<const float2*>(vec + BQ + c0 + 2 * u), minus1,
+                         make_float2(dp[2 * u], dp[2 * u + 1]));
+            }
+            const float2 ds = fmul2(make_float2(pr[ch * 32 + 2 * u], pr[ch * 32 + 2 * u + 1]), dd);
+            dk[u] = pack_bf16(ds.x, ds.y);
           }
-          float2 x = ffma2(make_float2(sv[2 * u], sv[2 * u + 1]), sl2, nl);
-          if constexpr (kMask) x = fadd2(x, make_float2(mk[2 * u], mk[2 * u + 1]));
-          float2 pv = make_float2(ex2(x.x), ex2(x.y));
-          if constexpr (kBits) {  // a hidden key has P = 0, and so dS = 0
-            if (!((vbits >> (2 * u)) & 1u)) pv.x = 0.f;
-            if (!((vbits >> (2 * u + 1)) & 1u)) pv.y = 0.f;
+          // dS^T row r, query columns c0..c0+31: four 16-byte chunks of a 128-byte swizzled
+          // row (box c0 / 64, chunk (c0 % 64) / 8 + u, XOR (r % 8))
+          uint8_t* atom = dsrow + (c0 / 64) * kBox;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int chunk = ((c0 % 64) / 8 + u) ^ (r & 7);
+            *reinterpret_cast<uint4*>(atom + chunk * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
           }
-          if (diag) {
-            if (key > q0 + c + p.offset) pv.x = 0.f;
-            if (key > q0 + c + 1 + p.offset) pv.y = 0.f;
-          }
-          pr[ch * 32 + 2 * u] = pv.x;
-          pr[ch * 32 + 2 * u + 1] = pv.y;
-          if constexpr (kDrop) {  // dV takes the kept weights (scaled by c in its epilogue)
-            const uint32_t kb = kbits[ch] >> (2 * u);
-            pk[u] = pack_bf16((kb & 1u) ? pv.x : 0.f, (kb & 2u) ? pv.y : 0.f);
-          } else {
-            pk[u] = pack_bf16(pv.x, pv.y);
-          }
+          if (ch == 0) flush_held(0);
         }
-        }
-        tmem_st16(tmem + lane_off + kColS + wg * 64 + ch * 16, pk);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&ctl.ds_done);
+        flush_held(1);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&ctl.p_done);
-      // ---- the previous tile's dQ^T partial, while dK/dQ of that tile and dV of this one run
       if constexpr (kDQ) {
-        if (it > 0 && !(ok = read_out_dq(it - 1))) break;
+        if (ok) ok = read_out_dq(nq - 1, g + nq - 1);
       }
-      // ---- phase B: dS^T = P^T * (dP^T - D), to shared memory only
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dp_full, it & 1, p.status, abort));
+      if (ok) {
+        flush_held(0);
+        flush_held(1);
+      }
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.kv_done, ni & 1, p.status, abort));
       if (!ok) break;
-      tc_fence_after();
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int c0 = wg * 64 + ch * 32;
-        float dp[32];
-        tmem_ld32(tmem + lane_off + kColDP + c0, dp);
-        uint32_t dk[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          float2 dd;
-          if constexpr (kDrop) {  // dP of a dropped key is 0; a kept one is scaled
-            const float2 dvec = *reinterpret_cast<const float2*>(vec + BQ + c0 + 2 * u);
-            const uint32_t kb = kbits[ch] >> (2 * u);
-            dd = make_float2((kb & 1u) ? fmaf(dp[2 * u], pv.drop_scale, -dvec.x) : -dvec.x,
-                             (kb & 2u) ? fmaf(dp[2 * u + 1], pv.drop_scale, -dvec.y) : -dvec.y);
-          } else {
-            dd = ffma2(*reinterpret_cast<const float2*>(vec + BQ + c0 + 2 * u), minus1,
-                       make_float2(dp[2 * u], dp[2 * u + 1]));
-          }
-          const float2 ds = fmul2(make_float2(pr[ch * 32 + 2 * u], pr[ch * 32 + 2 * u + 1]), dd);
-          dk[u] = pack_bf16(ds.x, ds.y);
-        }
-        // dS^T row r, query columns c0..c0+31: four 16-byte chunks of a 128-byte swizzled
-        // row (box c0 / 64, chunk (c0 % 64) / 8 + u, XOR (r % 8))
-        uint8_t* atom = dsrow + (c0 / 64) * kBox;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = ((c0 % 64) / 8 + u) ^ (r & 7);
-          *reinterpret_cast<uint4*>(atom + chunk * 16) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-        }
-        if (ch == 0) flush_held(0);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&ctl.ds_done);
-      flush_held(1);
-    }
-    if constexpr (kDQ) {
-      if (ok) ok = read_out_dq(nq - 1);
-    }
-    if (ok) {
-      flush_held(0);
-      flush_held(1);
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.kv_done, 0, p.status, abort));
-    if (ok) {
       // dV and dK of key row r; warpgroup wg writes columns wg*D/2 .. wg*D/2 + D/2 - 1
       tc_fence_after();
       const size_t row = (size_t)krow_base + kt * BN + r;
@@ -680,8 +753,8 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll 1
       for (int c0 = wg * (D / 2); c0 < wg * (D / 2) + D / 2; c0 += 32) {
         float v[32];
-        uint4 w[4];
-        uint32_t* wu = reinterpret_cast<uint32_t*>(w);
+        uint4 wv[4];
+        uint32_t* wu = reinterpret_cast<uint32_t*>(wv);
         tmem_ld32(tmem + lane_off + kColDV + c0, v);
         if constexpr (kDrop) {  // kept weights entered dV unscaled
 #pragma unroll
@@ -693,7 +766,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         uint4* dv = reinterpret_cast<uint4*>(p.dV + row * D + c0);
         if (in) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) dv[u] = w[u];
+          for (int u = 0; u < 4; ++u) dv[u] = wv[u];
         }
         tmem_ld32(tmem + lane_off + kColDK + c0, v);
 #pragma unroll
@@ -701,9 +774,14 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         uint4* dk = reinterpret_cast<uint4*>(p.dK + row * D + c0);
         if (in) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) dk[u] = w[u];
+          for (int u = 0; u < 4; ++u) dk[u] = wv[u];
         }
       }
+      // the next item's dV and dK may overwrite the accumulators
+      tc_fence_before();
+      mbar_arrive(&ctl.acc_empty);
+      g += nq;
+      ++ni;
     }
   }
 
@@ -716,6 +794,19 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Streaming multiprocessors of the current device (looked up once per device).
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 template <int D, int kVar, bool kDQ>
@@ -762,7 +853,9 @@ cudaError_t launch_wide(const void* Q, const void* K, const void* V, const void*
   pv.seed_hi = (uint32_t)(var.seed >> 32);
   pv.drop_tt = var.threshold * 0x01010101u;
   pv.drop_scale = (float)(256.0 / (256.0 - (double)var.threshold));
-  const int64_t grid = (int64_t)p.kvtiles * p.heads;
+  // one CTA per SM (the shared memory allows no second), each running items until none is left
+  const int64_t items = (int64_t)p.kvtiles * p.heads;
+  const int64_t grid = items < sm_count() ? items : sm_count();
   if (s.N % BQ != 0 || s.keys() % BN != 0)
     fa_bwd_wide_kernel<D, true, kVar, kDQ><<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, p, pv);
   else

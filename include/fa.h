@@ -116,7 +116,7 @@ FA_API fa_status_t fa_bwd(const void* Q, const void* K, const void* V, const voi
  *                           128-query tiles recomputes S and dP and accumulates dQ on chip;
  *                           dQ does not depend on the order of any additions.
  *   FA_BWD_DQ_AUTO     (0, the default): the atomic mode, the faster of the two at every
- *                           shape measured on GB300 (the separate pass costs 15-27% more).
+ *                           shape measured on GB300 (the separate pass costs 16-28% more).
  * The setting is process-wide and applies to calls made after it; masked and dropout
  * backward calls always use the atomic mode. fa_set_bwd_dq_mode returns
  * FA_ERR_INVALID_ARG for any other value; fa_get_bwd_dq_mode returns the setting.
