@@ -59,6 +59,8 @@
 // and rows past the end are neither accumulated nor stored.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "fa_internal.h"
 #include "philox.cuh"
 #include "sm100_ptx.cuh"
@@ -798,15 +800,15 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
 // Streaming multiprocessors of the current device (looked up once per device).
 int sm_count() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (!cached[dev]) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 template <int D, int kVar, bool kDQ>
