@@ -8,7 +8,7 @@
 // and O += P V accumulates in TMEM. The 1/sqrt(d) scale and log2(e) are folded into a
 // single multiplier so every exponential is one FFMA + one ex2 (§7, scale folding).
 //
-// CTA = two 128-row Q tiles of one head (rows 256*pair .. +255), 10 warps:
+// CTA = two 128-row Q tiles of one head (rows 256*pair .. +255), 10 warps (11 at d = 64):
 //   warps 0-3  softmax for Q tile 0 (one thread per row = one TMEM lane)
 //   warps 4-7  softmax for Q tile 1
 //   warp 8     TMA producer: Q once, then K_j / V_j into a ring of shared-memory stages
