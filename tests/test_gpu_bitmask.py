@@ -63,6 +63,9 @@ CASES = [  # B, H, N, d, causal, kind
     (1, 4, 1024, 128, True, "random"),
     (2, 2, 640, 128, False, "band"),
     (1, 3, 333, 64, True, "hidden_rows"),
+    # more items than SMs: each persistent backward CTA runs two or three (key tile, head) items
+    (1, 40, 1024, 128, True, "random"),
+    (1, 48, 700, 64, False, "band"),
 ]
 
 

@@ -46,6 +46,9 @@ CASES = [  # B, H, N, d, causal, p, seed
     (1, 3, 200, 128, True, 0.5, 2 ** 40 + 3),
     (2, 2, 1024, 128, True, 0.2, 11),
     (1, 2, 640, 64, False, 0.05, 12345),
+    # more items than SMs: each persistent backward CTA runs two or three (key tile, head) items
+    (1, 40, 1024, 128, True, 0.2, 13),
+    (1, 48, 700, 64, False, 0.1, 14),
 ]
 
 

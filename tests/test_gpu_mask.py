@@ -57,6 +57,9 @@ CASES = [  # B, H, N, d, causal, kind
     (1, 2, 100, 64, False, "bias"),          # rows padded to 104 by padded_mask
     (1, 4, 1024, 128, True, "bias"),
     (2, 2, 640, 128, False, "broadcast"),
+    # more items than SMs: each persistent backward CTA runs two or three (key tile, head) items
+    (1, 40, 1024, 128, True, "bias"),
+    (1, 48, 700, 64, False, "broadcast"),
 ]
 
 
