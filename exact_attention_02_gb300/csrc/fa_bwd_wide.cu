@@ -85,7 +85,7 @@ constexpr uint32_t kTmemCols = 512;
 
 struct WideCtl {
   uint64_t kv_full, q_full[kStages], do_full[kStages], q_empty[kStages], do_empty[kStages];
-  uint64_t s_full, dp_full, p_done, ds_done, dq_full, dq_empty, kv_done, acc_empty, drain;
+  uint64_t s_full, dp_full, p_done, ds_done, dq_full, dq_empty, kv_done, dv_final, acc_empty, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -237,6 +237,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     mbar_init(&ctl.dq_full, 1);
     mbar_init(&ctl.dq_empty, 256);
     mbar_init(&ctl.kv_done, 1);
+    mbar_init(&ctl.dv_final, 1);
     mbar_init(&ctl.acc_empty, 256);
     mbar_init(&ctl.drain, 1);
     ctl.abort = 0;
@@ -431,6 +432,7 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tc_fence_after();
         issue_dV(true, s0);
         mma_commit(&ctl.do_empty[s0]);  // dP(0) and dV(0), the readers of dO(0), issued
+        if (nq == 1) mma_commit(&ctl.dv_final);  // the item's last dV product
         for (int it = 0; ok && it < nq; ++it) {
           const int gi = g + it;
           const int s = gi % kStages, s1 = (gi + 1) % kStages;
@@ -471,12 +473,14 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             tc_fence_after();
             issue_dV(false, s1);
             mma_commit(&ctl.do_empty[s1]);  // dP(i+1) and dV(i+1), the readers of dO(i+1), issued
+            if (it + 2 == nq) mma_commit(&ctl.dv_final);
           } else if (next) {
             // dV(i+1) reads P^T(i+1) from TMEM and dO(i+1) from its stage: both must be in
             if (!(ok = mbar_wait(&ctl.p_done, (gi + 1) & 1, p.status, abort))) break;
             if (!(ok = mbar_wait(&ctl.do_full[s1], par1, p.status, abort))) break;
             tc_fence_after();
             issue_dV(false, s1);
+            if (it + 2 == nq) mma_commit(&ctl.dv_final);
             // dP(i+1) once the softmax warps have read the dQ^T(i) partial out of its columns
             if constexpr (kDQ && !C::kSepDQ) {
               if (!(ok = mbar_wait(&ctl.dq_empty, gi & 1, p.status, abort))) break;
@@ -739,19 +743,13 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         mbar_arrive(&ctl.ds_done);
         flush_held(1);
       }
-      if constexpr (kDQ) {
-        if (ok) ok = read_out_dq(nq - 1, g + nq - 1);
-      }
-      if (ok) {
-        flush_held(0);
-        flush_held(1);
-      }
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.kv_done, ni & 1, p.status, abort));
-      if (!ok) break;
-      // dV and dK of key row r; warpgroup wg writes columns wg*D/2 .. wg*D/2 + D/2 - 1
-      tc_fence_after();
+      // dV is final once the item's last dV product has run (before dK and dQ of the last tile):
+      // store it while those run
       const size_t row = (size_t)krow_base + kt * BN + r;
       const bool in = !kTail || kt * BN + r < p.Nk;  // key rows past the end are not stored
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.dv_final, ni & 1, p.status, abort));
+      if (!ok) break;
+      tc_fence_after();
 #pragma unroll 1
       for (int c0 = wg * (D / 2); c0 < wg * (D / 2) + D / 2; c0 += 32) {
         float v[32];
@@ -770,6 +768,23 @@ fa_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
           for (int u = 0; u < 4; ++u) dv[u] = wv[u];
         }
+      }
+      if constexpr (kDQ) {
+        if (ok) ok = read_out_dq(nq - 1, g + nq - 1);
+      }
+      if (ok) {
+        flush_held(0);
+        flush_held(1);
+      }
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl.kv_done, ni & 1, p.status, abort));
+      if (!ok) break;
+      // dK of key row r; warpgroup wg writes columns wg*D/2 .. wg*D/2 + D/2 - 1
+      tc_fence_after();
+#pragma unroll 1
+      for (int c0 = wg * (D / 2); c0 < wg * (D / 2) + D / 2; c0 += 32) {
+        float v[32];
+        uint4 wv[4];
+        uint32_t* wu = reinterpret_cast<uint32_t*>(wv);
         tmem_ld32(tmem + lane_off + kColDK + c0, v);
 #pragma unroll
         for (int u = 0; u < 16; ++u) wu[u] = pack_bf16(v[2 * u] * p.scale, v[2 * u + 1] * p.scale);
