@@ -42,15 +42,22 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     assert f(*ptrs, 0, 1, 128, 128, 0.088, 1, fa.FA_DTYPE_BF16, None) == fa.FA_ERR_INVALID_ARG
 
 
+NOALLOC_SHAPES = [  # the last two have more (key tile, head) items than a GB300 has SMs
+    Workload("noalloc_b1h4_n1024_d128_bf16_causal", 1, 4, 1024, 128, "bf16", True, seed=21),
+    Workload("noalloc_b1h8_n8192_d128_bf16_causal", 1, 8, 8192, 128, "bf16", True, seed=22),
+    Workload("noalloc_b2h16_n2048_d64_bf16", 2, 16, 2048, 64, "bf16", False, seed=23),
+]
+
+
 @pytest.mark.gpu
-def test_noalloc_matches_fa_bwd_on_consecutive_calls():
+@pytest.mark.parametrize("w", NOALLOC_SHAPES, ids=lambda w: w.name)
+def test_noalloc_matches_fa_bwd_on_consecutive_calls(w):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from exact_attention_02_gb300.build import build
     build()
     f = _noalloc(fa.lib())
-    w = Workload("noalloc_b1h4_n1024_d128_bf16_causal", 1, 4, 1024, 128, "bf16", True, seed=21)
     assert w.B * w.H * w.N * w.d <= 8 * 1024 * 1024
     x = make_inputs(w)
     q, k, v, do = (torch.from_numpy(x[n]).cuda().to(torch.bfloat16) for n in ("q", "k", "v", "do"))
